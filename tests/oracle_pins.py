@@ -1,0 +1,248 @@
+"""Checks that pin the oracle to things other than itself.
+
+Each ``check_*`` raises AssertionError on failure. ``test_oracle_pins.py``
+runs them against the oracle as built; ``test_oracle_mutants.py`` runs them
+against copies of the oracle with a plausible mistake planted, and requires
+every mutant to fail at least one check.
+
+Pins (what fixes the expected value):
+  * fp64 brute force of the materialised (W + s B A) x -- a different
+    association of the same product (ferrox-core weight_matrix/lora.rs test
+    ``dense_delta``, tolerance 1e-4);
+  * worked examples under tests/golden/ (page-printed scale factors; a hand
+    derivation with exact arithmetic);
+  * byte identities the pages state: scale 0 and slot -1 equal the base-only
+    product (ferrox lora.rs module doc, 'Cost when absent'); a fused q/k/v base
+    with one copy of A and split B rows equals the stacked split calls
+    (frink lora_attach.rs module doc); zero-padded rank equals true rank
+    (spark_model lora_delta.rs, LoraPair doc); a batch equals its rows
+    (ferrox test ``batch_delta_is_the_matvec_delta_per_position``);
+  * closed forms: alpha/sqrt(r) = (alpha/r) * sqrt(r) exactly at r = 4, 16, 64;
+    doubling the adapter scale doubles the delta exactly;
+  * numpy's stable argsort for the routing sort.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+import oracle
+import workloads
+from workloads import Adapter, bf16_to_f32, f32_to_bf16
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _bf(a):
+    return f32_to_bf16(np.asarray(a, dtype=np.float32))
+
+
+def _f64(u16):
+    return bf16_to_f32(u16).astype(np.float64)
+
+
+def brute_force_fp64(wl, scales=None) -> np.ndarray:
+    """y = (W + s_i B A) x_i with the delta matrix materialised, in fp64."""
+    W = _f64(wl.W)
+    x = _f64(wl.x)
+    y = np.empty((wl.M, wl.N), dtype=np.float64)
+    for i in range(wl.M):
+        s = int(wl.seq_slot[i])
+        Weff = W
+        if 0 <= s < len(wl.adapters) and wl.adapters[s] is not None:
+            ad = wl.adapters[s]
+            sc = scales[s] if scales is not None else oracle.scale(ad.alpha, ad.rank, ad.use_rslora,
+                                                                     ad.adapter_scale)
+            if sc != 0.0:
+                Weff = W + np.float64(sc) * (_f64(ad.B) @ _f64(ad.A))
+        y[i] = Weff @ x[i]
+    return y
+
+
+def check_scale_examples():
+    with open(os.path.join(GOLDEN, "scale_examples.json")) as f:
+        g = json.load(f)
+    for alpha, rank, rs, asc, want in g["rows"]:
+        got = oracle.scale(alpha, rank, bool(rs), asc)
+        assert abs(got - want) < 1e-7, (alpha, rank, rs, asc, got, want)
+
+
+def check_hand_example():
+    with open(os.path.join(GOLDEN, "hand_example.json")) as f:
+        g = json.load(f)
+    ads = [Adapter(A=_bf(a["A"]), B=_bf(a["B"]), rank=a["rank"], alpha=a["alpha"],
+                   use_rslora=bool(a["use_rslora"]), adapter_scale=a["adapter_scale"])
+           for a in g["adapters"]]
+    y = oracle.proj(_bf(g["x"]), _bf(g["W"]), np.array(g["seq_slot"], np.int32), ads)
+    want = np.array(g["expected_y"], dtype=np.float32)
+    assert np.array_equal(y, want), (y, want)
+
+
+def check_brute_force(wl, tol=1e-4):
+    y = oracle.workload_proj(wl)
+    ref = brute_force_fp64(wl)
+    err = np.abs(y.astype(np.float64) - ref)
+    assert err.max() <= tol * (1.0 + np.abs(ref)).max(), (wl.name, err.max())
+
+
+def check_brute_force_suite():
+    check_brute_force(workloads.make("tiny"))
+    cases = [
+        dict(seed=11, M=5, K=7, N=9, L=3, R=4),
+        dict(seed=12, M=16, K=16, N=16, L=4, R=8, alpha=[0.0, 3.0, 0.0, 5.0]),
+        dict(seed=13, M=9, K=13, N=6, L=2, R=3, rslora=True),
+        dict(seed=14, M=3, K=16, N=11, L=5, R=2, adapter_scales=[0.5, -1.0, 2.0, 0.0, 0.25]),
+        dict(seed=15, M=12, K=1, N=4, L=2, R=1),
+    ]
+    for c in cases:
+        check_brute_force(workloads.random_small(**c))
+
+
+def check_no_delta_rows_are_base_bytes():
+    wl = workloads.make("tiny")
+    y = oracle.workload_proj(wl)
+    base = oracle.proj(wl.x, wl.W, np.full(wl.M, -1, np.int32), wl.adapters)
+    none = wl.seq_slot < 0
+    assert none.any() and (~none).any()
+    assert np.array_equal(y[none].view(np.uint32), base[none].view(np.uint32))
+    # adapted rows differ from base (the delta is really applied)
+    assert not np.array_equal(y[~none], base[~none])
+    # adapter scale 0 (every slot): byte-identical to base
+    zero = [Adapter(a.A, a.B, a.rank, a.alpha, a.use_rslora, 0.0) for a in wl.adapters]
+    y0 = oracle.proj(wl.x, wl.W, wl.seq_slot, zero)
+    assert np.array_equal(y0.view(np.uint32), base.view(np.uint32))
+    # a slot at or past max_loras is treated as no adapter
+    far = wl.seq_slot.copy()
+    far[:] = len(wl.adapters) + 3
+    yf = oracle.proj(wl.x, wl.W, far, wl.adapters)
+    assert np.array_equal(yf.view(np.uint32), base.view(np.uint32))
+    # an empty slot (no pair) is no adapter
+    empty = [None] * len(wl.adapters)
+    ye = oracle.proj(wl.x, wl.W, wl.seq_slot, empty)
+    assert np.array_equal(ye.view(np.uint32), base.view(np.uint32))
+
+
+def check_fused_split_exact(wl=None, rows=None):
+    if wl is None:
+        wl = workloads.random_small(seed=21, M=10, K=24, N=20, L=3, R=4)
+        splits = [12, 4, 4]
+    else:
+        splits = wl.splits
+    fused = oracle.proj(wl.x, wl.W, wl.seq_slot, wl.adapters, rows=rows)
+    parts = []
+    row0 = 0
+    for n in splits:
+        ads = []
+        for a in wl.adapters:
+            if a is None:
+                ads.append(None)
+                continue
+            ads.append(Adapter(a.A, np.ascontiguousarray(a.B[row0:row0 + n]), a.rank, a.alpha,
+                               a.use_rslora, a.adapter_scale))
+        parts.append(oracle.proj(wl.x, np.ascontiguousarray(wl.W[row0:row0 + n]), wl.seq_slot,
+                                 ads, rows=rows))
+        row0 += n
+    stacked = np.concatenate(parts, axis=1)
+    assert np.array_equal(fused.view(np.uint32), stacked.view(np.uint32))
+
+
+def check_rslora_closed_form():
+    for r in (4, 16, 64):
+        wl = workloads.random_small(seed=30 + r, M=6, K=32, N=10, L=2, R=r, ranks=[r, r],
+                                    alpha=[8.0, 3.0])
+        zeroW = np.zeros_like(wl.W)
+        plain = oracle.proj(wl.x, zeroW, wl.seq_slot, wl.adapters)
+        rs = [Adapter(a.A, a.B, a.rank, a.alpha, True, a.adapter_scale) for a in wl.adapters]
+        root = oracle.proj(wl.x, zeroW, wl.seq_slot, rs)
+        k = np.float32(np.sqrt(r))
+        assert np.array_equal(root.view(np.uint32), (plain * k).view(np.uint32)), r
+        assert np.any(plain != 0)
+
+
+def check_zero_padding_exact():
+    wl = workloads.random_small(seed=41, M=8, K=40, N=12, L=3, R=8, ranks=[3, 5, 8])
+    pads = []
+    scales = []
+    for a in wl.adapters:
+        R = 8
+        A = np.zeros((R, wl.K), np.uint16)
+        A[:a.rank] = a.A
+        B = np.zeros((wl.N, R), np.uint16)
+        B[:, :a.rank] = a.B
+        pads.append(Adapter(A, B, R, a.alpha, a.use_rslora, a.adapter_scale))
+        scales.append(oracle.scale(a.alpha, a.rank, a.use_rslora, a.adapter_scale))
+    y_true = oracle.workload_proj(wl)
+    y_pad = oracle.proj(wl.x, wl.W, wl.seq_slot, pads, scales=scales)
+    assert np.array_equal(y_true.view(np.uint32), y_pad.view(np.uint32))
+
+
+def check_linear_in_scale():
+    wl = workloads.random_small(seed=51, M=7, K=20, N=9, L=2, R=4, p_none=0.0)
+    zeroW = np.zeros_like(wl.W)
+    one = oracle.proj(wl.x, zeroW, wl.seq_slot, wl.adapters)
+    dbl = [Adapter(a.A, a.B, a.rank, a.alpha, a.use_rslora, 2.0 * a.adapter_scale)
+           for a in wl.adapters]
+    two = oracle.proj(wl.x, zeroW, wl.seq_slot, dbl)
+    assert np.array_equal(two.view(np.uint32), (one * np.float32(2)).view(np.uint32))
+    assert np.any(one != 0)
+
+
+def check_batch_is_rows():
+    wl = workloads.make("tiny")
+    y = oracle.workload_proj(wl)
+    for i in range(wl.M):
+        yi = oracle.workload_proj(wl, rows=[i])
+        assert np.array_equal(y[i:i + 1].view(np.uint32), yi.view(np.uint32)), i
+    cols = np.array([255, 0, 17, 128], np.int32)
+    yc = oracle.workload_proj(wl, rows=[3, 1], cols=cols)
+    assert np.array_equal(yc.view(np.uint32), y[[3, 1]][:, cols].view(np.uint32))
+
+
+def check_slot_sort():
+    rng = np.random.default_rng(7)
+    for M, L in [(0, 3), (1, 1), (64, 16), (257, 5), (1000, 33)]:
+        s = rng.integers(-3, L + 3, size=M).astype(np.int32)
+        perm, seg = oracle.slot_sort(s, L)
+        key = np.where((s >= 0) & (s < L), s + 1, 0)
+        want = np.argsort(key, kind="stable").astype(np.int32)
+        assert np.array_equal(perm, want)
+        assert np.array_equal(np.sort(perm), np.arange(M))
+        counts = np.bincount(key, minlength=L + 1)
+        assert np.array_equal(np.diff(seg), counts) and seg[0] == 0 and seg[-1] == M
+
+
+def small_moe():
+    return workloads.synth.moe(seed=5, tokens=24, E=3, top_k=2, K=40, N=24, n_adapters=3, rank=4)
+
+
+def check_moe_segments():
+    wl = small_moe()
+    y = oracle.workload_moe(wl)
+    for e in range(wl.E):
+        a, b = int(wl.expert_offsets[e]), int(wl.expert_offsets[e + 1])
+        if a == b:
+            continue
+        seg = oracle.proj(wl.x[a:b], wl.W[e], wl.seq_slot[a:b], wl.adapters[e])
+        assert np.array_equal(y[a:b].view(np.uint32), seg.view(np.uint32)), e
+    perm, seg = oracle.moe_slot_sort(wl.expert_offsets, wl.seq_slot, wl.max_loras)
+    ex = np.repeat(np.arange(wl.E), np.diff(wl.expert_offsets))
+    key = np.where((wl.seq_slot >= 0) & (wl.seq_slot < wl.max_loras), wl.seq_slot + 1, 0)
+    want = np.lexsort((key, ex)).astype(np.int32)  # primary expert, then key, stable
+    assert np.array_equal(perm, want)
+
+
+ALL_CHECKS = [
+    check_scale_examples,
+    check_hand_example,
+    check_brute_force_suite,
+    check_no_delta_rows_are_base_bytes,
+    check_fused_split_exact,
+    check_rslora_closed_form,
+    check_zero_padding_exact,
+    check_linear_in_scale,
+    check_batch_is_rows,
+    check_slot_sort,
+    check_moe_segments,
+]

@@ -1,0 +1,483 @@
+#!/usr/bin/env python3
+"""Benchmark of the multi-adapter LoRA projection on GB300.
+
+One step = one lora_proj_apply (or lora_moe_down_apply) call over one batch:
+the routing sort, the shrink, the base product and the fused expand-fold.
+Default workload: the decode batch (64 rows, W [4096 x 4096] bf16, 16
+adapters of ranks {8,16,32,64} in a rank-64 pool, 10% rows without adapter).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+N > 1 (under torchrun): every rank runs an independent replica on its own GPU
+(the projection shards by rows with no exchange); value = all ranks' rows /
+the slowest rank's time. Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-projection rows/s at 1 GB300; achieved HBM GB/s / tensor TFLOPS vs peak"
+L2_BYTES = 129 * 1024 * 1024
+
+DESCRIBE = {
+    "tiny": "tiny: 8 rows x W[256x256] bf16, 4 adapters r=8 alpha=16",
+    "decode": "decode: 64 rows x W[4096x4096] bf16, 16 adapters r in {8,16,32,64} pool R=64, "
+              "alpha=2r, 10% rows slot -1",
+    "qkv": "fused QKV: 256 rows x W[6144x4096] (q4096+k1024+v1024) bf16, 32 adapters r=16, "
+           "Zipf(1.1) slots, 5% rows -1, adapter scales {0,0.5,1} alpha=32",
+    "prefill": "prefill gate/up: 8192 rows (8 seqs x 1024) x W[14336x4096] bf16, 8 adapters r=64 "
+               "rsLoRA alpha=16",
+    "moe": "MoE down: 8 experts W_e[4096x14336] bf16, 512 tokens top-2 = 1024 slot-rows, "
+           "4 adapters/expert r=16 alpha=32",
+}
+BOUND = {"tiny": "hbm", "decode": "hbm", "qkv": "hbm", "prefill": "tensor", "moe": "hbm"}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained",
+                                                                          d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------
+# algorithmic bytes / flops of one call (true ranks, touched slots only)
+# ----------------------------------------------------------------------------
+
+def _scale_on(ad):
+    if ad is None or ad.adapter_scale == 0.0:
+        return False
+    return True
+
+
+def proj_algorithmic(wl):
+    M, K, N = wl.M, wl.K, wl.N
+    byts = N * K * 2 + M * K * 2 + M * N * 2 + M * 4
+    flops = 2.0 * M * N * K
+    touched = set()
+    for i in range(M):
+        s = int(wl.seq_slot[i])
+        if 0 <= s < wl.max_loras and _scale_on(wl.adapters[s]):
+            r = wl.adapters[s].rank
+            flops += 2.0 * r * (K + N)
+            touched.add(s)
+    for s in touched:
+        r = wl.adapters[s].rank
+        byts += (r * K + N * r) * 2
+    return float(byts), float(flops)
+
+
+def moe_algorithmic(wl):
+    T, K, N = wl.T, wl.K, wl.N
+    byts = T * K * 2 + T * N * 2 + T * 4 + (wl.E + 1) * 4
+    flops = 2.0 * T * N * K
+    for e in range(wl.E):
+        a, b = int(wl.expert_offsets[e]), int(wl.expert_offsets[e + 1])
+        if b > a:
+            byts += N * K * 2
+        touched = set()
+        for j in range(a, b):
+            s = int(wl.seq_slot[j])
+            if 0 <= s < wl.max_loras and _scale_on(wl.adapters[e][s]):
+                flops += 2.0 * wl.adapters[e][s].rank * (K + N)
+                touched.add(s)
+        for s in touched:
+            r = wl.adapters[e][s].rank
+            byts += (r * K + N * r) * 2
+    return float(byts), float(flops)
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ----------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[3:7]):
+                if v.lower() in ("active", "1", "yes"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def source_sha():
+    h = hashlib.sha256()
+    cdir = os.path.join(ROOT, "rank_delta_gb300", "csrc")
+    for f in sorted(os.listdir(cdir)):
+        with open(os.path.join(cdir, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config, kernel):
+    """dram bytes per launch from a committed ncu capture, if the kernels are unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(config)
+    if not ent or ent.get("source_sha") != source_sha() or ent.get("kernel") != kernel:
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ProjSet:
+    """One buffer set: its own copy of W, pool/tables, x, y and workspace."""
+
+    def __init__(self, wl, th, rd, torch):
+        self.x = th.to_device_bf16(wl.x)
+        self.W = th.to_device_bf16(wl.W)
+        self.slots = torch.from_numpy(wl.seq_slot.astype(np.int32)).cuda()
+        self.route = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.K, wl.N)
+        self.route.pack_all(wl.adapters)
+        self.y = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+        self.ws = th.workspace(rd.lora_proj_workspace_bytes(wl.M, self.route.rt))
+        self.bytes = (self.W.numel() * 2 + self.route.pool_bytes + self.x.numel() * 2 +
+                      self.y.numel() * 2)
+
+    def step(self, wl, rd, stream, x=None, slots=None, y=None):
+        x = self.x if x is None else x
+        slots = self.slots if slots is None else slots
+        y = self.y if y is None else y
+        rd.lora_proj_apply(x, x.stride(0), self.W, wl.M, wl.K, wl.N, slots, self.route.rt, y,
+                           y.stride(0), self.ws, self.ws.numel(), stream)
+
+
+class MoeSet:
+    def __init__(self, wl, th, rd, torch):
+        self.x = th.to_device_bf16(wl.x)
+        self.W = [th.to_device_bf16(w) for w in wl.W]
+        self.off = torch.from_numpy(wl.expert_offsets.astype(np.int32)).cuda()
+        self.slots = torch.from_numpy(wl.seq_slot.astype(np.int32)).cuda()
+        self.routes = []
+        for e in range(wl.E):
+            r = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.K, wl.N)
+            r.pack_all(wl.adapters[e])
+            self.routes.append(r)
+        self.rts = [r.rt for r in self.routes]
+        self.y = torch.empty((wl.T, wl.N), dtype=torch.bfloat16, device="cuda")
+        self.ws = th.workspace(rd.lora_moe_workspace_bytes(wl.E, wl.T, self.rts))
+        self.bytes = (sum(w.numel() for w in self.W) * 2 + sum(r.pool_bytes for r in self.routes)
+                      + self.x.numel() * 2 + self.y.numel() * 2)
+
+    def step(self, wl, rd, stream, x=None, slots=None, y=None):
+        x = self.x if x is None else x
+        slots = self.slots if slots is None else slots
+        y = self.y if y is None else y
+        rd.lora_moe_down_apply(x, x.stride(0), self.W, self.off, wl.E, wl.T, wl.K, wl.N, slots,
+                               self.rts, y, y.stride(0), self.ws, self.ws.numel(), stream)
+
+
+LAUNCHES_PER_STEP = 3  # routing sort, shrink, fused base + expand-fold
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import workloads
+    import rank_delta_gb300 as rd
+    from rank_delta_gb300 import build as rdbuild
+    from rank_delta_gb300 import torch_helpers as th
+
+    if rank == 0:
+        rdbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    rd.lib()
+    torch.cuda.set_device(local_rank)
+    wl = workloads.make(args.config)
+    is_moe = args.config == "moe"
+    rows = wl.T if is_moe else wl.M
+    algo_bytes, algo_flops = moe_algorithmic(wl) if is_moe else proj_algorithmic(wl)
+    Set = MoeSet if is_moe else ProjSet
+    first = Set(wl, th, rd, torch)
+    nsets = max(1, int(np.ceil(3 * L2_BYTES / first.bytes)))
+    sets = [first] + [Set(wl, th, rd, torch) for _ in range(nsets - 1)]
+    stream = torch.cuda.current_stream()
+
+    for i in range(args.warmup):
+        sets[i % nsets].step(wl, rd, stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        ev[2 * i].record(stream)
+        sets[i % nsets].step(wl, rd, stream)
+        ev[2 * i + 1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    # keep the same step loop running ~1 s so the clock sampler sees the GPU under load
+    t_keep = time.time()
+    j = 0
+    while time.time() - t_keep < 1.0:
+        for _ in range(50):
+            sets[j % nsets].step(wl, rd, stream)
+            j += 1
+        torch.cuda.synchronize()
+    clk = clocks.stop()
+
+    elapsed_ms = t_start.elapsed_time(t_end)
+    per_call = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = rows * args.steps * world / (elapsed_ms / 1e3)
+    status = rd.lora_status_get(sets[0].ws)
+
+    # end to end through the C ABI: pinned host x / seq_slot in, y out, every step
+    x_h = sets[0].x.cpu().pin_memory()
+    s_h = sets[0].slots.cpu().pin_memory()
+    y_h = torch.empty(sets[0].y.shape, dtype=torch.bfloat16).pin_memory()
+    xs = [torch.empty_like(s.x) for s in sets]
+    ss = [torch.empty_like(s.slots) for s in sets]
+    for i in range(args.warmup):
+        k = i % nsets
+        xs[k].copy_(x_h, non_blocking=True)
+        ss[k].copy_(s_h, non_blocking=True)
+        sets[k].step(wl, rd, stream, x=xs[k], slots=ss[k])
+        y_h.copy_(sets[k].y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        k = i % nsets
+        xs[k].copy_(x_h, non_blocking=True)
+        ss[k].copy_(s_h, non_blocking=True)
+        sets[k].step(wl, rd, stream, x=xs[k], slots=ss[k])
+        y_h.copy_(sets[k].y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = rows * args.steps * world / (e2e_ms / 1e3)
+
+    hbm, tf_burst, tf_sus, peak_kind = load_peaks()
+    avg_call_s = float(np.mean(per_call)) / 1e3
+    bound = BOUND[args.config]
+    if bound == "hbm":
+        achieved = algo_bytes / avg_call_s / 1e9
+        peak, unit = hbm, "GB/s"
+    else:
+        achieved = algo_flops / avg_call_s / 1e12
+        peak, unit = tf_burst, "TFLOP/s"
+    kernel = "tc_kernel" if (is_moe or rows > 16) else "simt_kernel"
+    traffic = recorded_traffic(args.config, kernel)
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
+        "config": {
+            "workload": DESCRIBE[args.config],
+            "rows_per_step": rows,
+            "parallelism": f"replicas x{world} (rows shard, no collective)",
+            "l2": f"rotating {nsets} buffer sets of {first.bytes / 1e6:.1f} MB (>= 3x L2)",
+        },
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "rows/s",
+                "h2d_bytes_per_step": int(x_h.numel() * 2 + s_h.numel() * 4),
+                "d2h_bytes_per_step": int(y_h.numel() * 2)},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "roofline": {
+            "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic,
+            "kernel": f"{kernel} (timed as the whole call: sort + shrink + {kernel})",
+            "algorithmic_bytes_per_call": algo_bytes, "algorithmic_flops_per_call": algo_flops,
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else
+                           "fallback",
+            "call_ms_median": float(np.median(per_call)), "call_ms_min": float(np.min(per_call)),
+        },
+        "status_flags": status,
+    }
+    return out, wl
+
+
+# ----------------------------------------------------------------------------
+# oracle timing (cpu_baseline leg and the reference arm)
+# ----------------------------------------------------------------------------
+
+def oracle_rate(wl, config, budget_s=12.0, cap_s=30.0):
+    """Oracle rows/s on a bounded sample of the workload (whole rows, all columns)."""
+    import oracle
+    oracle.build()
+    is_moe = config == "moe"
+    rows_total = wl.T if is_moe else wl.M
+    fn = oracle.workload_moe if is_moe else oracle.workload_proj
+    # calibrate on a few rows, then size the sample to ~budget_s
+    n0 = min(rows_total, 2)
+    idx = np.arange(n0, dtype=np.int32)
+    t = time.perf_counter()
+    fn(wl, rows=idx)
+    dt = max(time.perf_counter() - t, 1e-6)
+    n = int(min(rows_total, max(n0, budget_s / (dt / n0))))
+    rng = np.random.default_rng(0)
+    idx = np.sort(rng.choice(rows_total, size=n, replace=False)).astype(np.int32)
+    done, t = 0, time.perf_counter()
+    while True:
+        fn(wl, rows=idx)
+        done += n
+        el = time.perf_counter() - t
+        if el >= min(budget_s, cap_s) or el + el / (done / n) > cap_s:
+            break
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    omp = os.environ.get("OMP_NUM_THREADS")
+    threads = int(omp) if omp else cores
+    return {"value": done / el, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {rows_total} rows (all {wl.N} output columns each), "
+                      f"{done // n} pass(es), {el:.1f} s of fp32 C loops"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import workloads
+    wl = workloads.make(args.config)
+    per = []
+    cpu = None
+    for _ in range(args.warmup):
+        pass
+    for _ in range(max(1, args.steps)):
+        cpu = oracle_rate(wl, args.config, budget_s=max(2.0, 60.0 / max(1, args.steps)),
+                          cap_s=max(4.0, 90.0 / max(1, args.steps)))
+        per.append(cpu["value"])
+    value = float(np.median(per))
+    rows = wl.T if args.config == "moe" else wl.M
+    cpu["value"] = value
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": rows / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded)",
+        "config": {"workload": DESCRIBE[args.config], "rows_per_step": rows,
+                   "note": "the reference is the CPU oracle (plain fp32 loops), no reference code "
+                           "exists to install"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="decode", choices=sorted(DESCRIBE))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    out, wl = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = oracle_rate(wl, args.config)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,272 @@
+/*
+ * rank_delta.h -- C ABI of the GB300 multi-adapter LoRA projection.
+ *
+ * One operation, in two shapes:
+ *
+ *   y[i,:] = W x_i + s[slot_i] * B[slot_i] (A[slot_i] x_i)        (lora_proj_apply)
+ *
+ * and the same per slot-row of a mixture-of-experts down projection, with the
+ * expert's own base and adapters (lora_moe_down_apply).
+ *
+ * Sources (page title, section):
+ *   - ferrox-core `weight_matrix/lora.rs`, module doc ("Layouts", "Scale",
+ *     "Cost when absent") and `LoraDelta`: the formula, the layouts
+ *     W [n_out][n_in], A [rank][n_in], B [n_out][rank], the scale rule and the
+ *     rule that a zero scale skips the delta before any arithmetic;
+ *   - spark_model `layers/ops/lora_delta.rs`, `LoraRoute`, `LoraPair`,
+ *     `apply_lora_bgmv`: per-row routing through an i32 seq_slot buffer
+ *     (negative = no delta), [max_loras] device pointer tables a_table/b_table
+ *     (NULL = base only) and an f32 scale_table, the pool padded to max_rank
+ *     with zeros, row strides in elements, and a graph-safe contract (no
+ *     allocation, no synchronisation);
+ *   - metrale `lora/slot_math.rs`, `pool_slot_bytes`, `module_slot_offsets`,
+ *     `scale_table_values`, `build_seq_slot_host`: the pool byte layout (A then
+ *     B per slot, bf16) and the host seq_slot helper.
+ *
+ * Conventions (all entry points):
+ *   - The library allocates nothing. Every buffer is the caller's. Device
+ *     pointers are plain CUDA device addresses; "host" arguments are plain
+ *     host memory. bf16 values are passed as raw 16-bit storage (`uint16_t`).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is
+ *     enqueued on it; the hot-path calls never synchronise the host.
+ *   - Every call returns a lora_status. Host argument errors enqueue
+ *     nothing; lora_last_error() then returns a message naming every
+ *     dimension involved (thread-local, valid until the next call on that
+ *     thread).
+ *   - Device-side anomalies (a seq_slot >= max_loras, an in-kernel wait that
+ *     gave up) never trap: the row takes the no-delta path and a bit is set in
+ *     the workspace status word (lora_status_get).
+ *   - Alignment: x, W and the pool must start on a 16-byte boundary, and
+ *     n_in, max_rank and every x row stride must be multiples of 8
+ *     elements (16 bytes): the kernels stage x and W tiles with the tensor
+ *     memory accelerator, which copies 16-byte granules.
+ */
+#ifndef RANK_DELTA_H
+#define RANK_DELTA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t without requiring the CUDA headers. */
+typedef struct CUstream_st *lora_stream_t;
+
+typedef int lora_status;
+enum {
+    LORA_OK = 0,
+    LORA_ERR_NULL = 1,        /* a required pointer is NULL */
+    LORA_ERR_SHAPE = 2,       /* a dimension, rank or stride does not fit */
+    LORA_ERR_RANGE = 3,       /* a slot or expert index is out of range */
+    LORA_ERR_ALIGN = 4,       /* a pointer or stride breaks the 16-byte rule */
+    LORA_ERR_WORKSPACE = 5,   /* the workspace is smaller than required */
+    LORA_ERR_CUDA = 6,        /* a CUDA runtime call failed (message has the CUDA error) */
+    LORA_ERR_UNSUPPORTED = 7, /* a size beyond what the kernels handle (message says which) */
+    LORA_ERR_NOT_INIT = 8     /* the route was not set up by lora_route_init */
+};
+
+/* Bits of the workspace status word (lora_status_get). */
+enum {
+    LORA_FLAG_SLOT_RANGE = 1u << 0,   /* a seq_slot value >= max_loras was seen; those rows got no delta */
+    LORA_FLAG_WAIT_TIMEOUT = 1u << 1, /* an in-kernel wait gave up; that call's output is not valid */
+    LORA_FLAG_BAD_OFFSETS = 1u << 2   /* expert_offsets not non-decreasing within [0, T]; rows outside skipped */
+};
+
+/* Path selection for lora_proj_apply_ex (lora_proj_apply uses LORA_PATH_AUTO). */
+enum {
+    LORA_PATH_AUTO = 0, /* by row count: CUDA-core GEMV for few rows, tensor cores otherwise */
+    LORA_PATH_SIMT = 1, /* CUDA-core GEMV path (any row count; slow for many rows) */
+    LORA_PATH_TC = 2    /* tcgen05 tensor-core path */
+};
+
+/*
+ * One projection's adapter pool and routing tables (spark_model
+ * `lora_delta.rs`, `LoraRoute`). Filled by lora_route_init; the caller owns
+ * the struct (host memory) and every buffer it points to (device memory).
+ *
+ * pool        max_loras slots of slot_bytes = (max_rank*n_in + n_out*max_rank)*2
+ *             bytes. Slot s starts at pool + s*slot_bytes and holds A as
+ *             [max_rank][n_in] bf16 followed by B as [n_out][max_rank] bf16,
+ *             rows and columns past the adapter's rank zero (metrale
+ *             `slot_math.rs`, `pool_slot_bytes`).
+ * a_table     [max_loras] device pointers to each slot's A, NULL = empty slot.
+ * b_table     [max_loras] device pointers to each slot's B, NULL = empty slot.
+ * scale_table [max_loras] f32 effective scale, read by the kernels at apply
+ *             time; 0 = the delta is skipped.
+ * factor_table[max_loras] f32 alpha factor (alpha/rank, alpha/sqrt(rank), or 1
+ *             when alpha is 0), so that lora_set_scale can rebuild the scale.
+ * rank_table  [max_loras] i32 true rank of each slot (0 = empty).
+ */
+typedef struct lora_route {
+    void *pool;
+    const void **a_table;
+    const void **b_table;
+    float *scale_table;
+    float *factor_table;
+    int32_t *rank_table;
+    int32_t n_in;      /* K */
+    int32_t n_out;     /* N */
+    int32_t max_rank;  /* R: the pool's padded rank */
+    int32_t max_loras; /* L: number of slots */
+    uint64_t magic;    /* set by lora_route_init */
+} lora_route;
+
+/* Bytes of one projection's pool: max_loras * (max_rank*n_in + n_out*max_rank) * 2.
+ * Returns 0 for a non-positive argument. */
+size_t lora_pool_bytes(int max_loras, int max_rank, int n_in, int n_out);
+
+/* Bytes of the device tables of one route (a_table, b_table, scale_table,
+ * factor_table, rank_table, each 256-byte aligned). 0 for max_loras <= 0. */
+size_t lora_route_table_bytes(int max_loras);
+
+/*
+ * Fill `rt` and clear its tables on `stream` (every slot empty).
+ *   pool    device buffer of at least lora_pool_bytes(...) bytes, 16-byte aligned
+ *   tables  device buffer of at least lora_route_table_bytes(max_loras) bytes,
+ *           256-byte aligned
+ * Errors: NULL pointers, non-positive sizes, n_in not a multiple of 8, buffers
+ * too small (message names the sizes), max_loras > 1023, max_rank > 256 or
+ * not a multiple of 8.
+ */
+lora_status lora_route_init(lora_route *rt, void *pool, size_t pool_bytes, void *tables,
+                            size_t table_bytes, int max_loras, int max_rank, int n_in,
+                            int n_out, lora_stream_t stream);
+
+/*
+ * Copy one adapter's pair into `slot` and publish it in the tables
+ * (spark_model `lora_delta.rs`, `LoraPair`: PEFT layout, zero padding to the
+ * pool rank, scale not folded into B).
+ *   A      [rank][n_in] bf16, row-major, host or device memory
+ *   B      [n_out][rank] bf16, row-major, host or device memory
+ *   alpha  the adapter's alpha; 0 means absent (the scale is then the bare
+ *          adapter_scale)
+ *   use_rslora  nonzero: factor alpha/sqrt(rank) instead of alpha/rank
+ *   adapter_scale  runtime multiplier (1 for a plain adapter)
+ * The slot is zeroed first, so pad rows of A and pad columns of B are zero.
+ * scale_table[slot] = adapter_scale * factor, computed in f32 on the host
+ * (ferrox-core `lora.rs`, `LoraDelta::new` and `effective_scale`).
+ * Errors: slot outside [0, max_loras) (message names the range); rank 0 or
+ * rank > max_rank (message names [n_out x n_in], the rank, max_rank and the
+ * element counts A and B must have); NULL A or B.
+ * Stream-ordered: applies enqueued earlier on `stream` see the old contents.
+ */
+lora_status lora_pool_pack(const lora_route *rt, int slot, const void *A, const void *B,
+                           int rank, float alpha, int use_rslora, float adapter_scale,
+                           lora_stream_t stream);
+
+/* Empty `slot` (table entries NULL / 0): its rows get no delta afterwards. */
+lora_status lora_pool_unpack(const lora_route *rt, int slot, lora_stream_t stream);
+
+/*
+ * Set the runtime scale of `slot`: scale_table[slot] = adapter_scale *
+ * factor_table[slot], written by a one-thread kernel on `stream`, so it takes
+ * effect for every apply enqueued after it (ferrox-core `lora.rs`,
+ * `LoraScale`; the scale is read at apply time). An empty slot keeps scale 0.
+ * Errors: slot outside [0, max_loras); the message names the range (frink
+ * `lora_attach.rs`, `set_lora_scales`).
+ */
+lora_status lora_set_scale(const lora_route *rt, int slot, float adapter_scale,
+                           lora_stream_t stream);
+
+/*
+ * Workspace of lora_proj_apply for M rows on route `rt` (device scratch the
+ * caller provides: the routing sort, the shrink work list, the rank-sized h of
+ * every row, handoff counters and the status word). 256-byte aligned
+ * sections; the caller passes a buffer of at least this many bytes, 256-byte
+ * aligned. Returns 0 if rt is NULL or not initialised.
+ */
+size_t lora_proj_workspace_bytes(int M, const lora_route *rt);
+
+/*
+ * y[i, :] = W x_i + s * B_s (A_s x_i), s = seq_slot[i], for i in [0, M)
+ * (spark_model `lora_delta.rs`, `apply_lora_bgmv`; ferrox-core `lora.rs`,
+ * `LoraDelta::add_batch_to`).
+ *   x         device, M rows of n_in bf16, row i at x + i*x_stride (elements)
+ *   W         device, [N][K] bf16 row-major (the base weight, n_out x n_in)
+ *   M, K, N   rows, n_in, n_out; K and N must equal rt->n_in and rt->n_out
+ *   seq_slot  device [M] int32: slot in [0, max_loras) or negative for no delta
+ *   y         device, M rows of N bf16, row i at y + i*y_stride (elements);
+ *             written, not accumulated into
+ *   ws        device workspace of lora_proj_workspace_bytes(M, rt) bytes
+ * A row gets no delta -- its output is exactly the base product rounded to
+ * bf16, byte for byte what an all-(-1) seq_slot gives -- when its slot is
+ * negative, >= max_loras (a status bit is also set), empty, or has scale 0.
+ * Accumulation is fp32; y is rounded once, to nearest even.
+ * M = 0 is a no-op. The call enqueues kernels on `stream` only; it neither
+ * allocates nor synchronises, so it can be captured in a CUDA graph.
+ * Errors: NULL pointers (M > 0), K or N not matching the route, K or x_stride
+ * not a multiple of 8, x_stride < K, y_stride < N, x or W not 16-byte
+ * aligned, ws too small.
+ */
+lora_status lora_proj_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int N,
+                            const int32_t *seq_slot, const lora_route *rt, void *y,
+                            int64_t y_stride, void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/* lora_proj_apply with an explicit path (LORA_PATH_*); results of the two
+ * paths agree within the fp32 accumulation-order tolerance, not bit for bit. */
+lora_status lora_proj_apply_ex(const void *x, int64_t x_stride, const void *W, int M, int K,
+                               int N, const int32_t *seq_slot, const lora_route *rt, void *y,
+                               int64_t y_stride, void *ws, size_t ws_bytes, int path,
+                               lora_stream_t stream);
+
+/* Largest expert count lora_moe_down_apply takes in one call. */
+#define LORA_MAX_EXPERTS 16
+
+/* Workspace of lora_moe_down_apply for T slot-rows over E experts whose
+ * routes are rts[0..E-1] (same n_in, n_out, max_rank and max_loras). */
+size_t lora_moe_workspace_bytes(int E, int T, const lora_route *rts);
+
+/*
+ * Mixture-of-experts down projection with a per-expert LoRA fold
+ * (spark_model `lora_delta.rs`, `LoraKernels`: the down_proj fold keyed on the
+ * expert through device expert_offsets). Slot-row j with
+ * expert_offsets[e] <= j < expert_offsets[e+1] gets
+ *   y[j, :] = W_e x_j + s * B_{e,s} (A_{e,s} x_j),  s = seq_slot[j],
+ * from expert e's route rts[e].
+ *   x               device, T rows of K bf16 grouped by expert, stride x_stride
+ *   W_e             host array [E] of device pointers, each [N][K] bf16
+ *   expert_offsets  device [E+1] int32, non-decreasing, expert_offsets[E] <= T
+ *   seq_slot        device [T] int32
+ *   rts             host array [E] of routes (same K, N, max_rank, max_loras)
+ *   y               device, T rows of N bf16, stride y_stride; rows outside
+ *                   every expert segment are left untouched
+ * E must be in [1, LORA_MAX_EXPERTS]. Same conventions and errors as
+ * lora_proj_apply.
+ */
+lora_status lora_moe_down_apply(const void *x, int64_t x_stride, const void *const *W_e,
+                                const int32_t *expert_offsets, int E, int T, int K, int N,
+                                const int32_t *seq_slot, const lora_route *rts, void *y,
+                                int64_t y_stride, void *ws, size_t ws_bytes,
+                                lora_stream_t stream);
+
+/* Read the status word (LORA_FLAG_* bits) of the most recent call that used
+ * workspace `ws`. Synchronises `stream` (diagnostic, not a hot-path call). */
+lora_status lora_status_get(const void *ws, uint32_t *flags, lora_stream_t stream);
+
+/*
+ * Copy the routing sort of the most recent lora_proj_apply on `ws` to host
+ * memory: perm [M] (row ids grouped by slot, stable: bucket 0 = rows with no
+ * valid slot, then slot 0, 1, ...) and seg_off [max_loras + 2] (bucket starts,
+ * last entry M). Synchronises `stream`. For tests and diagnostics.
+ */
+lora_status lora_proj_routing(const void *ws, int M, int max_loras, int32_t *perm,
+                              int32_t *seg_off, lora_stream_t stream);
+
+/* Message of the last error on this thread ("" after a successful call). */
+const char *lora_last_error(void);
+
+/*
+ * Host helper (metrale `lora/slot_math.rs`, `build_seq_slot_host`): out[i] =
+ * adapter_slots[i] for i < n when it is >= 0, `active` when it is negative;
+ * out[i] = -1 for the padding rows n <= i < padded_n. Requires n <= padded_n.
+ */
+lora_status lora_build_seq_slot(const int32_t *adapter_slots, int n, int padded_n, int active,
+                                int32_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RANK_DELTA_H */

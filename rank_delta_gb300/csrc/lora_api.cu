@@ -1,0 +1,555 @@
+// Host side of the C ABI declared in include/rank_delta.h: argument checks,
+// pool packing, workspace carving, tensor-map encoding and kernel launches.
+// No allocation and no host synchronisation on the apply path.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "lora_internal.cuh"
+
+using namespace rd;
+
+namespace {
+
+constexpr uint64_t ROUTE_MAGIC = 0x6c6f72615f727431ull; // "lora_rt1"
+constexpr int MAX_LORAS = MAX_BUCKETS - 1;
+constexpr int MAX_RANK = 256;
+constexpr int SIMT_MAX_ROWS = 16; // LORA_PATH_AUTO: at most this many rows per segment -> GEMV
+
+thread_local std::string g_err;
+
+lora_status fail(lora_status code, const char *fmt, ...)
+{
+    char buf[1024];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+lora_status ok()
+{
+    g_err.clear();
+    return LORA_OK;
+}
+
+lora_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(LORA_ERR_CUDA, "%s: CUDA error %d (%s)", what, (int)e, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t slot_bytes(int R, int K, int N) { return ((size_t)R * K + (size_t)N * R) * 2; }
+
+struct TableLayout {
+    size_t a, b, scale, factor, rank, total;
+};
+
+TableLayout table_layout(int L)
+{
+    TableLayout t;
+    size_t o = 0;
+    t.a = o;      o = align256(o + sizeof(void *) * (size_t)L);
+    t.b = o;      o = align256(o + sizeof(void *) * (size_t)L);
+    t.scale = o;  o = align256(o + sizeof(float) * (size_t)L);
+    t.factor = o; o = align256(o + sizeof(float) * (size_t)L);
+    t.rank = o;   o = align256(o + sizeof(int32_t) * (size_t)L);
+    t.total = o;
+    return t;
+}
+
+lora_status check_route(const lora_route *rt, const char *who)
+{
+    if (rt == nullptr)
+        return fail(LORA_ERR_NULL, "%s: route is NULL", who);
+    if (rt->magic != ROUTE_MAGIC)
+        return fail(LORA_ERR_NOT_INIT, "%s: route was not set up by lora_route_init", who);
+    return LORA_OK;
+}
+
+// The alpha factor of one adapter, in f32: alpha/rank, alpha/sqrt(rank)
+// under rsLoRA, 1 when alpha is 0 (ferrox-core `weight_matrix/lora.rs`,
+// `LoraDelta::new`; spark_model `lora_delta.rs`, `LoraPair`).
+float alpha_factor(float alpha, int rank, int use_rslora)
+{
+    if (alpha == 0.0f)
+        return 1.0f;
+    return use_rslora ? alpha / sqrtf((float)rank) : alpha / (float)rank;
+}
+
+struct DevInfo {
+    int num_sms = 0;
+};
+
+bool device_info(DevInfo &out)
+{
+    static std::mutex mu;
+    static DevInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return false;
+    std::lock_guard<std::mutex> g(mu);
+    if (cache[dev].num_sms == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return false;
+        cache[dev].num_sms = sms;
+    }
+    out = cache[dev];
+    return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// 2D bf16 map over [rows][inner] (row stride in elements), box inner x box_rows,
+// 128-byte swizzle, zero fill out of bounds.
+bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t stride_elems,
+              uint32_t box_inner, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {stride_elems * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+} // namespace
+
+extern "C" {
+
+const char *lora_last_error(void) { return g_err.c_str(); }
+
+size_t lora_pool_bytes(int max_loras, int max_rank, int n_in, int n_out)
+{
+    if (max_loras <= 0 || max_rank <= 0 || n_in <= 0 || n_out <= 0)
+        return 0;
+    return (size_t)max_loras * slot_bytes(max_rank, n_in, n_out);
+}
+
+size_t lora_route_table_bytes(int max_loras)
+{
+    if (max_loras <= 0)
+        return 0;
+    return table_layout(max_loras).total;
+}
+
+lora_status lora_route_init(lora_route *rt, void *pool, size_t pool_bytes, void *tables,
+                            size_t table_bytes, int max_loras, int max_rank, int n_in, int n_out,
+                            lora_stream_t stream)
+{
+    if (rt == nullptr || pool == nullptr || tables == nullptr)
+        return fail(LORA_ERR_NULL, "lora_route_init: route, pool and tables must be non-NULL");
+    if (max_loras <= 0 || max_rank <= 0 || n_in <= 0 || n_out <= 0)
+        return fail(LORA_ERR_SHAPE,
+                    "lora_route_init: sizes must be positive (max_loras %d, max_rank %d, n_in %d, "
+                    "n_out %d)",
+                    max_loras, max_rank, n_in, n_out);
+    if (max_loras > MAX_LORAS)
+        return fail(LORA_ERR_UNSUPPORTED, "lora_route_init: max_loras %d exceeds %d", max_loras,
+                    MAX_LORAS);
+    if (max_rank > MAX_RANK || max_rank % 8 != 0)
+        return fail(LORA_ERR_UNSUPPORTED,
+                    "lora_route_init: max_rank %d must be a multiple of 8 and at most %d", max_rank,
+                    MAX_RANK);
+    if (n_in % 8 != 0)
+        return fail(LORA_ERR_ALIGN, "lora_route_init: n_in %d must be a multiple of 8", n_in);
+    if (!aligned16(pool))
+        return fail(LORA_ERR_ALIGN, "lora_route_init: pool must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(tables) & 255u) != 0)
+        return fail(LORA_ERR_ALIGN, "lora_route_init: tables must be 256-byte aligned");
+    const size_t need_pool = lora_pool_bytes(max_loras, max_rank, n_in, n_out);
+    const size_t need_tab = lora_route_table_bytes(max_loras);
+    if (pool_bytes < need_pool || table_bytes < need_tab)
+        return fail(LORA_ERR_WORKSPACE,
+                    "lora_route_init: pool has %zu bytes (needs %zu for %d slots of [%d x %d] at "
+                    "max_rank %d), tables have %zu bytes (needs %zu)",
+                    pool_bytes, need_pool, max_loras, n_out, n_in, max_rank, table_bytes, need_tab);
+    const TableLayout tl = table_layout(max_loras);
+    uint8_t *tb = static_cast<uint8_t *>(tables);
+    cudaError_t e = cudaMemsetAsync(tables, 0, tl.total, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lora_route_init: clearing tables");
+    rt->pool = pool;
+    rt->a_table = reinterpret_cast<const void **>(tb + tl.a);
+    rt->b_table = reinterpret_cast<const void **>(tb + tl.b);
+    rt->scale_table = reinterpret_cast<float *>(tb + tl.scale);
+    rt->factor_table = reinterpret_cast<float *>(tb + tl.factor);
+    rt->rank_table = reinterpret_cast<int32_t *>(tb + tl.rank);
+    rt->n_in = n_in;
+    rt->n_out = n_out;
+    rt->max_rank = max_rank;
+    rt->max_loras = max_loras;
+    rt->magic = ROUTE_MAGIC;
+    return ok();
+}
+
+lora_status lora_pool_pack(const lora_route *rt, int slot, const void *A, const void *B, int rank,
+                           float alpha, int use_rslora, float adapter_scale, lora_stream_t stream)
+{
+    lora_status s = check_route(rt, "lora_pool_pack");
+    if (s != LORA_OK)
+        return s;
+    if (slot < 0 || slot >= rt->max_loras)
+        return fail(LORA_ERR_RANGE, "lora_pool_pack: slot %d is out of range: pool has %d slot(s)",
+                    slot, rt->max_loras);
+    if (rank <= 0 || rank > rt->max_rank)
+        return fail(LORA_ERR_SHAPE,
+                    "lora_pool_pack: rank %d does not fit route [n_out %d x n_in %d] with "
+                    "max_rank %d (need 1 <= rank <= max_rank; A holds rank*n_in = %lld values, "
+                    "B n_out*rank = %lld)",
+                    rank, rt->n_out, rt->n_in, rt->max_rank, (long long)rank * rt->n_in,
+                    (long long)rt->n_out * rank);
+    if (A == nullptr || B == nullptr)
+        return fail(LORA_ERR_NULL, "lora_pool_pack: A and B must be non-NULL");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int R = rt->max_rank, K = rt->n_in, N = rt->n_out;
+    uint8_t *base = static_cast<uint8_t *>(rt->pool) + (size_t)slot * slot_bytes(R, K, N);
+    uint16_t *dA = reinterpret_cast<uint16_t *>(base);
+    uint16_t *dB = reinterpret_cast<uint16_t *>(base + (size_t)R * K * 2);
+    // Unpublish first so no apply ordered after this call sees a half-written slot.
+    cudaError_t e = launch_table_set(*rt, slot, nullptr, nullptr, 0, 0.0f, 0.0f, st);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(base, 0, slot_bytes(R, K, N), st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(dA, A, (size_t)rank * K * 2, cudaMemcpyDefault, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(dB, (size_t)R * 2, B, (size_t)rank * 2, (size_t)rank * 2, (size_t)N,
+                              cudaMemcpyDefault, st);
+    const float factor = alpha_factor(alpha, rank, use_rslora);
+    if (e == cudaSuccess)
+        e = launch_table_set(*rt, slot, dA, dB, rank, factor, adapter_scale * factor, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lora_pool_pack");
+    return ok();
+}
+
+lora_status lora_pool_unpack(const lora_route *rt, int slot, lora_stream_t stream)
+{
+    lora_status s = check_route(rt, "lora_pool_unpack");
+    if (s != LORA_OK)
+        return s;
+    if (slot < 0 || slot >= rt->max_loras)
+        return fail(LORA_ERR_RANGE, "lora_pool_unpack: slot %d is out of range: pool has %d slot(s)",
+                    slot, rt->max_loras);
+    cudaError_t e = launch_table_set(*rt, slot, nullptr, nullptr, 0, 0.0f, 0.0f,
+                                     reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lora_pool_unpack");
+    return ok();
+}
+
+lora_status lora_set_scale(const lora_route *rt, int slot, float adapter_scale, lora_stream_t stream)
+{
+    lora_status s = check_route(rt, "lora_set_scale");
+    if (s != LORA_OK)
+        return s;
+    if (slot < 0 || slot >= rt->max_loras)
+        return fail(LORA_ERR_RANGE, "lora_set_scale: slot %d is outside [0, %d)", slot,
+                    rt->max_loras);
+    cudaError_t e = launch_scale_set(*rt, slot, adapter_scale, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lora_set_scale");
+    return ok();
+}
+
+lora_status lora_build_seq_slot(const int32_t *adapter_slots, int n, int padded_n, int active,
+                                int32_t *out)
+{
+    if (n < 0 || padded_n < n)
+        return fail(LORA_ERR_SHAPE, "lora_build_seq_slot: need 0 <= n (%d) <= padded_n (%d)", n,
+                    padded_n);
+    if ((n > 0 && adapter_slots == nullptr) || (padded_n > 0 && out == nullptr))
+        return fail(LORA_ERR_NULL, "lora_build_seq_slot: NULL buffer");
+    for (int i = 0; i < padded_n; ++i)
+        out[i] = i < n ? (adapter_slots[i] >= 0 ? adapter_slots[i] : active) : -1;
+    return ok();
+}
+
+} // extern "C"
+
+namespace {
+
+lora_status carve_ws(void *ws, size_t ws_bytes, int rows, int nb, int R, Ws &out, const char *who)
+{
+    const WsLayout l = ws_layout(rows, nb, R);
+    if (ws == nullptr)
+        return fail(LORA_ERR_NULL, "%s: workspace is NULL", who);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return fail(LORA_ERR_ALIGN, "%s: workspace must be 256-byte aligned", who);
+    if (ws_bytes < l.total)
+        return fail(LORA_ERR_WORKSPACE,
+                    "%s: workspace has %zu bytes, needs %zu (%d rows, %d buckets, max_rank %d)", who,
+                    ws_bytes, l.total, rows, nb, R);
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    out.status = reinterpret_cast<uint32_t *>(b + l.status);
+    out.perm = reinterpret_cast<int32_t *>(b + l.perm);
+    out.seg_off = reinterpret_cast<int32_t *>(b + l.seg_off);
+    out.unit_off = reinterpret_cast<int32_t *>(b + l.unit_off);
+    out.done = reinterpret_cast<int32_t *>(b + l.done);
+    out.h = reinterpret_cast<float *>(b + l.h);
+    return LORA_OK;
+}
+
+Tables tables_of(const lora_route &rt)
+{
+    Tables t;
+    t.a_table = reinterpret_cast<const uint16_t *const *>(rt.a_table);
+    t.b_table = reinterpret_cast<const uint16_t *const *>(rt.b_table);
+    t.scale_table = rt.scale_table;
+    t.rank_table = rt.rank_table;
+    return t;
+}
+
+lora_status check_io(const char *who, const void *x, int64_t x_stride, int rows, int K, int N,
+                     const int32_t *seq_slot, void *y, int64_t y_stride)
+{
+    if (x == nullptr || seq_slot == nullptr || y == nullptr)
+        return fail(LORA_ERR_NULL, "%s: x, seq_slot and y must be non-NULL", who);
+    if (K % 8 != 0)
+        return fail(LORA_ERR_ALIGN, "%s: K %d must be a multiple of 8", who, K);
+    if (x_stride < K || x_stride % 8 != 0)
+        return fail(LORA_ERR_ALIGN, "%s: x_stride %lld must be >= K %d and a multiple of 8", who,
+                    (long long)x_stride, K);
+    if (y_stride < N)
+        return fail(LORA_ERR_SHAPE, "%s: y_stride %lld must be >= N %d", who, (long long)y_stride, N);
+    if (!aligned16(x))
+        return fail(LORA_ERR_ALIGN, "%s: x must be 16-byte aligned", who);
+    (void)rows;
+    return LORA_OK;
+}
+
+// prep (routing sort + work list) -> shrink -> base GEMM with the fused expand.
+lora_status run(const Params &p, int path, int token_tile, cudaStream_t st, const char *who)
+{
+    DevInfo di;
+    if (!device_info(di))
+        return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
+    cudaError_t e = launch_prep(p, st);
+    if (e == cudaSuccess)
+        e = launch_shrink(p, di.num_sms, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, who);
+    if (path == LORA_PATH_SIMT) {
+        e = launch_simt(p, di.num_sms, st);
+    } else {
+        TmapSet maps;
+        memset(&maps, 0, sizeof maps);
+        if (!make_map(&maps.x, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64,
+                      (uint32_t)token_tile))
+            return fail(LORA_ERR_CUDA, "%s: encoding the x tensor map failed", who);
+        for (int q = 0; q < p.E; ++q)
+            if (!make_map(&maps.w[q], p.W[q], (uint64_t)p.K, (uint64_t)p.N, (uint64_t)p.K, 64, 128))
+                return fail(LORA_ERR_CUDA, "%s: encoding the W tensor map of expert %d failed", who, q);
+        e = launch_tc(p, maps, token_tile, st);
+    }
+    if (e != cudaSuccess)
+        return cuda_fail(e, who);
+    return ok();
+}
+
+lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int N,
+                       const int32_t *seq_slot, const lora_route *rt, void *y, int64_t y_stride,
+                       void *ws, size_t ws_bytes, int path, lora_stream_t stream)
+{
+    const char *who = "lora_proj_apply";
+    lora_status s = check_route(rt, who);
+    if (s != LORA_OK)
+        return s;
+    if (M < 0)
+        return fail(LORA_ERR_SHAPE, "%s: M %d is negative", who, M);
+    if (path < LORA_PATH_AUTO || path > LORA_PATH_TC)
+        return fail(LORA_ERR_RANGE, "%s: path %d is not one of LORA_PATH_*", who, path);
+    if (K != rt->n_in || N != rt->n_out)
+        return fail(LORA_ERR_SHAPE,
+                    "%s: x is [M %d][K %d] and W [N %d][K %d], but the route is [n_out %d x n_in %d]",
+                    who, M, K, N, K, rt->n_out, rt->n_in);
+    if (M == 0)
+        return ok();
+    if (W == nullptr)
+        return fail(LORA_ERR_NULL, "%s: W is NULL", who);
+    if (!aligned16(W))
+        return fail(LORA_ERR_ALIGN, "%s: W must be 16-byte aligned", who);
+    if ((s = check_io(who, x, x_stride, M, K, N, seq_slot, y, y_stride)) != LORA_OK)
+        return s;
+    Params p;
+    memset(&p, 0, sizeof p);
+    p.x = static_cast<const uint16_t *>(x);
+    p.x_stride = x_stride;
+    p.y = static_cast<uint16_t *>(y);
+    p.y_stride = y_stride;
+    p.seq_slot = seq_slot;
+    p.expert_offsets = nullptr;
+    p.E = 1;
+    p.rows = M;
+    p.K = K;
+    p.N = N;
+    p.L = rt->max_loras;
+    p.R = rt->max_rank;
+    p.W[0] = static_cast<const uint16_t *>(W);
+    p.tab[0] = tables_of(*rt);
+    if ((s = carve_ws(ws, ws_bytes, M, p.L + 1, p.R, p.ws, who)) != LORA_OK)
+        return s;
+    if (path == LORA_PATH_AUTO)
+        path = M <= SIMT_MAX_ROWS ? LORA_PATH_SIMT : LORA_PATH_TC;
+    return run(p, path, tc_token_tile(M), reinterpret_cast<cudaStream_t>(stream), who);
+}
+
+} // namespace
+
+extern "C" {
+
+size_t lora_proj_workspace_bytes(int M, const lora_route *rt)
+{
+    if (rt == nullptr || rt->magic != ROUTE_MAGIC || M < 0)
+        return 0;
+    return ws_layout(M, rt->max_loras + 1, rt->max_rank).total;
+}
+
+lora_status lora_proj_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int N,
+                            const int32_t *seq_slot, const lora_route *rt, void *y, int64_t y_stride,
+                            void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    return proj_apply(x, x_stride, W, M, K, N, seq_slot, rt, y, y_stride, ws, ws_bytes,
+                      LORA_PATH_AUTO, stream);
+}
+
+lora_status lora_proj_apply_ex(const void *x, int64_t x_stride, const void *W, int M, int K, int N,
+                               const int32_t *seq_slot, const lora_route *rt, void *y,
+                               int64_t y_stride, void *ws, size_t ws_bytes, int path,
+                               lora_stream_t stream)
+{
+    return proj_apply(x, x_stride, W, M, K, N, seq_slot, rt, y, y_stride, ws, ws_bytes, path, stream);
+}
+
+size_t lora_moe_workspace_bytes(int E, int T, const lora_route *rts)
+{
+    if (rts == nullptr || E < 1 || E > MAX_E || T < 0 || rts[0].magic != ROUTE_MAGIC)
+        return 0;
+    return ws_layout(T, E * (rts[0].max_loras + 1), rts[0].max_rank).total;
+}
+
+lora_status lora_moe_down_apply(const void *x, int64_t x_stride, const void *const *W_e,
+                                const int32_t *expert_offsets, int E, int T, int K, int N,
+                                const int32_t *seq_slot, const lora_route *rts, void *y,
+                                int64_t y_stride, void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    const char *who = "lora_moe_down_apply";
+    if (E < 1 || E > MAX_E)
+        return fail(LORA_ERR_UNSUPPORTED, "%s: E %d must be in [1, %d]", who, E, MAX_E);
+    if (rts == nullptr || W_e == nullptr || expert_offsets == nullptr)
+        return fail(LORA_ERR_NULL, "%s: rts, W_e and expert_offsets must be non-NULL", who);
+    for (int q = 0; q < E; ++q) {
+        lora_status s = check_route(&rts[q], who);
+        if (s != LORA_OK)
+            return s;
+        if (rts[q].n_in != K || rts[q].n_out != N || rts[q].max_rank != rts[0].max_rank ||
+            rts[q].max_loras != rts[0].max_loras)
+            return fail(LORA_ERR_SHAPE,
+                        "%s: route of expert %d is [n_out %d x n_in %d] rank %d with %d slots; "
+                        "expected [%d x %d] rank %d with %d slots",
+                        who, q, rts[q].n_out, rts[q].n_in, rts[q].max_rank, rts[q].max_loras, N, K,
+                        rts[0].max_rank, rts[0].max_loras);
+        if (W_e[q] == nullptr)
+            return fail(LORA_ERR_NULL, "%s: W_e[%d] is NULL", who, q);
+        if (!aligned16(W_e[q]))
+            return fail(LORA_ERR_ALIGN, "%s: W_e[%d] must be 16-byte aligned", who, q);
+    }
+    if (T < 0)
+        return fail(LORA_ERR_SHAPE, "%s: T %d is negative", who, T);
+    if (T == 0)
+        return ok();
+    lora_status s = check_io(who, x, x_stride, T, K, N, seq_slot, y, y_stride);
+    if (s != LORA_OK)
+        return s;
+    const int L = rts[0].max_loras, R = rts[0].max_rank;
+    if (E * (L + 1) > MAX_BUCKETS)
+        return fail(LORA_ERR_UNSUPPORTED, "%s: E * (max_loras + 1) = %d exceeds %d", who, E * (L + 1),
+                    MAX_BUCKETS);
+    Params p;
+    memset(&p, 0, sizeof p);
+    p.x = static_cast<const uint16_t *>(x);
+    p.x_stride = x_stride;
+    p.y = static_cast<uint16_t *>(y);
+    p.y_stride = y_stride;
+    p.seq_slot = seq_slot;
+    p.expert_offsets = expert_offsets;
+    p.E = E;
+    p.rows = T;
+    p.K = K;
+    p.N = N;
+    p.L = L;
+    p.R = R;
+    for (int q = 0; q < E; ++q) {
+        p.W[q] = static_cast<const uint16_t *>(W_e[q]);
+        p.tab[q] = tables_of(rts[q]);
+    }
+    if ((s = carve_ws(ws, ws_bytes, T, E * (L + 1), R, p.ws, who)) != LORA_OK)
+        return s;
+    return run(p, LORA_PATH_TC, 256, reinterpret_cast<cudaStream_t>(stream), who);
+}
+
+lora_status lora_status_get(const void *ws, uint32_t *flags, lora_stream_t stream)
+{
+    if (ws == nullptr || flags == nullptr)
+        return fail(LORA_ERR_NULL, "lora_status_get: ws and flags must be non-NULL");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(flags, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lora_status_get");
+    return ok();
+}
+
+lora_status lora_proj_routing(const void *ws, int M, int max_loras, int32_t *perm, int32_t *seg_off,
+                              lora_stream_t stream)
+{
+    if (ws == nullptr || perm == nullptr || seg_off == nullptr)
+        return fail(LORA_ERR_NULL, "lora_proj_routing: ws, perm and seg_off must be non-NULL");
+    if (M < 0 || max_loras <= 0 || max_loras > MAX_LORAS)
+        return fail(LORA_ERR_SHAPE, "lora_proj_routing: M %d / max_loras %d out of range", M,
+                    max_loras);
+    const WsLayout l = ws_layout(M, max_loras + 1, 8);
+    const uint8_t *b = static_cast<const uint8_t *>(ws);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (M > 0)
+        e = cudaMemcpyAsync(perm, b + l.perm, sizeof(int32_t) * (size_t)M, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(seg_off, b + l.seg_off, sizeof(int32_t) * (size_t)(max_loras + 2),
+                            cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "lora_proj_routing");
+    return ok();
+}
+
+} // extern "C"

@@ -1,0 +1,288 @@
+// Routing and shrink kernels of the LoRA projection.
+//
+// prep_kernel   -- one CTA: stable counting sort of rows into (expert, slot)
+//                  buckets (perm / seg_off), the shrink work list (unit_off),
+//                  handoff counters cleared, status word of this call.
+// shrink_kernel -- h_i = A_s x_i for every adapted row, rank-sized, fp32
+//                  (ferrox-core `weight_matrix/lora.rs`, `LoraDelta::project`),
+//                  one work unit = 8 ranks x up to 16 rows of one slot, so each
+//                  slot's A rows are read once per 16 rows, not once per row.
+// table kernels -- stream-ordered writes of one slot's table entries.
+#include "lora_internal.cuh"
+#include "vec.cuh"
+
+namespace rd {
+
+__device__ __forceinline__ int row_bucket(const Params &p, const int *offs, int i)
+{
+    int e = -1;
+    for (int q = 0; q < p.E; ++q)
+        if (offs[q] <= i && i < offs[q + 1]) {
+            e = q;
+            break;
+        }
+    if (e < 0)
+        return -1;
+    int s = p.seq_slot[i];
+    int key = (s >= 0 && s < p.L) ? s + 1 : 0;
+    return e * (p.L + 1) + key;
+}
+
+// Exclusive scan of one value per thread across the 1024-thread block.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += t;
+    }
+    if (lane == 31)
+        warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = warp_tot[lane];
+        int wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int t = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o)
+                wi += t;
+        }
+        warp_tot[lane] = wi - w; // exclusive prefix of warp totals
+        if (lane == 31)
+            warp_tot[32] = wi;
+    }
+    __syncthreads();
+    int r = warp_tot[warp] + incl - v;
+    total = warp_tot[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
+{
+    extern __shared__ int4 prep_smem4[];
+    int *sm = reinterpret_cast<int *>(prep_smem4);
+    const int nb = p.E * (p.L + 1);
+    int *cnt = sm;                                          // [nb]
+    int *base = sm + nb;                                    // [nb]
+    uint16_t *wc = reinterpret_cast<uint16_t *>(sm + 2 * nb); // [32][nb]
+    __shared__ int offs[MAX_E + 1];
+    __shared__ int warp_tot[33];
+    __shared__ uint32_t flags;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0)
+        flags = 0;
+    if (tid <= p.E)
+        offs[tid] = p.expert_offsets ? p.expert_offsets[tid] : (tid == 0 ? 0 : p.rows);
+    for (int b = tid; b < nb; b += PREP_THREADS)
+        cnt[b] = 0;
+    __syncthreads();
+    if (tid == 0) {
+        bool ok = offs[0] >= 0 && offs[p.E] <= p.rows;
+        for (int q = 0; q < p.E; ++q)
+            ok = ok && offs[q] <= offs[q + 1];
+        if (!ok)
+            flags |= LORA_FLAG_BAD_OFFSETS;
+    }
+    __syncthreads();
+
+    // Pass 1: bucket sizes.
+    for (int i = tid; i < p.rows; i += PREP_THREADS) {
+        int b = row_bucket(p, offs, i);
+        if (b >= 0) {
+            atomicAdd(&cnt[b], 1);
+            if (p.seq_slot[i] >= p.L)
+                atomicOr(&flags, (uint32_t)LORA_FLAG_SLOT_RANGE);
+        }
+    }
+    __syncthreads();
+    {
+        int v = tid < nb ? cnt[tid] : 0, total;
+        int ex = block_exclusive_scan(v, warp_tot, total);
+        if (tid < nb) {
+            base[tid] = ex;
+            p.ws.seg_off[tid] = ex;
+        }
+        if (tid == 0)
+            p.ws.seg_off[nb] = total;
+    }
+    __syncthreads();
+
+    // Pass 2: stable placement, 1024 rows at a time in input order. Inside a
+    // chunk, a row's position among equal keys = (rows of earlier warps with
+    // that key) + (earlier lanes of its own warp with that key).
+    for (int c0 = 0; c0 < p.rows; c0 += PREP_THREADS) {
+        for (int q = tid; q < 32 * nb; q += PREP_THREADS)
+            wc[q] = 0;
+        __syncthreads();
+        const int i = c0 + tid;
+        const int b = i < p.rows ? row_bucket(p, offs, i) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, b);
+        const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
+        if (b >= 0 && rank_in_warp == 0)
+            wc[warp * nb + b] = (uint16_t)__popc(peers);
+        __syncthreads();
+        for (int bb = tid; bb < nb; bb += PREP_THREADS) {
+            int run = 0;
+            for (int w = 0; w < 32; ++w) {
+                int v = wc[w * nb + bb];
+                wc[w * nb + bb] = (uint16_t)run;
+                run += v;
+            }
+            cnt[bb] = run; // this chunk's rows of bucket bb
+        }
+        __syncthreads();
+        if (b >= 0)
+            p.ws.perm[base[b] + wc[warp * nb + b] + rank_in_warp] = i;
+        __syncthreads();
+        for (int bb = tid; bb < nb; bb += PREP_THREADS)
+            base[bb] += cnt[bb];
+        __syncthreads();
+    }
+
+    // Shrink work list: units of (8 ranks) x (16 rows) per adapted bucket.
+    {
+        int units = 0;
+        if (tid < nb) {
+            const int e = tid / (p.L + 1), key = tid % (p.L + 1);
+            if (key > 0) {
+                const int s = key - 1;
+                const Tables &t = p.tab[e];
+                const int rk = t.rank_table[s];
+                const bool active = t.a_table[s] != nullptr && t.b_table[s] != nullptr &&
+                                    t.scale_table[s] != 0.0f && rk > 0;
+                const int rows_b = p.ws.seg_off[tid + 1] - p.ws.seg_off[tid];
+                if (active && rows_b > 0)
+                    units = ((rk + SHRINK_RG - 1) / SHRINK_RG) * ((rows_b + SHRINK_TC - 1) / SHRINK_TC);
+            }
+            p.ws.done[tid] = 0;
+        }
+        int total;
+        int ex = block_exclusive_scan(units, warp_tot, total);
+        if (tid < nb)
+            p.ws.unit_off[tid] = ex;
+        if (tid == 0) {
+            p.ws.unit_off[nb] = total;
+            *p.ws.status = flags;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) shrink_kernel(Params p)
+{
+    const int nb = p.E * (p.L + 1);
+    const int total = p.ws.unit_off[nb];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        int lo = 0, hi = nb;
+        while (hi - lo > 1) {
+            int mid = (lo + hi) >> 1;
+            if (p.ws.unit_off[mid] <= u)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int b = lo;
+        const int e = b / (p.L + 1), s = b % (p.L + 1) - 1;
+        const Tables &t = p.tab[e];
+        const int rk = t.rank_table[s];
+        const int nrg = (rk + SHRINK_RG - 1) / SHRINK_RG;
+        const int local = u - p.ws.unit_off[b];
+        const int rg = local % nrg, tc = local / nrg;
+        const int r0 = p.ws.seg_off[b] + tc * SHRINK_TC;
+        const int nrows = min(SHRINK_TC, p.ws.seg_off[b + 1] - r0);
+        const int r = rg * SHRINK_RG + warp;
+        int row[SHRINK_TC];
+#pragma unroll
+        for (int j = 0; j < SHRINK_TC; ++j)
+            row[j] = p.ws.perm[r0 + min(j, nrows - 1)];
+        float acc[SHRINK_TC];
+#pragma unroll
+        for (int j = 0; j < SHRINK_TC; ++j)
+            acc[j] = 0.0f;
+        if (r < rk) {
+            const uint16_t *arow = t.a_table[s] + (size_t)r * p.K;
+            for (int k0 = lane * 8; k0 < p.K; k0 += 256) {
+                const uint4 a8 = ld_nc_16(arow + k0);
+#pragma unroll
+                for (int j = 0; j < SHRINK_TC; ++j)
+                    if (j < nrows)
+                        acc[j] = dot8_acc(acc[j], a8, ld_16(p.x + (int64_t)row[j] * p.x_stride + k0));
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < SHRINK_TC; ++j)
+            acc[j] = warp_sum(acc[j]);
+        // ranks past the adapter's rank, up to the next multiple of 8, are
+        // written as zero so the expand can run in 8-wide vectors
+        if (lane < nrows) {
+            float v = 0.0f;
+#pragma unroll
+            for (int j = 0; j < SHRINK_TC; ++j)
+                if (j == lane)
+                    v = acc[j];
+            p.ws.h[(size_t)row[lane] * p.R + r] = (r < rk) ? v : 0.0f;
+        }
+    }
+}
+
+cudaError_t launch_prep(const Params &p, cudaStream_t st)
+{
+    const int nb = p.E * (p.L + 1);
+    const size_t smem = (size_t)nb * 8 + (size_t)32 * nb * 2;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)((size_t)MAX_BUCKETS * 8 + (size_t)32 * MAX_BUCKETS * 2));
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    prep_kernel<<<1, PREP_THREADS, smem, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st)
+{
+    shrink_kernel<<<2 * num_sms, 256, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- table writes
+__global__ void table_set_kernel(const void **a_table, const void **b_table, float *scale_table,
+                                 float *factor_table, int32_t *rank_table, int slot, const void *a,
+                                 const void *b, int rank, float factor, float scale)
+{
+    a_table[slot] = a;
+    b_table[slot] = b;
+    rank_table[slot] = rank;
+    factor_table[slot] = factor;
+    scale_table[slot] = scale;
+}
+
+__global__ void scale_set_kernel(float *scale_table, const float *factor_table, int slot,
+                                 float adapter_scale)
+{
+    scale_table[slot] = adapter_scale * factor_table[slot];
+}
+
+cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, const void *b, int rank,
+                             float factor, float scale, cudaStream_t st)
+{
+    table_set_kernel<<<1, 1, 0, st>>>(rt.a_table, rt.b_table, rt.scale_table, rt.factor_table,
+                                      rt.rank_table, slot, a, b, rank, factor, scale);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st)
+{
+    scale_set_kernel<<<1, 1, 0, st>>>(rt.scale_table, rt.factor_table, slot, adapter_scale);
+    return cudaGetLastError();
+}
+
+} // namespace rd

@@ -1,0 +1,149 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared
+symbol, sizes follow the pool layout, and host argument errors are refused
+with messages naming the dimensions -- before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import rank_delta_gb300 as rd
+from rank_delta_gb300 import build as rdbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rank_delta.h")
+MAGIC = 0x6C6F72615F727431  # the value lora_route_init stamps into a route
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    rdbuild.build()
+    return rd.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(lora_[a-z_0-9]+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 15, names
+    lib = ctypes.CDLL(rd.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(rd.exported_symbols()) == names
+
+
+def test_pool_bytes_layout():
+    # slot = A [R][K] then B [N][R], bf16
+    assert rd.lora_pool_bytes(16, 64, 4096, 4096) == 16 * (64 * 4096 + 4096 * 64) * 2
+    assert rd.lora_pool_bytes(32, 16, 4096, 6144) == 32 * (16 * 4096 + 6144 * 16) * 2
+    assert rd.lora_pool_bytes(0, 64, 4096, 4096) == 0
+    assert rd.lora_route_table_bytes(16) >= 16 * (8 + 8 + 4 + 4 + 4)
+    assert rd.lora_route_table_bytes(0) == 0
+
+
+def fake_route(L=4, R=8, K=256, N=256):
+    rt = rd.lora_route()
+    rt.pool = rt.a_table = rt.b_table = rt.scale_table = rt.factor_table = rt.rank_table = 256
+    rt.n_in, rt.n_out, rt.max_rank, rt.max_loras, rt.magic = K, N, R, L, MAGIC
+    return rt
+
+
+def expect(code, fn, *args, contains=()):
+    with pytest.raises(rd.LoraError) as ei:
+        fn(*args)
+    assert ei.value.code == code, ei.value
+    for c in contains:
+        assert c in ei.value.message, ei.value.message
+    return ei.value.message
+
+
+def test_route_init_refusals():
+    rt = rd.lora_route()
+    expect(rd.LORA_ERR_NULL, rd.lora_route_init, rt, 0, 0, 0, 0, 4, 8, 256, 256)
+    expect(rd.LORA_ERR_SHAPE, rd.lora_route_init, rt, 256, 1 << 20, 256, 4096, 0, 8, 256, 256)
+    expect(rd.LORA_ERR_UNSUPPORTED, rd.lora_route_init, rt, 256, 1 << 30, 256, 1 << 20, 4, 12, 256, 256,
+           contains=("max_rank 12",))
+    expect(rd.LORA_ERR_ALIGN, rd.lora_route_init, rt, 256, 1 << 30, 256, 1 << 20, 4, 8, 250, 256)
+    msg = expect(rd.LORA_ERR_WORKSPACE, rd.lora_route_init, rt, 256, 100, 256, 1 << 20, 4, 8, 256, 256)
+    assert "4 slots" in msg and "[256 x 256]" in msg
+
+
+def test_uninitialised_route_is_refused():
+    rt = rd.lora_route()
+    expect(rd.LORA_ERR_NOT_INIT, rd.lora_set_scale, rt, 0, 1.0)
+    expect(rd.LORA_ERR_NOT_INIT, rd.lora_pool_unpack, rt, 0)
+
+
+def test_pack_refuses_bad_rank_naming_every_dimension():
+    rt = fake_route(L=4, R=8, K=256, N=128)
+    A = np.zeros((16, 256), np.uint16)
+    B = np.zeros((128, 16), np.uint16)
+    msg = expect(rd.LORA_ERR_SHAPE, rd.lora_pool_pack, rt, 0, A, B, 16, 1.0, False, 1.0)
+    for part in ("rank 16", "n_out 128", "n_in 256", "max_rank 8", "4096", "2048"):
+        assert part in msg, (part, msg)
+    expect(rd.LORA_ERR_SHAPE, rd.lora_pool_pack, rt, 0, A, B, 0, 1.0, False, 1.0)
+
+
+def test_slot_out_of_range_names_the_range():
+    rt = fake_route(L=4)
+    A = np.zeros((8, 256), np.uint16)
+    B = np.zeros((256, 8), np.uint16)
+    expect(rd.LORA_ERR_RANGE, rd.lora_pool_pack, rt, 4, A, B, 8, 1.0, False, 1.0,
+           contains=("slot 4", "4 slot"))
+    expect(rd.LORA_ERR_RANGE, rd.lora_set_scale, rt, 7, 1.0, contains=("slot 7", "[0, 4)"))
+    expect(rd.LORA_ERR_RANGE, rd.lora_set_scale, rt, -1, 1.0)
+    expect(rd.LORA_ERR_RANGE, rd.lora_pool_unpack, rt, 9)
+
+
+def test_apply_argument_checks():
+    rt = fake_route(L=4, R=8, K=256, N=256)
+    ws_need = rd.lora_proj_workspace_bytes(8, rt)
+    assert ws_need > 0
+    good = dict(x=4096, x_stride=256, W=8192, M=8, K=256, N=256, seq_slot=4096, rt=rt, y=4096,
+                y_stride=256, ws=1 << 20, ws_bytes=ws_need)
+
+    def call(**kw):
+        a = dict(good, **kw)
+        return lambda: rd.lora_proj_apply(a["x"], a["x_stride"], a["W"], a["M"], a["K"], a["N"], a["seq_slot"],
+                           a["rt"], a["y"], a["y_stride"], a["ws"], a["ws_bytes"])
+
+    expect(rd.LORA_ERR_SHAPE, call(K=512), contains=("K 512", "n_in 256"))
+    expect(rd.LORA_ERR_NULL, call(x=0))
+    expect(rd.LORA_ERR_NULL, call(W=0))
+    expect(rd.LORA_ERR_ALIGN, call(x=4098))
+    expect(rd.LORA_ERR_ALIGN, call(x_stride=260))
+    expect(rd.LORA_ERR_SHAPE, call(y_stride=100))
+    expect(rd.LORA_ERR_WORKSPACE, call(ws_bytes=ws_need - 1))
+    expect(rd.LORA_ERR_ALIGN, call(ws=(1 << 20) + 16))
+    expect(rd.LORA_ERR_RANGE, lambda: rd.lora_proj_apply(4096, 256, 8192, 8, 256, 256, 4096, rt,
+                                                         4096, 256, 1 << 20, ws_need, path=9))
+    # M = 0 is a no-op that launches nothing
+    rd.lora_proj_apply(0, 256, 0, 0, 256, 256, 0, rt, 0, 256, 0, 0)
+
+
+def test_moe_argument_checks():
+    rts = [fake_route(L=4, R=16, K=512, N=256) for _ in range(3)]
+    need = rd.lora_moe_workspace_bytes(3, 100, rts)
+    assert need > 0
+    expect(rd.LORA_ERR_UNSUPPORTED, rd.lora_moe_down_apply, 4096, 512, [8192] * 17, 4096, 17, 100,
+           512, 256, 4096, [fake_route(L=4, R=16, K=512, N=256)] * 17, 4096, 256, 1 << 20, need)
+    bad = [fake_route(L=4, R=16, K=512, N=256), fake_route(L=4, R=8, K=512, N=256),
+           fake_route(L=4, R=16, K=512, N=256)]
+    expect(rd.LORA_ERR_SHAPE, rd.lora_moe_down_apply, 4096, 512, [8192] * 3, 4096, 3, 100, 512, 256,
+           4096, bad, 4096, 256, 1 << 20, need, contains=("expert 1",))
+    expect(rd.LORA_ERR_NULL, rd.lora_moe_down_apply, 4096, 512, [8192, 0, 8192], 4096, 3, 100, 512,
+           256, 4096, rts, 4096, 256, 1 << 20, need, contains=("W_e[1]",))
+
+
+def test_build_seq_slot_host_helper():
+    # metrale lora/slot_math.rs build_seq_slot_host: negative -> active; padding -> -1
+    out = rd.lora_build_seq_slot([3, -1, 0, -5], 6, 2)
+    assert out.tolist() == [3, 2, 0, 2, -1, -1]
+    assert rd.lora_build_seq_slot([], 3, 1).tolist() == [-1, -1, -1]
+    expect(rd.LORA_ERR_SHAPE, rd.lora_build_seq_slot, [1, 2, 3], 2, 0)

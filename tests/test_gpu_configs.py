@@ -1,0 +1,145 @@
+"""The full-size workloads through the C ABI in the launch configuration the
+bench times, checked against the oracle on sampled rows (every output column
+of each sampled row) and on properties that hold at any size (GPU only)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rank_delta_gb300 as rd
+import workloads
+from rank_delta_gb300 import build as rdbuild
+from rank_delta_gb300 import torch_helpers as th
+from tests.gpu_common import SENTINEL, ProjRun, assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    rdbuild.build()
+    assert torch.cuda.is_available()
+    return rd.lib()
+
+
+def sample_rows(seq_slot, per_slot=2, extra=8, seed=0):
+    """Some rows of every slot (and of the no-delta rows), plus random ones."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    for s in np.unique(seq_slot):
+        idx = np.where(seq_slot == s)[0]
+        rows += list(rng.choice(idx, size=min(per_slot, idx.size), replace=False))
+    rows += list(rng.integers(0, seq_slot.shape[0], size=extra))
+    return np.array(sorted(set(int(r) for r in rows)), dtype=np.int32)
+
+
+@pytest.fixture(scope="module")
+def qkv():
+    return ProjRun(workloads.make("qkv"))
+
+
+def test_qkv_matches_oracle_on_sampled_rows(qkv):
+    y = qkv.apply()
+    assert qkv.last_status == 0
+    rows = sample_rows(qkv.wl.seq_slot, per_slot=1, extra=8)
+    assert_close(y[rows], oracle.workload_proj(qkv.wl, rows=rows), "qkv")
+
+
+def test_qkv_fused_equals_three_split_calls(qkv):
+    """One A per adapter, B rows split q/k/v: the fused call's bytes equal the
+    stacked split calls' bytes (frink lora_attach.rs module doc)."""
+    wl = qkv.wl
+    fused = qkv.apply()
+    parts = []
+    row0 = 0
+    for n in wl.splits:
+        sub = workloads.ProjWorkload(
+            f"qkv{row0}", wl.seed, wl.M, wl.K, n, wl.max_loras, wl.max_rank,
+            np.ascontiguousarray(wl.W[row0:row0 + n]), wl.x, wl.seq_slot,
+            [workloads.Adapter(a.A, np.ascontiguousarray(a.B[row0:row0 + n]), a.rank, a.alpha,
+                               a.use_rslora, a.adapter_scale) for a in wl.adapters])
+        parts.append(ProjRun(sub).apply())
+        row0 += n
+    assert np.array_equal(fused, np.concatenate(parts, axis=1))
+
+
+def test_qkv_no_delta_rows_are_base_bytes(qkv):
+    wl = qkv.wl
+    y = qkv.apply()
+    base = qkv.apply(slots=torch.full_like(qkv.slots, -1))
+    scales = np.array([oracle.scale(a.alpha, a.rank, a.use_rslora, a.adapter_scale)
+                       for a in wl.adapters])
+    none = (wl.seq_slot < 0) | (scales[np.maximum(wl.seq_slot, 0)] == 0.0)
+    assert none.sum() > int((wl.seq_slot < 0).sum())  # includes zero-scale adapters
+    assert np.array_equal(y[none], base[none])
+
+
+def test_prefill_matches_oracle_on_sampled_rows():
+    run = ProjRun(workloads.make("prefill"))
+    y = run.apply()
+    assert run.last_status == 0
+    wl = run.wl
+    rows = sample_rows(wl.seq_slot, per_slot=2, extra=4, seed=1)
+    assert_close(y[rows], oracle.workload_proj(wl, rows=rows), "prefill")
+    # every output written (the sentinel is NaN)
+    assert np.isfinite(th.bf16_bits_to_f32(y[::97])).all()
+    perm, seg = rd.lora_proj_routing(run.ws, wl.M, wl.max_loras)
+    operm, oseg = oracle.slot_sort(wl.seq_slot, wl.max_loras)
+    assert np.array_equal(perm, operm) and np.array_equal(seg, oseg)
+
+
+class MoeRun:
+    def __init__(self, wl, device="cuda"):
+        self.wl = wl
+        self.x = th.to_device_bf16(wl.x, device)
+        self.W = [th.to_device_bf16(w, device) for w in wl.W]
+        self.off = torch.from_numpy(wl.expert_offsets.astype(np.int32)).to(device)
+        self.slots = torch.from_numpy(wl.seq_slot.astype(np.int32)).to(device)
+        self.routes = []
+        for e in range(wl.E):
+            r = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.K, wl.N, device)
+            r.pack_all(wl.adapters[e])
+            self.routes.append(r)
+        self.rts = [r.rt for r in self.routes]
+        self.ws = th.workspace(rd.lora_moe_workspace_bytes(wl.E, wl.T, self.rts), device)
+
+    def apply(self, slots=None, off=None):
+        wl = self.wl
+        y = torch.empty((wl.T, wl.N), dtype=torch.int16, device="cuda")
+        y.fill_(SENTINEL)
+        y = y.view(torch.bfloat16)
+        rd.lora_moe_down_apply(self.x, self.x.stride(0), self.W, self.off if off is None else off,
+                               wl.E, wl.T, wl.K, wl.N, self.slots if slots is None else slots,
+                               self.rts, y, y.stride(0), self.ws, self.ws.numel())
+        torch.cuda.synchronize()
+        self.last_status = rd.lora_status_get(self.ws)
+        return th.to_numpy_bf16(y)
+
+
+def test_moe_matches_oracle_on_sampled_rows():
+    run = MoeRun(workloads.make("moe"))
+    y = run.apply()
+    assert run.last_status == 0
+    wl = run.wl
+    ex = np.repeat(np.arange(wl.E), np.diff(wl.expert_offsets))
+    rows = sample_rows(ex * 10 + (wl.seq_slot + 1), per_slot=1, extra=4, seed=2)
+    assert_close(y[rows], oracle.workload_moe(wl, rows=rows), "moe")
+    base = run.apply(slots=torch.full_like(run.slots, -1))
+    none = wl.seq_slot < 0
+    assert np.array_equal(y[none], base[none])
+
+
+def test_small_moe_matches_oracle_everywhere():
+    wl = workloads.synth.moe(seed=9, tokens=96, E=5, top_k=2, K=256, N=192, n_adapters=3, rank=8)
+    run = MoeRun(wl)
+    y = run.apply()
+    assert run.last_status == 0
+    assert_close(y, oracle.workload_moe(wl), "small moe")
+
+
+def test_moe_bad_offsets_are_flagged():
+    wl = workloads.synth.moe(seed=10, tokens=32, E=3, top_k=2, K=64, N=64, n_adapters=2, rank=8)
+    run = MoeRun(wl)
+    bad = torch.tensor([0, 40, 20, 64], dtype=torch.int32, device="cuda")
+    run.apply(off=bad)
+    assert run.last_status & rd.LORA_FLAG_BAD_OFFSETS

@@ -211,6 +211,33 @@ lora_status lora_proj_apply_ex(const void *x, int64_t x_stride, const void *W, i
                                int64_t y_stride, void *ws, size_t ws_bytes, int path,
                                lora_stream_t stream);
 
+/*
+ * Bytes of the scratch array built into the library for
+ * lora_proj_apply_static_ws (held on every GPU that loads the library).
+ */
+#define LORA_STATIC_WS_BYTES (4u << 20)
+
+/*
+ * lora_proj_apply for callers that cannot allocate device memory -- for
+ * example a plugin whose host framework owns all device memory and offers no
+ * allocator, or a service that must not grow device memory after start-up.
+ * The pages have no counterpart: it exists for those callers only.
+ *
+ * Same arguments, results and argument errors as lora_proj_apply, without
+ * the workspace: the kernels use a fixed LORA_STATIC_WS_BYTES array compiled
+ * into the library instead, and nothing is allocated. Calls whose workspace
+ * need (lora_proj_workspace_bytes(M, rt)) exceeds LORA_STATIC_WS_BYTES are
+ * refused with LORA_ERR_UNSUPPORTED and a message giving both sizes.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture. All calls
+ * on a device share the array: calls that can overlap on the GPU race, so
+ * order them (one stream). Its status word is not readable through
+ * lora_status_get.
+ */
+lora_status lora_proj_apply_static_ws(const void *x, int64_t x_stride, const void *W, int M, int K,
+                                      int N, const int32_t *seq_slot, const lora_route *rt,
+                                      void *y, int64_t y_stride, lora_stream_t stream);
+
 /* Largest expert count lora_moe_down_apply takes in one call. */
 #define LORA_MAX_EXPERTS 16
 

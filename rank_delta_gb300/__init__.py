@@ -35,6 +35,7 @@ LORA_PATH_SIMT = 1
 LORA_PATH_TC = 2
 
 LORA_MAX_EXPERTS = 16
+LORA_STATIC_WS_BYTES = 4 << 20
 
 
 class LoraError(RuntimeError):
@@ -80,6 +81,7 @@ _SIGNATURES = {
     "lora_proj_apply": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_proj_apply_ex": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _i,
                                 _vp]),
+    "lora_proj_apply_static_ws": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp]),
     "lora_moe_workspace_bytes": (_sz, [_i, _i, _rtp]),
     "lora_moe_down_apply": (_i, [_vp, _i64, ctypes.POINTER(_vp), _vp, _i, _i, _i, _i, _vp, _rtp,
                                  _vp, _i64, _vp, _sz, _vp]),
@@ -183,6 +185,14 @@ def lora_proj_apply(x, x_stride: int, W, M: int, K: int, N: int, seq_slot, rt: l
                                         ctypes.byref(rt), _ptr(y), y_stride, _ptr(ws), ws_bytes,
                                         path, _stream(stream))
     _check(code)
+
+
+def lora_proj_apply_static_ws(x, x_stride: int, W, M: int, K: int, N: int, seq_slot,
+                              rt: lora_route, y, y_stride: int, stream=None) -> None:
+    """lora_proj_apply without a workspace argument, for callers that cannot
+    allocate device memory: the library's built-in scratch array is used."""
+    _check(lib().lora_proj_apply_static_ws(_ptr(x), x_stride, _ptr(W), M, K, N, _ptr(seq_slot),
+                                           ctypes.byref(rt), _ptr(y), y_stride, _stream(stream)))
 
 
 def lora_moe_workspace_bytes(E: int, T: int, rts) -> int:

@@ -142,6 +142,10 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, u
 
 } // namespace
 
+namespace rd {
+lora_status api_fail(lora_status code, const char *msg) { return fail(code, "%s", msg); }
+} // namespace rd
+
 extern "C" {
 
 const char *lora_last_error(void) { return g_err.c_str(); }

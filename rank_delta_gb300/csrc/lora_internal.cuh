@@ -107,6 +107,9 @@ cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, cons
                              int rank, float factor, float scale, cudaStream_t st);
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st);
 
+// Record `msg` as the thread's last error and return `code` (lora_api.cu).
+lora_status api_fail(lora_status code, const char *msg);
+
 // The token-tile sizes the tensor-core kernel is built for.
 inline int tc_token_tile(int rows_per_segment)
 {

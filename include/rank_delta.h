@@ -215,7 +215,7 @@ lora_status lora_proj_apply_ex(const void *x, int64_t x_stride, const void *W, i
  * Bytes of the scratch array built into the library for
  * lora_proj_apply_static_ws (held on every GPU that loads the library).
  */
-#define LORA_STATIC_WS_BYTES (4u << 20)
+#define LORA_STATIC_WS_BYTES (8u << 20)
 
 /*
  * lora_proj_apply for callers that cannot allocate device memory -- for

@@ -35,7 +35,7 @@ LORA_PATH_SIMT = 1
 LORA_PATH_TC = 2
 
 LORA_MAX_EXPERTS = 16
-LORA_STATIC_WS_BYTES = 4 << 20
+LORA_STATIC_WS_BYTES = 8 << 20
 
 
 class LoraError(RuntimeError):

@@ -140,6 +140,26 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, u
     return r == CUDA_SUCCESS;
 }
 
+// 3D view [K/64 chunks][rows][64] of a K-major bf16 matrix (K a multiple of
+// 64): one box of box_chunks x box_rows x 64 brings several 64-wide K slices
+// of the same rows in one copy, each slice laid out as a 2D 128-byte-swizzled
+// tile.
+bool make_map_3d(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, uint64_t stride_elems,
+                 uint32_t box_rows, uint32_t box_chunks)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {64, rows, K / 64};
+    cuuint64_t strides[2] = {stride_elems * 2, 128};
+    cuuint32_t box[3] = {64, box_rows, box_chunks};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 } // namespace
 
 namespace rd {
@@ -300,9 +320,10 @@ lora_status lora_build_seq_slot(const int32_t *adapter_slots, int n, int padded_
 
 namespace {
 
-lora_status carve_ws(void *ws, size_t ws_bytes, int rows, int nb, int R, Ws &out, const char *who)
+lora_status carve_ws(void *ws, size_t ws_bytes, int rows, int nb, int R, int kp, size_t part_elems,
+                     int ncnt, Ws &out, const char *who)
 {
-    const WsLayout l = ws_layout(rows, nb, R);
+    const WsLayout l = ws_layout(rows, nb, R, kp, part_elems, ncnt);
     if (ws == nullptr)
         return fail(LORA_ERR_NULL, "%s: workspace is NULL", who);
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -318,6 +339,9 @@ lora_status carve_ws(void *ws, size_t ws_bytes, int rows, int nb, int R, Ws &out
     out.unit_off = reinterpret_cast<int32_t *>(b + l.unit_off);
     out.done = reinterpret_cast<int32_t *>(b + l.done);
     out.h = reinterpret_cast<float *>(b + l.h);
+    out.tiles = reinterpret_cast<int32_t *>(b + l.tiles);
+    out.part = reinterpret_cast<float *>(b + l.part);
+    out.tile_cnt = reinterpret_cast<int32_t *>(b + l.tile_cnt);
     return LORA_OK;
 }
 
@@ -349,29 +373,44 @@ lora_status check_io(const char *who, const void *x, int64_t x_stride, int rows,
     return LORA_OK;
 }
 
-// prep (routing sort + work list) -> shrink -> base GEMM with the fused expand.
-lora_status run(const Params &p, int path, int token_tile, cudaStream_t st, const char *who)
+// Tensor-core path: prep (routing sort, work lists) then one fused launch
+// (shrink, base product, expand-fold). CUDA-core path: prep, shrink, GEMV.
+lora_status run(Params &p, int path, cudaStream_t st, const char *who)
 {
     DevInfo di;
     if (!device_info(di))
         return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
     cudaError_t e = launch_prep(p, st);
-    if (e == cudaSuccess)
-        e = launch_shrink(p, di.num_sms, st);
     if (e != cudaSuccess)
         return cuda_fail(e, who);
     if (path == LORA_PATH_SIMT) {
-        e = launch_simt(p, di.num_sms, st);
+        e = launch_shrink(p, di.num_sms, st);
+        if (e == cudaSuccess)
+            e = launch_simt(p, di.num_sms, st);
     } else {
+        const bool moe = p.expert_offsets != nullptr;
+        const TcPlan plan = plan_tc(p, moe);
         TmapSet maps;
         memset(&maps, 0, sizeof maps);
-        if (!make_map(&maps.x, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64,
-                      (uint32_t)token_tile))
+        bool ok;
+        if (plan.use3d)
+            ok = make_map_3d(&maps.x, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride,
+                             (uint32_t)plan.tn, (uint32_t)plan.kc);
+        else
+            ok = make_map(&maps.x, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64,
+                          (uint32_t)plan.tn);
+        if (!ok)
             return fail(LORA_ERR_CUDA, "%s: encoding the x tensor map failed", who);
-        for (int q = 0; q < p.E; ++q)
-            if (!make_map(&maps.w[q], p.W[q], (uint64_t)p.K, (uint64_t)p.N, (uint64_t)p.K, 64, 128))
+        for (int q = 0; q < p.E; ++q) {
+            if (plan.use3d)
+                ok = make_map_3d(&maps.w[q], p.W[q], (uint64_t)p.K, (uint64_t)p.N, (uint64_t)p.K, 128,
+                                 (uint32_t)plan.kc);
+            else
+                ok = make_map(&maps.w[q], p.W[q], (uint64_t)p.K, (uint64_t)p.N, (uint64_t)p.K, 64, 128);
+            if (!ok)
                 return fail(LORA_ERR_CUDA, "%s: encoding the W tensor map of expert %d failed", who, q);
-        e = launch_tc(p, maps, token_tile, st);
+        }
+        e = launch_tc(p, maps, plan, st);
     }
     if (e != cudaSuccess)
         return cuda_fail(e, who);
@@ -418,11 +457,15 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
     p.R = rt->max_rank;
     p.W[0] = static_cast<const uint16_t *>(W);
     p.tab[0] = tables_of(*rt);
-    if ((s = carve_ws(ws, ws_bytes, M, p.L + 1, p.R, p.ws, who)) != LORA_OK)
+    p.kp = shrink_kparts(K);
+    size_t part_elems = 0;
+    split_scratch(M, K, N, part_elems, p.ncnt);
+    if ((s = carve_ws(ws, ws_bytes, M, p.L + 1, p.R, p.kp, part_elems, p.ncnt, p.ws, who)) != LORA_OK)
         return s;
     if (path == LORA_PATH_AUTO)
         path = M <= SIMT_MAX_ROWS ? LORA_PATH_SIMT : LORA_PATH_TC;
-    return run(p, path, tc_token_tile(M), reinterpret_cast<cudaStream_t>(stream), who);
+    p.tn = tc_token_tile(M);
+    return run(p, path, reinterpret_cast<cudaStream_t>(stream), who);
 }
 
 } // namespace
@@ -433,7 +476,11 @@ size_t lora_proj_workspace_bytes(int M, const lora_route *rt)
 {
     if (rt == nullptr || rt->magic != ROUTE_MAGIC || M < 0)
         return 0;
-    return ws_layout(M, rt->max_loras + 1, rt->max_rank).total;
+    size_t part_elems = 0;
+    int ncnt = 0;
+    split_scratch(M, rt->n_in, rt->n_out, part_elems, ncnt);
+    return ws_layout(M, rt->max_loras + 1, rt->max_rank, shrink_kparts(rt->n_in), part_elems, ncnt)
+        .total;
 }
 
 lora_status lora_proj_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int N,
@@ -456,7 +503,8 @@ size_t lora_moe_workspace_bytes(int E, int T, const lora_route *rts)
 {
     if (rts == nullptr || E < 1 || E > MAX_E || T < 0 || rts[0].magic != ROUTE_MAGIC)
         return 0;
-    return ws_layout(T, E * (rts[0].max_loras + 1), rts[0].max_rank).total;
+    return ws_layout(T, E * (rts[0].max_loras + 1), rts[0].max_rank, shrink_kparts(rts[0].n_in))
+        .total;
 }
 
 lora_status lora_moe_down_apply(const void *x, int64_t x_stride, const void *const *W_e,
@@ -514,9 +562,14 @@ lora_status lora_moe_down_apply(const void *x, int64_t x_stride, const void *con
         p.W[q] = static_cast<const uint16_t *>(W_e[q]);
         p.tab[q] = tables_of(rts[q]);
     }
-    if ((s = carve_ws(ws, ws_bytes, T, E * (L + 1), R, p.ws, who)) != LORA_OK)
+    p.kp = shrink_kparts(K);
+    p.ncnt = 0;
+    if ((s = carve_ws(ws, ws_bytes, T, E * (L + 1), R, p.kp, 0, 0, p.ws, who)) != LORA_OK)
         return s;
-    return run(p, LORA_PATH_TC, 256, reinterpret_cast<cudaStream_t>(stream), who);
+    // token tile: the mean expert segment with 1/8 headroom, so a typical
+    // expert is one tile
+    p.tn = tc_token_tile((T + E - 1) / E + (T + E - 1) / E / 8);
+    return run(p, LORA_PATH_TC, reinterpret_cast<cudaStream_t>(stream), who);
 }
 
 lora_status lora_status_get(const void *ws, uint32_t *flags, lora_stream_t stream)
@@ -540,7 +593,7 @@ lora_status lora_proj_routing(const void *ws, int M, int max_loras, int32_t *per
     if (M < 0 || max_loras <= 0 || max_loras > MAX_LORAS)
         return fail(LORA_ERR_SHAPE, "lora_proj_routing: M %d / max_loras %d out of range", M,
                     max_loras);
-    const WsLayout l = ws_layout(M, max_loras + 1, 8);
+    const WsLayout l = ws_layout(M, max_loras + 1, 8, 1); // perm / seg_off do not depend on R or kp
     const uint8_t *b = static_cast<const uint8_t *>(ws);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaSuccess;

@@ -11,7 +11,7 @@ namespace rd {
 constexpr int MAX_E = LORA_MAX_EXPERTS;
 constexpr int MAX_BUCKETS = 1024;   // experts * (max_loras + 1)
 constexpr int SHRINK_RG = 8;        // ranks per shrink work unit (one warp each)
-constexpr int SHRINK_TC = 16;       // rows per shrink work unit
+constexpr int SHRINK_TC = 4;        // rows per shrink work unit (one pass)
 constexpr int PREP_THREADS = 1024;
 
 // Device routing tables of one expert's route.
@@ -52,7 +52,10 @@ struct Ws {
     int32_t *seg_off;   // [nb + 1] bucket starts in perm
     int32_t *unit_off;  // [nb + 1] first shrink unit of each bucket
     int32_t *done;      // [nb] finished shrink units per bucket
-    float *h;           // [rows][R] A_s x_i of every adapted row (fp32)
+    float *h;           // [kp][rows][R] partial A_s x_i of every adapted row (fp32)
+    int32_t *tiles;     // [1 + 3*max_tiles]: count, then (expert, first row, rows) per token tile
+    float *part;        // [tiles][csplit][tn][128] split-K partial tiles (fp32)
+    int32_t *tile_cnt;  // [tiles] split-K parts written so far (zeroed by prep)
 };
 
 // Everything a launch needs except tensor maps.
@@ -67,18 +70,32 @@ struct Params {
     int E;
     int rows; // M (projection) or T (slot-rows)
     int K, N, L, R;
+    int tn;   // token tile of the tensor-core path (rows per tile)
+    int kp;   // K parts of a shrink unit (h is summed over them)
+    int ncnt; // split-K tile counters the prep kernel clears
     const uint16_t *W[MAX_E];
     Tables tab[MAX_E];
     Ws ws;
 };
 
 struct WsLayout {
-    size_t status, perm, seg_off, unit_off, done, h, total;
+    size_t status, perm, seg_off, unit_off, done, h, tiles, part, tile_cnt, total;
 };
+
+// Upper bound on token tiles: each expert adds at most one partial tile.
+__host__ __device__ inline int max_token_tiles(int rows, int E) { return rows / 16 + E + 1; }
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-inline WsLayout ws_layout(int rows, int nb, int R)
+// K parts of a shrink unit: about 2048 of K each, at most 4 (enough units to
+// spread over the SMs for a decode batch, few enough to keep each one busy).
+inline int shrink_kparts(int K)
+{
+    int kp = K / 2048;
+    return kp < 1 ? 1 : (kp > 4 ? 4 : kp);
+}
+
+inline WsLayout ws_layout(int rows, int nb, int R, int kp, size_t part_elems = 0, int ncnt = 0)
 {
     WsLayout l;
     size_t o = 0;
@@ -87,7 +104,10 @@ inline WsLayout ws_layout(int rows, int nb, int R)
     l.seg_off = o;  o = align256(o + sizeof(int32_t) * (size_t)(nb + 1));
     l.unit_off = o; o = align256(o + sizeof(int32_t) * (size_t)(nb + 1));
     l.done = o;     o = align256(o + sizeof(int32_t) * (size_t)nb);
-    l.h = o;        o = align256(o + sizeof(float) * (size_t)rows * (size_t)R);
+    l.h = o;        o = align256(o + sizeof(float) * (size_t)kp * (size_t)rows * (size_t)R);
+    l.tiles = o;    o = align256(o + sizeof(int32_t) * (1 + 3 * (size_t)max_token_tiles(rows, nb)));
+    l.part = o;     o = align256(o + sizeof(float) * part_elems);
+    l.tile_cnt = o; o = align256(o + sizeof(int32_t) * (size_t)ncnt);
     l.total = o;
     return l;
 }
@@ -102,7 +122,15 @@ struct TmapSet {
 cudaError_t launch_prep(const Params &p, cudaStream_t st);
 cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st);
 cudaError_t launch_simt(const Params &p, int num_sms, cudaStream_t st);
-cudaError_t launch_tc(const Params &p, const TmapSet &maps, int token_tile, cudaStream_t st);
+// Shape of one tensor-core launch: token tile, 64-wide K chunks per pipeline
+// stage, stages, CTAs per cluster splitting K, and whether the 3D tensor-map
+// view (K a multiple of 64) is used.
+struct TcPlan {
+    int tn, kc, stages, csplit, use3d;
+    int sb; // B slices staged in shared memory for the expand
+};
+TcPlan plan_tc(const Params &p, bool per_expert_tiles);
+cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, cudaStream_t st);
 cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, const void *b,
                              int rank, float factor, float scale, cudaStream_t st);
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st);
@@ -110,12 +138,35 @@ cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale
 // Record `msg` as the thread's last error and return `code` (lora_api.cu).
 lora_status api_fail(lora_status code, const char *msg);
 
-// The token-tile sizes the tensor-core kernel is built for.
+// Token tile of the tensor-core path: the rows of one segment rounded up to
+// 16 (the UMMA N granularity), at most 256 (the largest UMMA N and TMA box).
 inline int tc_token_tile(int rows_per_segment)
 {
-    if (rows_per_segment <= 64) return 64;
-    if (rows_per_segment <= 128) return 128;
-    return 256;
+    int t = (rows_per_segment + 15) / 16 * 16;
+    if (t < 16) t = 16;
+    return t > 256 ? 256 : t;
+}
+
+// CTAs splitting K for one tile, from the row count and K only -- never from
+// N -- so a fused q/k/v call and its split calls compute every element
+// identically. Several token tiles (rows > 256) or expert tiles: no split.
+inline int tc_csplit(int rows, int K, bool per_expert_tiles)
+{
+    if (per_expert_tiles || rows > 256)
+        return 1;
+    const int cap = rows <= 64 ? 4 : 3;
+    const int c = ((K + 63) / 64) / 16;
+    return c < 1 ? 1 : (c > cap ? cap : c);
+}
+
+// Split-K scratch of a projection call: partial tiles and tile counters.
+inline void split_scratch(int M, int K, int N, size_t &part_elems, int &ncnt)
+{
+    const int tn = tc_token_tile(M);
+    const int cs = tc_csplit(M, K, false);
+    const int tiles = ((N + 127) / 128) * ((M + tn - 1) / tn);
+    part_elems = cs > 1 ? (size_t)tiles * cs * 128 * tn : 0;
+    ncnt = cs > 1 ? tiles : 0;
 }
 
 } // namespace rd

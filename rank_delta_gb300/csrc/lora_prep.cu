@@ -2,13 +2,16 @@
 //
 // prep_kernel   -- one CTA: stable counting sort of rows into (expert, slot)
 //                  buckets (perm / seg_off), the shrink work list (unit_off),
-//                  handoff counters cleared, status word of this call.
-// shrink_kernel -- h_i = A_s x_i for every adapted row, rank-sized, fp32
-//                  (ferrox-core `weight_matrix/lora.rs`, `LoraDelta::project`),
-//                  one work unit = 8 ranks x up to 16 rows of one slot, so each
-//                  slot's A rows are read once per 16 rows, not once per row.
+//                  handoff counters cleared, the token tiles of each expert
+//                  segment, status word of this call. It lets the dependent
+//                  projection kernel launch at once (programmatic dependent
+//                  launch); that kernel waits for this one only where it reads
+//                  these results.
+// shrink_kernel -- the shrink units (shrink.cuh) as a kernel of their own, for
+//                  the CUDA-core GEMV path.
 // table kernels -- stream-ordered writes of one slot's table entries.
 #include "lora_internal.cuh"
+#include "shrink.cuh"
 #include "vec.cuh"
 
 namespace rd {
@@ -75,6 +78,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
     __shared__ uint32_t flags;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0)
         flags = 0;
     if (tid <= p.E)
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
                                     t.scale_table[s] != 0.0f && rk > 0;
                 const int rows_b = p.ws.seg_off[tid + 1] - p.ws.seg_off[tid];
                 if (active && rows_b > 0)
-                    units = ((rk + SHRINK_RG - 1) / SHRINK_RG) * ((rows_b + SHRINK_TC - 1) / SHRINK_TC);
+                    units = bucket_units(rk, rows_b, p.kp);
             }
             p.ws.done[tid] = 0;
         }
@@ -166,68 +170,41 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
         int ex = block_exclusive_scan(units, warp_tot, total);
         if (tid < nb)
             p.ws.unit_off[tid] = ex;
+        for (int q = tid; q < p.ncnt; q += PREP_THREADS)
+            p.ws.tile_cnt[q] = 0;
         if (tid == 0) {
             p.ws.unit_off[nb] = total;
             *p.ws.status = flags;
         }
     }
-}
 
-__global__ void __launch_bounds__(256) shrink_kernel(Params p)
-{
-    const int nb = p.E * (p.L + 1);
-    const int total = p.ws.unit_off[nb];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        int lo = 0, hi = nb;
-        while (hi - lo > 1) {
-            int mid = (lo + hi) >> 1;
-            if (p.ws.unit_off[mid] <= u)
-                lo = mid;
-            else
-                hi = mid;
-        }
-        const int b = lo;
-        const int e = b / (p.L + 1), s = b % (p.L + 1) - 1;
-        const Tables &t = p.tab[e];
-        const int rk = t.rank_table[s];
-        const int nrg = (rk + SHRINK_RG - 1) / SHRINK_RG;
-        const int local = u - p.ws.unit_off[b];
-        const int rg = local % nrg, tc = local / nrg;
-        const int r0 = p.ws.seg_off[b] + tc * SHRINK_TC;
-        const int nrows = min(SHRINK_TC, p.ws.seg_off[b + 1] - r0);
-        const int r = rg * SHRINK_RG + warp;
-        int row[SHRINK_TC];
-#pragma unroll
-        for (int j = 0; j < SHRINK_TC; ++j)
-            row[j] = p.ws.perm[r0 + min(j, nrows - 1)];
-        float acc[SHRINK_TC];
-#pragma unroll
-        for (int j = 0; j < SHRINK_TC; ++j)
-            acc[j] = 0.0f;
-        if (r < rk) {
-            const uint16_t *arow = t.a_table[s] + (size_t)r * p.K;
-            for (int k0 = lane * 8; k0 < p.K; k0 += 256) {
-                const uint4 a8 = ld_nc_16(arow + k0);
-#pragma unroll
-                for (int j = 0; j < SHRINK_TC; ++j)
-                    if (j < nrows)
-                        acc[j] = dot8_acc(acc[j], a8, ld_16(p.x + (int64_t)row[j] * p.x_stride + k0));
+    // Token tiles: each expert segment cut into tiles of at most tn rows.
+    if (tid == 0) {
+        const int cap = max_token_tiles(p.rows, nb);
+        const int tn = p.tn > 0 ? p.tn : 256;
+        int k = 0;
+        for (int e = 0; e < p.E; ++e) {
+            const int a = max(offs[e], 0), b = min(offs[e + 1], p.rows);
+            for (int r0 = a; r0 < b && k < cap; r0 += tn, ++k) {
+                p.ws.tiles[1 + 3 * k] = e;
+                p.ws.tiles[2 + 3 * k] = r0;
+                p.ws.tiles[3 + 3 * k] = min(tn, b - r0);
             }
         }
-#pragma unroll
-        for (int j = 0; j < SHRINK_TC; ++j)
-            acc[j] = warp_sum(acc[j]);
-        // ranks past the adapter's rank, up to the next multiple of 8, are
-        // written as zero so the expand can run in 8-wide vectors
-        if (lane < nrows) {
-            float v = 0.0f;
-#pragma unroll
-            for (int j = 0; j < SHRINK_TC; ++j)
-                if (j == lane)
-                    v = acc[j];
-            p.ws.h[(size_t)row[lane] * p.R + r] = (r < rk) ? v : 0.0f;
-        }
+        p.ws.tiles[0] = k;
+    }
+}
+
+__global__ void __launch_bounds__(SHRINK_WARPS * 32) shrink_kernel(Params p)
+{
+    __shared__ float red[SHRINK_WARPS * 32];
+    const int total = p.ws.unit_off[p.E * (p.L + 1)];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        const UnitLoc l = locate_unit(p, u, p.ws.unit_off, p.ws.seg_off);
+        shrink_unit(p, l, warp, lane, red, 1);
+        if (threadIdx.x == 0)
+            shrink_unit_done(p, l.b);
     }
 }
 
@@ -249,7 +226,7 @@ cudaError_t launch_prep(const Params &p, cudaStream_t st)
 
 cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st)
 {
-    shrink_kernel<<<2 * num_sms, 256, 0, st>>>(p);
+    shrink_kernel<<<4 * num_sms, SHRINK_WARPS * 32, 0, st>>>(p);
     return cudaGetLastError();
 }
 

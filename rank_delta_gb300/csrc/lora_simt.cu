@@ -7,6 +7,7 @@
 // (ferrox-core `weight_matrix/lora.rs`, `LoraDelta::accumulate`), with h_i
 // the rank-sized shrink of the row produced by shrink_kernel.
 #include "lora_internal.cuh"
+#include "shrink.cuh"
 #include "vec.cuh"
 
 namespace rd {
@@ -57,11 +58,10 @@ __global__ void __launch_bounds__(256) simt_kernel(Params p)
                     const SlotInfo si = slot_info(tab, p.seq_slot[t], p.L);
                     if (si.on) {
                         const uint16_t *brow = si.b + (size_t)n * p.R;
-                        const float *hrow = p.ws.h + (size_t)t * p.R;
                         float d = 0.0f;
                         for (int q = 0; q < si.rank; q += 8) {
-                            const float4 h0 = *reinterpret_cast<const float4 *>(hrow + q);
-                            const float4 h1 = *reinterpret_cast<const float4 *>(hrow + q + 4);
+                            float4 h0, h1;
+                            h_sum8(p, t, q, h0, h1);
                             d = dot8_bf_f32(d, ld_nc_16(brow + q), h0, h1);
                         }
                         v = v + si.scale * d;

@@ -1,7 +1,7 @@
 // Inline-PTX helpers for sm_103a: mbarriers, TMA tile loads, tcgen05 (TMEM
 // allocation, UMMA issue/commit, TMEM loads) and bounded waits.
 //
-// Every wait here is bounded: after WAIT_LIMIT polls it returns false, and the
+// Every wait here is bounded: after WAIT_NS of wall time it returns false, and the
 // caller records LORA_FLAG_WAIT_TIMEOUT and unwinds instead of hanging.
 #pragma once
 #include <cstdint>
@@ -9,8 +9,16 @@
 
 namespace rd {
 
-// ~2^22 polls with a short sleep between them: on the order of a second.
-constexpr uint32_t WAIT_LIMIT = 1u << 22;
+// Every wait gives up after WAIT_NS of wall time (read from %globaltimer
+// every 256 polls), so a wait that can never complete costs about a second.
+constexpr uint64_t WAIT_NS = 1000000000ull;
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
@@ -58,18 +66,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
     return ok != 0;
 }
 
-// Wait until the phase with the given parity of `bar` has completed.
-// Returns false after WAIT_LIMIT polls.
+// Wait until the phase with the given parity of `bar` has completed. Spins on
+// try_wait (which itself parks the thread briefly in hardware) without
+// sleeping, so a pipeline handoff costs no more than the barrier latency.
+// Returns false after WAIT_NS.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
-    uint32_t a = smem_u32(bar);
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(a, parity))
             return true;
-        if (i > 32)
-            __nanosleep(64);
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > WAIT_NS)
+            return false;
     }
-    return false;
 }
 
 // ------------------------------------------------------------------- TMA
@@ -85,9 +97,118 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// 3D tiled load (c0 innermost); used with a [chunks][rows][64] view of a
+// K-major matrix so one copy brings several 64-wide K slices of the same rows.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int32_t c0, int32_t c1,
+                                            int32_t c2, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ------------------------------------------------------- clusters / PDL
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_id_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %clusterid.x;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t ncluster_x()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// Shared-memory address of the same variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa(uint32_t local_smem, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier of another CTA of the cluster, releasing this
+// thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait (acquire, cluster scope) for a barrier that other CTAs arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait_cluster(a, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_cluster(a, parity))
+            return true;
+        if ((i & 255u) == 0 && globaltimer_ns() - t0 > WAIT_NS)
+            return false;
+    }
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+// Whole-cluster barrier (every thread of every CTA in the cluster).
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_acq_rel_cluster()
+{
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding kernel's results.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -155,6 +276,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 #pragma unroll
     for (int i = 0; i < 16; ++i)
         v[i] = __uint_as_float(r[i]);
+}
+
+// The same load without the wait, so several can be in flight; registers are
+// valid after tmem_wait_ld().
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile stored with the

@@ -123,11 +123,12 @@ cudaError_t launch_prep(const Params &p, cudaStream_t st);
 cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st);
 cudaError_t launch_simt(const Params &p, int num_sms, cudaStream_t st);
 // Shape of one tensor-core launch: token tile, 64-wide K chunks per pipeline
-// stage, stages, CTAs per cluster splitting K, and whether the 3D tensor-map
-// view (K a multiple of 64) is used.
+// stage, stages, K parts, whether the 3D tensor-map view (K a multiple of 64)
+// is used, and the expand's staging buffers.
 struct TcPlan {
     int tn, kc, stages, csplit, use3d;
-    int sb; // B slices staged in shared memory for the expand
+    int xblk; // 64-wide k blocks of one tensor-core expand round
+    int hl;   // planes of the staged s * h: 1 (bf16) or 2 (bf16 hi + lo)
 };
 TcPlan plan_tc(const Params &p, bool per_expert_tiles);
 cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, cudaStream_t st);

@@ -9,29 +9,43 @@
 // that never exceeds the SMs (every CTA resident). With csplit K parts, each
 // part writes its fp32 partial tile to the workspace (coalesced, L2-resident)
 // and bumps the tile's counter; once all parts are in, each part's CTA sums a
-// contiguous third (quarter) of the columns in part order -- so every output
-// element is computed the same way whatever N is. With csplit = 1 the CTA
-// keeps two TMEM accumulators, draining one while the next tile accumulates.
+// contiguous share of the columns in part order -- so every output element
+// is computed the same way whatever N is. Two TMEM accumulators let the
+// epilogue drain one item while the next accumulates.
+//
+// The expand-fold runs on the tensor cores too. For the slots whose delta an
+// item adds (adapted rows of the tile whose slot is this K part's: slot %
+// csplit), the epilogue warps stage in shared memory, in the same 128-byte
+// swizzled K-major layout TMA writes:
+//   XB[n, k]  the B rows n0..n0+127 of those slots, concatenated along k (each
+//             slot's rank padded to 16, slots in ascending order),
+//   XH[t, k]  s_t * h_t placed in its slot's k range, zero elsewhere (bf16;
+//             with two planes, hi + lo, so that h keeps 16 significant bits),
+// and the MMA warp issues D'[n, t] = sum_k XB[n, k] XH[t, k] (UMMA M=128,
+// N=tokens, K=16 per instruction). D' goes to its own TMEM columns and the
+// epilogue adds it only to the columns that take a delta, so a row with no
+// delta is the base product byte for byte, and an adapted row is base + D'
+// whatever else the tile holds (a row gives the same bits alone or in a
+// batch). D' has TMEM columns of its own when three token tiles fit in the
+// 512 columns; otherwise it borrows the other accumulator, and the next item
+// waits for this one's drain. When the staged k range exceeds the buffers,
+// the expand runs in several rounds.
 //
 // Warp roles (256 threads):
 //   warps 0, 1   TMA producers of W (even / odd pipeline stages): 3D boxes
 //                [kc chunks][128 rows][64] so one copy brings kc K-slices;
-//   warp  2      allocates TMEM and issues the UMMAs (M=128, N=tokens, K=16,
-//                bf16 in, f32 accumulate) from one elected thread;
+//   warp  2      allocates TMEM and issues the UMMAs from one elected thread;
 //   warp  3      TMA producer of x;
 //   warps 4..7   first run their share of the shrink work units (h = A_s x,
-//                shrink.cuh), then drain TMEM (warp w reads TMEM lanes
-//                32(w-4)..+31) and apply the expand-fold s * (B_s[n, :] . h_t)
-//                to the rows of the slots this K part owns (slot % csplit), the
-//                B rows of those slots staged in shared memory while the
-//                mainloop runs; rows with no delta get nothing added. The sum
-//                is rounded once to bf16 (spark_model `layers/ops/lora_delta.rs`:
-//                the fold fused with the base product instead of a scaled-add
-//                pass over an [m, n_out] scratch).
+//                shrink.cuh), then per item stage the expand operands and
+//                drain TMEM (warp w reads TMEM lanes 32(w-4)..+31), rounding
+//                once to bf16 (spark_model `layers/ops/lora_delta.rs`: the fold
+//                fused with the base product instead of a scaled-add pass over
+//                an [m, n_out] scratch).
 // The shrink is handed over inside the launch: a unit bumps its bucket's
 // counter after writing h; the epilogue waits (bounded) for the counters of
-// the buckets its tokens use. The grid never exceeds the SM count (one CTA
-// per SM), so every unit and every K part runs while others wait.
+// the slots it stages. The grid never exceeds the SM count (one CTA per SM),
+// so every unit and every K part runs while others wait.
 //
 // The kernel starts before the routing/prep kernel has finished (programmatic
 // dependent launch); only the roles that read its results wait for it.
@@ -55,6 +69,7 @@ constexpr int EPI_THREADS = 128;
 constexpr int MAX_TN = 256;
 constexpr int MAX_STAGES = 8;
 constexpr uint32_t W_CHUNK_BYTES = TC_BM * 64 * 2;
+constexpr uint32_t XB_BLOCK = TC_BM * 128; // 64 k of 128 B rows, 128 rows
 
 struct TcCfg {
     int tn, kc, stages, csplit;
@@ -62,21 +77,31 @@ struct TcCfg {
     int static_tiles; // total tiles when the host knows them, -1 when the prep kernel lists them
     int kchunks, kstages;
     int use3d;
-    int sb;           // B slices (one slot x 128 rows each) the expand keeps in shared memory
+    int xblk;         // 64-wide k blocks of one expand round
+    int hl;           // XH planes: 1 (bf16) or 2 (hi + lo)
+    int borrow;       // 1: no room for D' beside two accumulators; D' borrows the other one
     uint32_t x_chunk, stage_bytes;
-    uint32_t brow;    // bytes per staged B row (R * 2 + 16: padded against bank conflicts)
-    uint32_t s_off, aux_off, b_off, h_off, meta_off, x_off, bar_off, smem_bytes;
+    uint32_t xb_off, xh_off, aux_off, meta_off, red_off, bar_off, smem_bytes;
     uint32_t tmem_cols;
 };
 
-// Per-tile bookkeeping of the epilogue warps (shared memory at aux_off).
+// Per-item state of the epilogue warps (shared memory at aux_off) and the
+// expand round the MMA issuer reads. Offsets fit 16 bits: at most 256 slots
+// per tile, ranks at most 256, so every k offset is below 65536.
 struct EpiAux {
-    int16_t hidx[MAX_TN];    // row of the staged h for column j, or -1
-    int16_t entry[MAX_TN];   // staged B slice of column j's slot, or -1
-    int32_t slot_entry_n;    // staged B slices in use
-    int32_t slot_of_entry[64];
-    int32_t n_h;             // staged h rows in use
-    int32_t eslot[1024];     // staged B slice of slot s (-1 none yet, -2 claimed, -3 no room)
+    int32_t koff[MAX_TN];            // k offset of column j's slot in the expand, -1: no delta here
+    float cscale[MAX_TN];            // scale of column j's slot
+    int16_t crank[MAX_TN];           // rank of column j's slot
+    uint16_t soff[1024];             // per slot: padded rank if used (0 if not), then its k offset
+    int16_t entry_slot[MAX_TN];      // the expand's slots, ascending
+    int32_t ent_off[MAX_TN];         // k offset of entry e
+    int16_t ent_rank[MAX_TN];        // rank of entry e
+    const uint16_t *ent_b[MAX_TN];   // B of entry e
+    uint32_t onbits[MAX_TN / 32];    // bit j: column j takes its delta here
+    int32_t wsum[2][4];              // scan scratch: per-warp totals
+    int32_t n_on;
+    int32_t xr_mode;                 // 0 no expand, 1 expand into D'
+    int32_t xr_nk16, xr_last;        // K=16 steps of this round; last round of the item
 };
 
 struct Bars {
@@ -84,6 +109,8 @@ struct Bars {
     uint64_t empty[MAX_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
+    uint64_t x_full;   // an expand round is staged
+    uint64_t x_empty;  // the UMMAs of the last round have finished reading it
     uint64_t epi_done; // every epilogue thread has finished reading TMEM
     uint32_t tmem_base;
     int abort_flag;
@@ -182,23 +209,33 @@ drain:
             mbar_wait(bars->full + i, (uint32_t)last_parity[i]);
 }
 
+
+// UMMAs of every item: the base product into accumulator it & 1, then the
+// expand rounds the epilogue stages, into D'.
+// Accumulator acquisitions are counted per buffer (acq), matching the
+// epilogue's releases in order: item i takes buffer i & 1 and, when its D'
+// borrows the other buffer, that one too.
 __device__ __forceinline__ void issue_mma(const Params &p, const TcCfg &c, Bars *bars, uint8_t *smem,
                                           uint32_t tmem)
 {
     if (c.static_tiles < 0)
         grid_dependency_wait();
+    const EpiAux *aux = reinterpret_cast<const EpiAux *>(smem + c.aux_off);
+    const uint32_t xb = smem_u32(smem + c.xb_off), xh = smem_u32(smem + c.xh_off);
+    const uint32_t xh_plane = (uint32_t)c.xblk * (uint32_t)c.tn * 128u;
     const int total = item_total(p, c);
-    int g = 0, it = 0;
+    int g = 0, it = 0, xg = 0;
+    uint32_t acq[2] = {0u, 0u};
     TileInfo ti;
     for (int w = blockIdx.x; w < total && get_tile(p, c, w / c.csplit, total, ti); w += gridDim.x, ++it) {
         const int part = w % c.csplit;
         const int ks0 = part * c.kstages / c.csplit, ks1 = (part + 1) * c.kstages / c.csplit;
         const int buf = it & 1;
-        const uint32_t use = (uint32_t)(it >> 1);
-        if (aborted(bars) || !mbar_wait(bars->acc_empty + buf, (use & 1u) ^ 1u)) {
+        if (aborted(bars) || !mbar_wait(bars->acc_empty + buf, (acq[buf] & 1u) ^ 1u)) {
             flag_abort(p, bars);
             break;
         }
+        ++acq[buf];
         tc_fence_after();
         const uint32_t acc = tmem + (uint32_t)(buf * c.tn);
         const int nmma = (ti.cnt + 15) & ~15;
@@ -215,66 +252,64 @@ __device__ __forceinline__ void issue_mma(const Params &p, const TcCfg &c, Bars 
             }
             tc_fence_after();
             const uint32_t wb = smem_u32(smem + (size_t)slot * c.stage_bytes);
-            const uint32_t xb = wb + (uint32_t)c.kc * W_CHUNK_BYTES;
+            const uint32_t xsb = wb + (uint32_t)c.kc * W_CHUNK_BYTES;
             for (int q = 0; q < c.kc; ++q) {
                 if (ks * c.kc + q >= c.kchunks)
                     break;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     umma_bf16(acc, sw128_kmajor_desc(wb + q * W_CHUNK_BYTES + j * 32),
-                              sw128_kmajor_desc(xb + q * c.x_chunk + j * 32), idesc, accumulate);
+                              sw128_kmajor_desc(xsb + q * c.x_chunk + j * 32), idesc, accumulate);
                     accumulate = 1;
                 }
             }
             umma_commit(bars->empty + slot);
         }
+        // expand rounds of this item
+        bool first = true;
+        uint32_t dacc = 0;
+        while (ok) {
+            if (aborted(bars) || !mbar_wait(&bars->x_full, (uint32_t)xg & 1u)) {
+                flag_abort(p, bars);
+                ok = false;
+                break;
+            }
+            ++xg;
+            tc_fence_after();
+            const int mode = *(volatile const int32_t *)&aux->xr_mode;
+            const int nk16 = *(volatile const int32_t *)&aux->xr_nk16;
+            const int last = *(volatile const int32_t *)&aux->xr_last;
+            if (mode == 1 && first && c.borrow) {
+                const int ob = buf ^ 1;
+                if (aborted(bars) || !mbar_wait(bars->acc_empty + ob, (acq[ob] & 1u) ^ 1u)) {
+                    flag_abort(p, bars);
+                    ok = false;
+                    break;
+                }
+                ++acq[ob];
+                tc_fence_after();
+            }
+            if (first)
+                dacc = tmem + (uint32_t)((c.borrow ? (buf ^ 1) : 2) * c.tn);
+            uint32_t dacc_on = first ? 0u : 1u;
+            for (int k = 0; k < nk16; ++k) {
+                const uint32_t koff = (uint32_t)(k >> 2) * XB_BLOCK + (uint32_t)(k & 3) * 32u;
+                const uint32_t hoff = (uint32_t)(k >> 2) * (uint32_t)c.tn * 128u + (uint32_t)(k & 3) * 32u;
+                for (int h = 0; h < c.hl; ++h) {
+                    umma_bf16(dacc, sw128_kmajor_desc(xb + koff), sw128_kmajor_desc(xh + h * xh_plane + hoff),
+                              idesc, dacc_on);
+                    dacc_on = 1;
+                }
+            }
+            umma_commit(&bars->x_empty);
+            first = false;
+            if (last)
+                break;
+        }
         umma_commit(bars->acc_full + buf); // arrives once every UMMA above has finished
         if (!ok)
             break;
     }
-}
-
-// Deltas s * (B_s[n, :] . h_t) of four columns at once (so the loads of the
-// four are in flight together), h_t staged (row k of Hs), B_s[n, :] staged
-// (slice e of Bs) or, when the slot did not fit, read from the pool. Column
-// i takes part when on[i]; d[i] receives its delta.
-__device__ __forceinline__ void lora_delta4(const Params &p, const TcCfg &c, const SlotInfo *const (&si)[4],
-                                            const uint8_t *Bs, const float *Hs, const int (&e)[4],
-                                            const int (&k)[4], const bool (&on)[4], int et, int n,
-                                            float (&d)[4])
-{
-    int rk[4], rmax = 0;
-    const float *hrow[4];
-    const uint8_t *bst[4];
-    const uint16_t *bgl[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        d[i] = 0.0f;
-        rk[i] = on[i] ? si[i]->rank : 0;
-        rmax = max(rmax, rk[i]);
-        hrow[i] = Hs + (size_t)(on[i] ? k[i] : 0) * p.R;
-        bst[i] = Bs + ((size_t)(e[i] >= 0 ? e[i] : 0) * TC_BM + et) * c.brow;
-        bgl[i] = on[i] ? si[i]->b + (size_t)n * p.R : nullptr;
-    }
-#pragma unroll 2
-    for (int q = 0; q < rmax; q += 8) {
-        uint4 bv[4];
-        float4 h0[4], h1[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const bool use = q < rk[i];
-            bv[i] = !use ? make_uint4(0, 0, 0, 0)
-                         : (e[i] >= 0 ? *reinterpret_cast<const uint4 *>(bst[i] + q * 2) : ld_nc_16(bgl[i] + q));
-            h0[i] = use ? *reinterpret_cast<const float4 *>(hrow[i] + q) : make_float4(0, 0, 0, 0);
-            h1[i] = use ? *reinterpret_cast<const float4 *>(hrow[i] + q + 4) : make_float4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            d[i] = dot8_bf_f32(d[i], bv[i], h0[i], h1[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        d[i] *= on[i] ? si[i]->scale : 0.0f;
 }
 
 __device__ __forceinline__ bool wait_count(const int32_t *cnt, int target)
@@ -290,24 +325,185 @@ __device__ __forceinline__ bool wait_count(const int32_t *cnt, int target)
     }
 }
 
-// Per item: which columns get their delta here (adapted rows whose slot is
-// this K part's: slot % csplit), stage those slots' B rows and the summed h
-// of those columns in shared memory, then add the deltas to this part's
-// accumulator; with csplit > 1 write the partial tile and, once every part
-// is in, sum this part's share of the columns in part order.
+// Exclusive scan of two values over the 128 epilogue threads (ea, eb), and
+// their totals (ta, tb).
+__device__ __forceinline__ void epi_scan2(int a, int b, int &ea, int &eb, int &ta, int &tb, EpiAux *aux,
+                                          int et)
+{
+    const int lane = et & 31, w = et >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int xa = __shfl_up_sync(0xffffffffu, ia, o);
+        const int xb = __shfl_up_sync(0xffffffffu, ib, o);
+        if (lane >= o) {
+            ia += xa;
+            ib += xb;
+        }
+    }
+    if (lane == 31) {
+        aux->wsum[0][w] = ia;
+        aux->wsum[1][w] = ib;
+    }
+    named_bar_sync(1, EPI_THREADS);
+    int pa = 0, pb = 0;
+    ta = 0;
+    tb = 0;
+#pragma unroll
+    for (int q = 0; q < EPI_THREADS / 32; ++q) {
+        const int va = aux->wsum[0][q], vb = aux->wsum[1][q];
+        if (q < w) {
+            pa += va;
+            pb += vb;
+        }
+        ta += va;
+        tb += vb;
+    }
+    ea = pa + ia - a;
+    eb = pb + ib - b;
+    named_bar_sync(1, EPI_THREADS); // wsum is free again
+}
+
+// bf16 bits of v, and of the remainder v - bf16(v).
+__device__ __forceinline__ void split_hi_lo(float v, uint32_t &hi, uint32_t &lo)
+{
+    const uint16_t h = f32_to_bf16_bits(v);
+    hi = h;
+    lo = f32_to_bf16_bits(v - __uint_as_float((uint32_t)h << 16));
+}
+
+// This CTA's share of the shrink work units (h = A_s x, shrink.cuh); one
+// fence publishes them all, then each unit's bucket counter is bumped.
+__device__ __forceinline__ void epi_shrink(const Params &p, const int32_t *unit_off, const int32_t *seg_off,
+                                           float *red, int et)
+{
+    const int nb = p.E * (p.L + 1);
+    const int total_units = unit_off[nb];
+    for (int u = blockIdx.x; u < total_units; u += gridDim.x)
+        shrink_unit(p, locate_unit(p, u, unit_off, seg_off), et >> 5, et & 31, red, 1);
+    if (blockIdx.x < total_units) {
+        __threadfence();
+        named_bar_sync(1, EPI_THREADS);
+        for (int u = blockIdx.x + et * gridDim.x; u < total_units; u += EPI_THREADS * gridDim.x)
+            atomicAdd(p.ws.done + locate_unit(p, u, unit_off, seg_off).b, 1);
+    }
+}
+
+// B rows n0 + et of the expand's slots whose k range meets [r0k, r0k + kr),
+// copied into XB (128-byte swizzle) without passing through registers; pad
+// columns of the padded rank and rows past N are zero-filled.
+__device__ __forceinline__ void stage_b(const Params &p, const EpiAux *aux, uint8_t *XB, int nent, int r0k,
+                                        int kr, int n, int et)
+{
+    const bool row_ok = n < p.N;
+    for (int e = 0; e < nent; ++e) {
+        const int so = aux->ent_off[e] - r0k;
+        const int rk = aux->ent_rank[e];
+        const int pk = (rk + 15) & ~15;
+        if (so + pk <= 0 || so >= kr)
+            continue;
+        const uint16_t *src = aux->ent_b[e] + (size_t)(row_ok ? n : 0) * p.R;
+        for (int q = max(0, -so); q < pk && so + q < kr; q += 8) {
+            const int cq = (so + q) >> 3;
+            const bool has = row_ok && q < rk;
+            cp_async_16(XB + (cq >> 3) * XB_BLOCK + et * 128 + (((cq & 7) ^ (et & 7)) << 4),
+                        src + (has ? q : 0), has ? 16u : 0u);
+        }
+    }
+}
+
+// XH rows 0..nmma-1 of the round [r0k, r0k + kr): s_t * h_t in column t's
+// slot range (hi, and lo = the bf16 remainder when hl = 2), zero elsewhere.
+// First every chunk of the round is zeroed, then thread et writes the data
+// chunks of columns et, et + 128 with all its h loads issued together.
+__device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const EpiAux *aux, uint8_t *XH,
+                                        const TileInfo &ti, int nmma, int r0k, int kr, int et)
+{
+    const uint32_t xh_block = (uint32_t)c.tn * 128u;
+    const uint32_t xh_plane = (uint32_t)c.xblk * xh_block;
+    const int nch = ((kr + 63) >> 6) * 8;
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int idx = et; idx < nmma * nch; idx += EPI_THREADS) {
+        const int j = idx / nch, cq = idx - j * nch;
+        uint8_t *dst = XH + (uint32_t)(cq >> 3) * xh_block + j * 128 + (((cq & 7) ^ (j & 7)) << 4);
+        *reinterpret_cast<uint4 *>(dst) = z;
+        if (c.hl == 2)
+            *reinterpret_cast<uint4 *>(dst + xh_plane) = z;
+    }
+    named_bar_sync(1, EPI_THREADS);
+    const size_t part_stride = (size_t)p.rows * p.R;
+    for (int j = et; j < ti.cnt; j += EPI_THREADS) {
+        const int ko = aux->koff[j];
+        if (ko < 0)
+            continue;
+        const int rk = aux->crank[j];
+        const float s = aux->cscale[j];
+        // ranks r (multiples of 8, r < rank) of this slot that fall in the round
+        const int rlo = max(0, r0k - ko), rhi = min(rk, r0k + kr - ko);
+        const float *hrow = p.ws.h + (size_t)(ti.r0 + j) * p.R;
+        for (int r = rlo; r < rhi; r += 64) {
+            float4 a[8], b[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int rr = min(r + 8 * q, rhi - 1) & ~7; // clamped: loads stay in the row
+                const float *h = hrow + rr;
+                a[q] = __ldcg(reinterpret_cast<const float4 *>(h));
+                b[q] = __ldcg(reinterpret_cast<const float4 *>(h + 4));
+#pragma unroll
+                for (int kq = 1; kq < 4; ++kq) {
+                    const float *hq = h + (size_t)min(kq, p.kp - 1) * part_stride;
+                    const float4 c4 = __ldcg(reinterpret_cast<const float4 *>(hq));
+                    const float4 d4 = __ldcg(reinterpret_cast<const float4 *>(hq + 4));
+                    const bool use = kq < p.kp;
+                    a[q].x += use ? c4.x : 0.0f; a[q].y += use ? c4.y : 0.0f;
+                    a[q].z += use ? c4.z : 0.0f; a[q].w += use ? c4.w : 0.0f;
+                    b[q].x += use ? d4.x : 0.0f; b[q].y += use ? d4.y : 0.0f;
+                    b[q].z += use ? d4.z : 0.0f; b[q].w += use ? d4.w : 0.0f;
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (r + 8 * q >= rhi)
+                    break;
+                const float v[8] = {a[q].x * s, a[q].y * s, a[q].z * s, a[q].w * s,
+                                    b[q].x * s, b[q].y * s, b[q].z * s, b[q].w * s};
+                uint32_t h8[8], l8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    split_hi_lo(v[i], h8[i], l8[i]);
+                const int cq = (ko + r + 8 * q - r0k) >> 3;
+                uint8_t *dst = XH + (uint32_t)(cq >> 3) * xh_block + j * 128 + (((cq & 7) ^ (j & 7)) << 4);
+                *reinterpret_cast<uint4 *>(dst) = make_uint4(h8[0] | (h8[1] << 16), h8[2] | (h8[3] << 16),
+                                                             h8[4] | (h8[5] << 16), h8[6] | (h8[7] << 16));
+                if (c.hl == 2)
+                    *reinterpret_cast<uint4 *>(dst + xh_plane) =
+                        make_uint4(l8[0] | (l8[1] << 16), l8[2] | (l8[3] << 16), l8[4] | (l8[5] << 16),
+                                   l8[6] | (l8[7] << 16));
+            }
+        }
+    }
+}
+
+// Per item: which columns take their delta here (adapted rows whose slot is
+// this K part's: slot % csplit) and the k offset of each such slot; stage the
+// expand operands round by round for the MMA warp (the first round of the
+// first item is issued before this CTA's shrink units, so its B copies overlap
+// them); then drain the accumulator (adding D' to those columns only), and
+// with csplit > 1 write the partial tile and, once every part is in, sum this
+// part's share of the columns in part order.
 __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *bars, uint8_t *smem,
                                          uint32_t tmem)
 {
     const int et = threadIdx.x - (TC_THREADS - EPI_THREADS); // TMEM lane 0..127
-    const int ew = et >> 5, lane = et & 31;
-    SlotInfo *sinfo = reinterpret_cast<SlotInfo *>(smem + c.s_off);
+    const int ew = et >> 5;
     EpiAux *aux = reinterpret_cast<EpiAux *>(smem + c.aux_off);
-    uint8_t *Bs = smem + c.b_off;
-    float *Hs = reinterpret_cast<float *>(smem + c.h_off);
+    uint8_t *XB = smem + c.xb_off;
+    uint8_t *XH = smem + c.xh_off;
     const int C = c.csplit;
     const int nb = p.E * (p.L + 1);
     int32_t *unit_off = reinterpret_cast<int32_t *>(smem + c.meta_off); // copies of the routing
     int32_t *seg_off = unit_off + nb + 1;                                 // results, in shared memory
+    float *red = reinterpret_cast<float *>(smem + c.red_off);
 
     grid_dependency_wait();
     for (int q = et; q <= nb; q += EPI_THREADS) {
@@ -315,96 +511,125 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         seg_off[q] = p.ws.seg_off[q];
     }
     named_bar_sync(1, EPI_THREADS);
-    // this CTA's share of the shrink work units; one fence publishes them all
-    const int total_units = unit_off[nb];
-    float *scratch = reinterpret_cast<float *>(smem + c.x_off); // [16][128] fp32
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x)
-        shrink_unit(p, locate_unit(p, u, unit_off, seg_off), ew, lane, scratch, 1);
-    if (blockIdx.x < total_units) {
-        __threadfence();
-        named_bar_sync(1, EPI_THREADS);
-        for (int u = blockIdx.x + et * gridDim.x; u < total_units; u += EPI_THREADS * gridDim.x)
-            atomicAdd(p.ws.done + locate_unit(p, u, unit_off, seg_off).b, 1);
-    }
 
     const int total = item_total(p, c);
-    int it = 0;
+    bool shrink_done = false;
+    int it = 0, xg = 0;
     TileInfo ti;
     for (int w = blockIdx.x; w < total && get_tile(p, c, w / c.csplit, total, ti); w += gridDim.x, ++it) {
         const int tile = w / c.csplit, part = w % c.csplit;
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
-        const int n = ti.n0 + ew * 32 + lane;
+        const int n = ti.n0 + et;
         const Tables &tab = p.tab[ti.e];
+        const int nmma = (ti.cnt + 15) & ~15;
 
-        // (1) slot of every column; staged-h row and staged B slice of the
-        // columns whose delta this part adds
-        if (et == 0) {
-            aux->slot_entry_n = 0;
-            aux->n_h = 0;
-        }
+        // (1) the columns whose delta this part adds, and the slots they use
         for (int q = et; q < p.L; q += EPI_THREADS)
-            aux->eslot[q] = -1;
+            aux->soff[q] = 0;
+        if (et < MAX_TN / 32)
+            aux->onbits[et] = 0;
+        if (et == 0)
+            aux->n_on = 0;
         named_bar_sync(1, EPI_THREADS);
+        int my_on = 0;
         for (int j = et; j < ti.cnt; j += EPI_THREADS) {
             const int sl = p.seq_slot[ti.r0 + j];
             const SlotInfo si = slot_info(tab, sl, p.L);
-            sinfo[j] = si;
-            aux->hidx[j] = -1;
-            if (si.on && sl % C == part) {
-                aux->hidx[j] = (int16_t)atomicAdd(&aux->n_h, 1);
-                if (atomicCAS(&aux->eslot[sl], -1, -2) == -1) {
-                    const int e = atomicAdd(&aux->slot_entry_n, 1);
-                    if (e < c.sb) {
-                        aux->slot_of_entry[e] = sl;
-                        aux->eslot[sl] = e;
-                    } else {
-                        aux->eslot[sl] = -3;
-                    }
+            const bool on = si.on && sl % C == part;
+            aux->koff[j] = on ? sl : -1;
+            aux->cscale[j] = si.scale;
+            aux->crank[j] = (int16_t)si.rank;
+            if (on) {
+                aux->soff[sl] = (uint16_t)((si.rank + 15) & ~15); // same value from every writer
+                atomicOr(&aux->onbits[j >> 5], 1u << (j & 31));
+                ++my_on;
+            }
+        }
+        if (my_on)
+            atomicAdd(&aux->n_on, my_on);
+        named_bar_sync(1, EPI_THREADS);
+        // (2) k offsets: used slots in ascending order, each rank padded to 16
+        const int per = (p.L + EPI_THREADS - 1) / EPI_THREADS;
+        const int s0 = min(p.L, et * per), s1 = min(p.L, s0 + per);
+        int ksum = 0, scount = 0;
+        for (int s = s0; s < s1; ++s) {
+            const int v = aux->soff[s];
+            ksum += v;
+            scount += v != 0;
+        }
+        int ek, ec, kx, nent;
+        epi_scan2(ksum, scount, ek, ec, kx, nent, aux, et);
+        for (int s = s0; s < s1; ++s) {
+            const int v = aux->soff[s];
+            if (v) {
+                aux->soff[s] = (uint16_t)ek;
+                aux->entry_slot[ec] = (int16_t)s;
+                aux->ent_off[ec] = ek;
+                ek += v;
+                ++ec;
+            }
+        }
+        named_bar_sync(1, EPI_THREADS);
+        for (int e = et; e < nent; e += EPI_THREADS) {
+            const int s = aux->entry_slot[e];
+            aux->ent_b[e] = tab.b_table[s];
+            aux->ent_rank[e] = (int16_t)tab.rank_table[s];
+        }
+        for (int j = et; j < ti.cnt; j += EPI_THREADS) {
+            const int sl = aux->koff[j];
+            if (sl >= 0)
+                aux->koff[j] = aux->soff[sl];
+        }
+        named_bar_sync(1, EPI_THREADS);
+        const int mode = aux->n_on > 0 ? 1 : 0;
+
+        // (3) expand rounds: k range [r0k, r0k + kr) of the concatenated slots
+        int r0k = 0;
+        bool stop = false;
+        do {
+            const int kr = min(kx - r0k, c.xblk * 64);
+            if (xg > 0) { // the UMMAs of the previous round have read the buffers
+                if (et == 0 && !mbar_wait(&bars->x_empty, (uint32_t)(xg - 1) & 1u))
+                    flag_abort(p, bars);
+                named_bar_sync(1, EPI_THREADS);
+            }
+            if (kr > 0)
+                stage_b(p, aux, XB, nent, r0k, kr, n, et);
+            if (!shrink_done) {
+                epi_shrink(p, unit_off, seg_off, red, et);
+                shrink_done = true;
+            }
+            if (r0k == 0 && nent > 0) { // the shrink of the staged slots has finished
+                for (int e = et; e < nent; e += EPI_THREADS) {
+                    const int b = ti.e * (p.L + 1) + aux->entry_slot[e] + 1;
+                    if (!wait_bucket(p, b, unit_off))
+                        flag_abort(p, bars);
+                }
+                named_bar_sync(1, EPI_THREADS);
+                if (aborted(bars)) {
+                    cp_async_wait_all();
+                    stop = true;
+                    break;
                 }
             }
-        }
-        named_bar_sync(1, EPI_THREADS);
-        for (int j = et; j < ti.cnt; j += EPI_THREADS) {
-            int e = -1;
-            if (aux->hidx[j] >= 0) {
-                e = aux->eslot[p.seq_slot[ti.r0 + j]];
-                e = e >= 0 ? e : -1;
+            if (kr > 0)
+                stage_h(p, c, aux, XH, ti, nmma, r0k, kr, et);
+            cp_async_wait_all();
+            fence_proxy_async_smem(); // generic-proxy writes, read by the UMMAs
+            named_bar_sync(1, EPI_THREADS);
+            if (et == 0) {
+                aux->xr_mode = mode;
+                aux->xr_nk16 = kr / 16;
+                aux->xr_last = r0k + kr >= kx ? 1 : 0;
+                mbar_arrive(&bars->x_full);
             }
-            aux->entry[j] = (int16_t)e;
-        }
-        // (2) B rows of the staged slots: thread et copies row n0 + et of each
-        const int nent = min(aux->slot_entry_n, c.sb);
-        for (int e = 0; e < nent; ++e) {
-            const int sl = aux->slot_of_entry[e];
-            const int rk = tab.rank_table[sl];
-            const uint16_t *src = tab.b_table[sl] + (size_t)n * p.R;
-            uint8_t *dst = Bs + ((size_t)e * TC_BM + et) * c.brow;
-#pragma unroll 4
-            for (int q = 0; q < rk; q += 8)
-                *reinterpret_cast<uint4 *>(dst + q * 2) = n < p.N ? ld_nc_16(src + q) : make_uint4(0, 0, 0, 0);
-        }
-        // (3) wait for the shrink of those columns, stage their h
-        for (int j = et; j < ti.cnt; j += EPI_THREADS) {
-            if (aux->hidx[j] < 0)
-                continue;
-            const int b = ti.e * (p.L + 1) + p.seq_slot[ti.r0 + j] + 1;
-            if (!wait_bucket(p, b, unit_off))
-                flag_abort(p, bars);
-        }
-        named_bar_sync(1, EPI_THREADS);
-        const int rv = p.R / 8;
-        for (int idx = et; idx < ti.cnt * rv; idx += EPI_THREADS) {
-            const int j = idx / rv, q = (idx % rv) * 8;
-            const int k = aux->hidx[j];
-            if (k < 0 || q >= sinfo[j].rank)
-                continue;
-            float4 a, b2;
-            h_sum8(p, ti.r0 + j, q, a, b2);
-            float *dst = Hs + (size_t)k * p.R + q;
-            *reinterpret_cast<float4 *>(dst) = a;
-            *reinterpret_cast<float4 *>(dst + 4) = b2;
-        }
+            ++xg;
+            r0k += kr;
+        } while (r0k < kx);
+        if (stop)
+            break;
+
         // (4) accumulator of this item
         const bool got = mbar_wait(bars->acc_full + buf, use & 1u);
         tc_fence_after();
@@ -413,53 +638,22 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         named_bar_sync(1, EPI_THREADS);
         if (aborted(bars))
             break;
-        const uint32_t tl = tmem + (uint32_t)(buf * c.tn) + ((uint32_t)(ew * 32) << 16);
+        const uint32_t lane_off = (uint32_t)(ew * 32) << 16;
+        const uint32_t tb = tmem + (uint32_t)(buf * c.tn) + lane_off;
+        const uint32_t td = tmem + (uint32_t)((c.borrow ? (buf ^ 1) : 2) * c.tn) + lane_off;
         float *my_part = p.ws.part + ((size_t)tile * C + part) * (size_t)c.tn * EPI_THREADS;
-        uint32_t raw[16];
-        tmem_ld16_nowait(tl, raw);
         for (int c0 = 0; c0 < ti.cnt; c0 += 16) {
+            uint32_t rb[16], rdl[16];
+            tmem_ld16_nowait(tb + (uint32_t)c0, rb);
+            if (mode)
+                tmem_ld16_nowait(td + (uint32_t)c0, rdl);
+            const uint32_t on16 = mode ? (aux->onbits[c0 >> 5] >> (c0 & 16)) & 0xFFFFu : 0u;
             tmem_wait_ld();
             float v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-                v[j] = __uint_as_float(raw[j]);
-            if (c0 + 16 < ti.cnt) // next chunk's accumulator load overlaps this chunk's work
-                tmem_ld16_nowait(tl + (uint32_t)(c0 + 16), raw);
-            bool any = false;
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-                any |= c0 + j < ti.cnt && aux->hidx[c0 + j] >= 0;
-            if (any && n < p.N) { // columns to adapt: deltas four at a time, values via scratch
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    scratch[j * EPI_THREADS + et] = v[j];
-#pragma unroll 1
-                for (int j4 = 0; j4 < 16; j4 += 4) {
-                    const SlotInfo *si[4];
-                    int e[4], k[4];
-                    bool on[4], any4 = false;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int col = c0 + j4 + i;
-                        k[i] = col < ti.cnt ? aux->hidx[col] : -1;
-                        on[i] = k[i] >= 0;
-                        any4 |= on[i];
-                        e[i] = on[i] ? aux->entry[col] : -1;
-                        si[i] = sinfo + (col < ti.cnt ? col : 0);
-                    }
-                    if (!any4)
-                        continue;
-                    float d[4];
-                    lora_delta4(p, c, si, Bs, Hs, e, k, on, et, n, d);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (on[i])
-                            scratch[(j4 + i) * EPI_THREADS + et] += d[i];
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    v[j] = scratch[j * EPI_THREADS + et];
-            }
+                v[j] = (on16 >> j) & 1u ? __uint_as_float(rb[j]) + __uint_as_float(rdl[j])
+                                        : __uint_as_float(rb[j]);
             if (C == 1) {
                 if (n < p.N) {
 #pragma unroll
@@ -480,6 +674,8 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         named_bar_sync(1, EPI_THREADS);
         if (et == 0) {
             mbar_arrive(bars->acc_empty + buf);
+            if (mode && c.borrow)
+                mbar_arrive(bars->acc_empty + (buf ^ 1));
             if (C > 1)
                 atomicAdd(p.ws.tile_cnt + tile, 1);
         }
@@ -498,9 +694,10 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj)
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (q < C && col + jj < ce)
-                            acc[jj][q] = __ldcg(parts + q * pstride + (size_t)(col + jj) * EPI_THREADS + et);
+                    for (int q = 0; q < 4; ++q) {
+                        const int cc = min(col + jj, ce - 1), qq = min(q, C - 1); // clamped: in bounds
+                        acc[jj][q] = __ldcg(parts + qq * pstride + (size_t)cc * EPI_THREADS + et);
+                    }
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
                     if (col + jj >= ce || n >= p.N)
@@ -514,8 +711,10 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
                 }
             }
         }
-        named_bar_sync(1, EPI_THREADS); // staged rows are rewritten by the next item
+        named_bar_sync(1, EPI_THREADS); // per-item state is rewritten by the next item
     }
+    if (!shrink_done) // a CTA without items still runs its shrink units
+        epi_shrink(p, unit_off, seg_off, red, et);
 }
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -536,6 +735,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(bars->acc_full + b, 1);
             mbar_init(bars->acc_empty + b, 1);
         }
+        mbar_init(&bars->x_full, 1);
+        mbar_init(&bars->x_empty, 1);
         mbar_init(&bars->epi_done, EPI_THREADS);
         bars->abort_flag = 0;
         fence_barrier_init();
@@ -587,16 +788,9 @@ static uint32_t pow2_at_least(uint32_t v)
 
 static uint32_t align_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-// Bytes per staged B row: R bf16, plus 16 when the row length is a multiple
-// of 64 bytes (rows that would otherwise put a warp's 16-byte reads in the
-// same shared-memory banks).
-static uint32_t staged_brow(int R)
-{
-    const uint32_t b = (uint32_t)R * 2u;
-    return (b % 64u) == 0 ? b + 16u : b;
-}
-
-// Shared-memory layout of one launch for a given plan.
+// Shared-memory layout of one launch for a given plan. The pipeline stages,
+// XB and XH start on 1024-byte boundaries (the 128-byte swizzle repeats every
+// 8 rows of 128 B): stage_bytes, XB_BLOCK and tn * 128 are multiples of 1024.
 static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
 {
     TcCfg c;
@@ -605,30 +799,29 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
     c.kc = plan.kc;
     c.csplit = plan.csplit;
     c.use3d = plan.use3d;
-    c.sb = plan.sb;
+    c.xblk = plan.xblk;
+    c.hl = plan.hl;
+    c.borrow = 3 * c.tn > 512 ? 1 : 0;
     c.n_tiles = (p.N + TC_BM - 1) / TC_BM;
     c.kchunks = (p.K + 63) / 64;
     c.kstages = (c.kchunks + c.kc - 1) / c.kc;
     c.x_chunk = (uint32_t)c.tn * 128u;
     c.stage_bytes = (uint32_t)c.kc * (W_CHUNK_BYTES + c.x_chunk);
     c.stages = plan.stages;
-    c.brow = staged_brow(p.R);
     uint32_t o = (uint32_t)c.stages * c.stage_bytes;
-    c.s_off = align_up(o, 16);
-    o = c.s_off + (uint32_t)(c.tn * sizeof(SlotInfo));
+    c.xb_off = o;
+    o += (uint32_t)c.xblk * XB_BLOCK;
+    c.xh_off = o;
+    o += (uint32_t)c.hl * (uint32_t)c.xblk * (uint32_t)c.tn * 128u;
     c.aux_off = align_up(o, 16);
     o = c.aux_off + (uint32_t)sizeof(EpiAux);
-    c.b_off = align_up(o, 16);
-    o = c.b_off + (uint32_t)c.sb * TC_BM * c.brow;
-    c.h_off = align_up(o, 16);
-    o = c.h_off + (uint32_t)c.tn * (uint32_t)p.R * 4u;
     c.meta_off = align_up(o, 16);
     o = c.meta_off + 2u * (uint32_t)(p.E * (p.L + 1) + 1) * 4u;
-    c.x_off = align_up(o, 16);
-    o = c.x_off + 16u * EPI_THREADS * 4u;
+    c.red_off = align_up(o, 16);
+    o = c.red_off + (uint32_t)(SHRINK_WARPS * 32 * 4);
     c.bar_off = align_up(o, 16);
     c.smem_bytes = 1024u + c.bar_off + (uint32_t)sizeof(Bars);
-    c.tmem_cols = pow2_at_least(2u * (uint32_t)c.tn);
+    c.tmem_cols = c.borrow ? 512u : pow2_at_least(3u * (uint32_t)c.tn);
     const int tt = (p.rows + c.tn - 1) / c.tn;
     c.static_tiles = dyn ? -1 : tt * c.n_tiles;
     return c;
@@ -636,10 +829,10 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
 
 static constexpr uint32_t SMEM_LIMIT = 232448; // 227 KB per CTA
 
-// Choose K chunks per stage, stages, reduction width and staged B slices:
-// keep at least 3 stages for tiles of 128+ rows (2 for the small decode
-// tile), then give the rest of shared memory to the B rows of the slots this
-// CTA finishes (up to every such slot).
+// Choose K chunks per stage, stages, expand k blocks and XH planes. In order:
+// at least 3 stages; W bytes in flight up to 6 chunks (96 KB); an expand round
+// of at least min(2, worst case) k blocks; two XH planes; more k blocks (up to
+// every slot of a K part at the pool rank); then larger copies.
 TcPlan plan_tc(const Params &p, bool dyn)
 {
     TcPlan plan;
@@ -648,40 +841,41 @@ TcPlan plan_tc(const Params &p, bool dyn)
     plan.use3d = (p.K % 64) == 0 ? 1 : 0;
     const int kchunks = (p.K + 63) / 64;
     plan.csplit = tc_csplit(p.rows, p.K, dyn);
-    const int need_sb = min(64, min(p.tn, (p.L + plan.csplit - 1) / plan.csplit));
-    const int min_stages = p.tn <= 64 ? 2 : 3;
-    int best = -1;
+    const int slots = min(p.tn, (p.L + plan.csplit - 1) / plan.csplit);
+    const int need_blk = max(1, min(8, (slots * ((p.R + 15) & ~15) + 63) / 64));
+    long best = -1;
     TcPlan cand = plan;
     const int kcs[3] = {4, 2, 1};
-    {
-        for (int ik = 0; ik < 3; ++ik) {
-            const int kc = kcs[ik];
-            if (kc > 1 && !plan.use3d)
-                continue;
-            if ((kchunks + kc - 1) / kc < plan.csplit)
-                continue;
-            for (int st = MAX_STAGES; st >= 2; --st) {
-                cand.kc = kc;
-                cand.stages = st;
-                cand.sb = 0;
-                const TcCfg c0 = make_cfg(p, cand, dyn);
-                if (c0.smem_bytes > SMEM_LIMIT)
-                    continue;
-                const uint32_t slice = (uint32_t)TC_BM * staged_brow(p.R);
-                cand.sb = (int)min((uint32_t)need_sb, (SMEM_LIMIT - c0.smem_bytes) / slice);
-                const int score = (st >= min_stages ? 100000 : 0) + (cand.sb >= need_sb ? 10000 : 0) +
-                                  cand.sb * 100 + min(st, 4) * 10 + kc * 2;
-                if (score > best) {
-                    best = score;
-                    plan = cand;
+    for (int ik = 0; ik < 3; ++ik) {
+        const int kc = kcs[ik];
+        if (kc > 1 && !plan.use3d)
+            continue;
+        if ((kchunks + kc - 1) / kc < plan.csplit)
+            continue;
+        for (int st = MAX_STAGES; st >= 2; --st)
+            for (int xb = need_blk; xb >= 1; --xb)
+                for (int hl = 2; hl >= 1; --hl) {
+                    cand.kc = kc;
+                    cand.stages = st;
+                    cand.xblk = xb;
+                    cand.hl = hl;
+                    const TcCfg c0 = make_cfg(p, cand, dyn);
+                    if (c0.smem_bytes > SMEM_LIMIT)
+                        continue;
+                    const long score = (st >= 3 ? 10000000L : 0L) + min(st * kc, 6) * 1000000L +
+                                       min(xb, min(need_blk, 2)) * 100000L + hl * 10000L + xb * 1000L +
+                                       kc * 10L + st;
+                    if (score > best) {
+                        best = score;
+                        plan = cand;
+                    }
                 }
-            }
-        }
     }
     if (best < 0) {
         plan.kc = 1;
         plan.stages = 2;
-        plan.sb = 0;
+        plan.xblk = 1;
+        plan.hl = 1;
     }
     return plan;
 }

@@ -84,6 +84,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     }
 }
 
+// ---------------------------------------------------------------- cp.async
+// 16-byte global -> shared copy that does not pass through registers; the
+// bytes past src_bytes (0 or 16) are written as zero. Complete after
+// cp_async_wait_all() in the issuing thread.
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gsrc, uint32_t src_bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- TMA
 // 2D tiled load global -> shared, completion counted on `bar` in bytes.
 // c0 is the innermost (contiguous) coordinate in elements, c1 the row.

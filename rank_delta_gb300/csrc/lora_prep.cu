@@ -16,21 +16,6 @@
 
 namespace rd {
 
-__device__ __forceinline__ int row_bucket(const Params &p, const int *offs, int i)
-{
-    int e = -1;
-    for (int q = 0; q < p.E; ++q)
-        if (offs[q] <= i && i < offs[q + 1]) {
-            e = q;
-            break;
-        }
-    if (e < 0)
-        return -1;
-    int s = p.seq_slot[i];
-    int key = (s >= 0 && s < p.L) ? s + 1 : 0;
-    return e * (p.L + 1) + key;
-}
-
 // Exclusive scan of one value per thread across the 1024-thread block.
 __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &total)
 {
@@ -65,42 +50,79 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &t
     return r;
 }
 
+// Bucket of row i given the expert segment bounds and its slot value.
+__device__ __forceinline__ int bucket_of(const Params &p, const int *offs, int i, int s)
+{
+    int e = -1;
+    for (int q = 0; q < p.E; ++q)
+        if (offs[q] <= i && i < offs[q + 1]) {
+            e = q;
+            break;
+        }
+    if (e < 0)
+        return -1;
+    const int key = (s >= 0 && s < p.L) ? s + 1 : 0;
+    return e * (p.L + 1) + key;
+}
+
+// Every global read the kernel needs is issued up front (the first 1024
+// slots, the expert offsets, the slot tables); later passes work from
+// registers and shared memory.
 __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
 {
     extern __shared__ int4 prep_smem4[];
     int *sm = reinterpret_cast<int *>(prep_smem4);
     const int nb = p.E * (p.L + 1);
-    int *cnt = sm;                                          // [nb]
-    int *base = sm + nb;                                    // [nb]
-    uint16_t *wc = reinterpret_cast<uint16_t *>(sm + 2 * nb); // [32][nb]
+    int *cnt = sm;                                            // [nb] rows per bucket (pass 1)
+    int *base = sm + nb;                                      // [nb] next free position
+    int *brank = sm + 2 * nb;                                 // [nb] rank of an active slot's bucket, else 0
+    int *ccnt = sm + 3 * nb;                                  // [nb] rows per bucket in this chunk
+    uint16_t *wc = reinterpret_cast<uint16_t *>(sm + 4 * nb); // [32][nb]
     __shared__ int offs[MAX_E + 1];
     __shared__ int warp_tot[33];
+    __shared__ int etiles[MAX_E + 1];
     __shared__ uint32_t flags;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int slot0 = tid < p.rows ? p.seq_slot[tid] : -1;
     if (tid == 0)
         flags = 0;
     if (tid <= p.E)
         offs[tid] = p.expert_offsets ? p.expert_offsets[tid] : (tid == 0 ? 0 : p.rows);
-    for (int b = tid; b < nb; b += PREP_THREADS)
+    for (int b = tid; b < nb; b += PREP_THREADS) {
         cnt[b] = 0;
+        const int e = b / (p.L + 1), key = b % (p.L + 1);
+        int rk = 0;
+        if (key > 0) {
+            const Tables &t = p.tab[e];
+            const int s = key - 1;
+            const int r = t.rank_table[s];
+            const bool active = t.a_table[s] != nullptr && t.b_table[s] != nullptr &&
+                                t.scale_table[s] != 0.0f && r > 0;
+            rk = active ? r : 0;
+        }
+        brank[b] = rk;
+        p.ws.done[b] = 0;
+    }
+    for (int q = tid; q < p.ncnt; q += PREP_THREADS)
+        p.ws.tile_cnt[q] = 0;
     __syncthreads();
     if (tid == 0) {
         bool ok = offs[0] >= 0 && offs[p.E] <= p.rows;
         for (int q = 0; q < p.E; ++q)
             ok = ok && offs[q] <= offs[q + 1];
         if (!ok)
-            flags |= LORA_FLAG_BAD_OFFSETS;
+            atomicOr(&flags, (uint32_t)LORA_FLAG_BAD_OFFSETS); // pass 1 may already be setting bits
     }
-    __syncthreads();
 
     // Pass 1: bucket sizes.
     for (int i = tid; i < p.rows; i += PREP_THREADS) {
-        int b = row_bucket(p, offs, i);
+        const int s = i < PREP_THREADS ? slot0 : p.seq_slot[i];
+        const int b = bucket_of(p, offs, i, s);
         if (b >= 0) {
             atomicAdd(&cnt[b], 1);
-            if (p.seq_slot[i] >= p.L)
+            if (s >= p.L)
                 atomicOr(&flags, (uint32_t)LORA_FLAG_SLOT_RANGE);
         }
     }
@@ -115,6 +137,18 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
         if (tid == 0)
             p.ws.seg_off[nb] = total;
     }
+    // Shrink work list from the bucket sizes (shared memory only).
+    {
+        int units = 0;
+        if (tid < nb && brank[tid] > 0 && cnt[tid] > 0)
+            units = bucket_units(brank[tid], cnt[tid], p.kp);
+        int total;
+        int ex = block_exclusive_scan(units, warp_tot, total);
+        if (tid < nb)
+            p.ws.unit_off[tid] = ex;
+        if (tid == 0)
+            p.ws.unit_off[nb] = total;
+    }
     __syncthreads();
 
     // Pass 2: stable placement, 1024 rows at a time in input order. Inside a
@@ -125,7 +159,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
             wc[q] = 0;
         __syncthreads();
         const int i = c0 + tid;
-        const int b = i < p.rows ? row_bucket(p, offs, i) : -1;
+        const int s = c0 == 0 ? slot0 : (i < p.rows ? p.seq_slot[i] : -1);
+        const int b = i < p.rows ? bucket_of(p, offs, i, s) : -1;
         const unsigned peers = __match_any_sync(0xffffffffu, b);
         const int rank_in_warp = __popc(peers & ((1u << lane) - 1u));
         if (b >= 0 && rank_in_warp == 0)
@@ -134,64 +169,46 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
         for (int bb = tid; bb < nb; bb += PREP_THREADS) {
             int run = 0;
             for (int w = 0; w < 32; ++w) {
-                int v = wc[w * nb + bb];
+                const int v = wc[w * nb + bb];
                 wc[w * nb + bb] = (uint16_t)run;
                 run += v;
             }
-            cnt[bb] = run; // this chunk's rows of bucket bb
+            ccnt[bb] = run;
         }
         __syncthreads();
         if (b >= 0)
             p.ws.perm[base[b] + wc[warp * nb + b] + rank_in_warp] = i;
         __syncthreads();
         for (int bb = tid; bb < nb; bb += PREP_THREADS)
-            base[bb] += cnt[bb];
+            base[bb] += ccnt[bb];
         __syncthreads();
     }
 
-    // Shrink work list: units of (8 ranks) x (16 rows) per adapted bucket.
-    {
-        int units = 0;
-        if (tid < nb) {
-            const int e = tid / (p.L + 1), key = tid % (p.L + 1);
-            if (key > 0) {
-                const int s = key - 1;
-                const Tables &t = p.tab[e];
-                const int rk = t.rank_table[s];
-                const bool active = t.a_table[s] != nullptr && t.b_table[s] != nullptr &&
-                                    t.scale_table[s] != 0.0f && rk > 0;
-                const int rows_b = p.ws.seg_off[tid + 1] - p.ws.seg_off[tid];
-                if (active && rows_b > 0)
-                    units = bucket_units(rk, rows_b, p.kp);
-            }
-            p.ws.done[tid] = 0;
-        }
-        int total;
-        int ex = block_exclusive_scan(units, warp_tot, total);
-        if (tid < nb)
-            p.ws.unit_off[tid] = ex;
-        for (int q = tid; q < p.ncnt; q += PREP_THREADS)
-            p.ws.tile_cnt[q] = 0;
-        if (tid == 0) {
-            p.ws.unit_off[nb] = total;
-            *p.ws.status = flags;
-        }
+    // Token tiles: each expert segment cut into tiles of at most tn rows,
+    // expert by expert (thread e counts expert e's tiles; a scan places them).
+    const int tn = p.tn > 0 ? p.tn : 256;
+    const int cap = max_token_tiles(p.rows, nb);
+    if (tid < p.E) {
+        const int a = max(offs[tid], 0), b = min(offs[tid + 1], p.rows);
+        etiles[tid + 1] = b > a ? (b - a + tn - 1) / tn : 0;
     }
-
-    // Token tiles: each expert segment cut into tiles of at most tn rows.
+    __syncthreads();
     if (tid == 0) {
-        const int cap = max_token_tiles(p.rows, nb);
-        const int tn = p.tn > 0 ? p.tn : 256;
-        int k = 0;
-        for (int e = 0; e < p.E; ++e) {
-            const int a = max(offs[e], 0), b = min(offs[e + 1], p.rows);
-            for (int r0 = a; r0 < b && k < cap; r0 += tn, ++k) {
-                p.ws.tiles[1 + 3 * k] = e;
-                p.ws.tiles[2 + 3 * k] = r0;
-                p.ws.tiles[3 + 3 * k] = min(tn, b - r0);
-            }
+        etiles[0] = 0;
+        for (int e = 0; e < p.E; ++e)
+            etiles[e + 1] += etiles[e];
+        p.ws.tiles[0] = min(etiles[p.E], cap);
+        *p.ws.status = flags;
+    }
+    __syncthreads();
+    if (tid < p.E) {
+        const int a = max(offs[tid], 0), b = min(offs[tid + 1], p.rows);
+        int k = etiles[tid];
+        for (int r0 = a; r0 < b && k < cap; r0 += tn, ++k) {
+            p.ws.tiles[1 + 3 * k] = tid;
+            p.ws.tiles[2 + 3 * k] = r0;
+            p.ws.tiles[3 + 3 * k] = min(tn, b - r0);
         }
-        p.ws.tiles[0] = k;
     }
 }
 
@@ -201,21 +218,21 @@ __global__ void __launch_bounds__(SHRINK_WARPS * 32) shrink_kernel(Params p)
     const int total = p.ws.unit_off[p.E * (p.L + 1)];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
-        const UnitLoc l = locate_unit(p, u, p.ws.unit_off, p.ws.seg_off);
-        shrink_unit(p, l, warp, lane, red, 1);
+        const UnitMeta m = unit_meta(p, u, p.ws.unit_off, p.ws.seg_off);
+        shrink_unit(p, m, warp, lane, red, 1);
         if (threadIdx.x == 0)
-            shrink_unit_done(p, l.b);
+            shrink_unit_done(p, m.b);
     }
 }
 
 cudaError_t launch_prep(const Params &p, cudaStream_t st)
 {
     const int nb = p.E * (p.L + 1);
-    const size_t smem = (size_t)nb * 8 + (size_t)32 * nb * 2;
+    const size_t smem = (size_t)nb * 16 + (size_t)32 * nb * 2;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)((size_t)MAX_BUCKETS * 8 + (size_t)32 * MAX_BUCKETS * 2));
+                                             (int)((size_t)MAX_BUCKETS * 16 + (size_t)32 * MAX_BUCKETS * 2));
         if (e != cudaSuccess)
             return e;
         attr_set = true;

@@ -81,7 +81,7 @@ struct TcCfg {
     int hl;           // XH planes: 1 (bf16) or 2 (hi + lo)
     int borrow;       // 1: no room for D' beside two accumulators; D' borrows the other one
     uint32_t x_chunk, stage_bytes;
-    uint32_t xb_off, xh_off, aux_off, meta_off, red_off, bar_off, smem_bytes;
+    uint32_t xb_off, xh_off, aux_off, meta_off, red_off, umeta_off, bar_off, smem_bytes;
     uint32_t tmem_cols;
 };
 
@@ -372,20 +372,31 @@ __device__ __forceinline__ void split_hi_lo(float v, uint32_t &hi, uint32_t &lo)
     lo = f32_to_bf16_bits(v - __uint_as_float((uint32_t)h << 16));
 }
 
-// This CTA's share of the shrink work units (h = A_s x, shrink.cuh); one
-// fence publishes them all, then each unit's bucket counter is bumped.
+constexpr int UNIT_BATCH = 64; // shrink units whose metadata is built at once
+
+// This CTA's share of the shrink work units (h = A_s x, shrink.cuh): the
+// metadata of up to UNIT_BATCH units is built in parallel (one thread each:
+// bucket search, table and perm reads) into shared memory, then the units run
+// back to back. One fence publishes them all, then each unit's bucket counter
+// is bumped.
 __device__ __forceinline__ void epi_shrink(const Params &p, const int32_t *unit_off, const int32_t *seg_off,
-                                           float *red, int et)
+                                           float *red, UnitMeta *um, int et)
 {
     const int nb = p.E * (p.L + 1);
     const int total_units = unit_off[nb];
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x)
-        shrink_unit(p, locate_unit(p, u, unit_off, seg_off), et >> 5, et & 31, red, 1);
-    if (blockIdx.x < total_units) {
+    const int mine = total_units > (int)blockIdx.x ? (total_units - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    for (int k0 = 0; k0 < mine; k0 += UNIT_BATCH) {
+        const int nk = min(UNIT_BATCH, mine - k0);
+        if (et < nk)
+            um[et] = unit_meta(p, (int)blockIdx.x + (k0 + et) * (int)gridDim.x, unit_off, seg_off);
+        named_bar_sync(1, EPI_THREADS);
+        for (int k = 0; k < nk; ++k)
+            shrink_unit(p, um[k], et >> 5, et & 31, red, 1);
         __threadfence();
         named_bar_sync(1, EPI_THREADS);
-        for (int u = blockIdx.x + et * gridDim.x; u < total_units; u += EPI_THREADS * gridDim.x)
-            atomicAdd(p.ws.done + locate_unit(p, u, unit_off, seg_off).b, 1);
+        if (et < nk)
+            atomicAdd(p.ws.done + um[et].b, 1);
+        named_bar_sync(1, EPI_THREADS); // um is rewritten by the next batch
     }
 }
 
@@ -414,8 +425,9 @@ __device__ __forceinline__ void stage_b(const Params &p, const EpiAux *aux, uint
 
 // XH rows 0..nmma-1 of the round [r0k, r0k + kr): s_t * h_t in column t's
 // slot range (hi, and lo = the bf16 remainder when hl = 2), zero elsewhere.
-// First every chunk of the round is zeroed, then thread et writes the data
-// chunks of columns et, et + 128 with all its h loads issued together.
+// First every chunk of the round is zeroed; then each column's data chunks
+// are split over 128 / nmma threads, each issuing the loads of up to four
+// chunks (every K part of h) before converting any.
 __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const EpiAux *aux, uint8_t *XH,
                                         const TileInfo &ti, int nmma, int r0k, int kr, int et)
 {
@@ -432,7 +444,10 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
     }
     named_bar_sync(1, EPI_THREADS);
     const size_t part_stride = (size_t)p.rows * p.R;
-    for (int j = et; j < ti.cnt; j += EPI_THREADS) {
+    // tpc threads per column (a power of two), each taking every tpc-th chunk
+    const int tpc = nmma >= EPI_THREADS ? 1 : EPI_THREADS / nmma;
+    const int sub = et % tpc;
+    for (int j = et / tpc; j < ti.cnt; j += EPI_THREADS / tpc) {
         const int ko = aux->koff[j];
         if (ko < 0)
             continue;
@@ -441,37 +456,38 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
         // ranks r (multiples of 8, r < rank) of this slot that fall in the round
         const int rlo = max(0, r0k - ko), rhi = min(rk, r0k + kr - ko);
         const float *hrow = p.ws.h + (size_t)(ti.r0 + j) * p.R;
-        for (int r = rlo; r < rhi; r += 64) {
-            float4 a[8], b[8];
+        for (int r = rlo + 8 * sub; r < rhi; r += 32 * tpc) {
+            float4 a[4], b[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int rr = min(r + 8 * q, rhi - 1) & ~7; // clamped: loads stay in the row
-                const float *h = hrow + rr;
-                a[q] = __ldcg(reinterpret_cast<const float4 *>(h));
-                b[q] = __ldcg(reinterpret_cast<const float4 *>(h + 4));
+            for (int u = 0; u < 4; ++u) {
+                const int rr = r + 8 * tpc * u;
+                a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                b[u] = a[u];
+                if (rr < rhi) {
 #pragma unroll
-                for (int kq = 1; kq < 4; ++kq) {
-                    const float *hq = h + (size_t)min(kq, p.kp - 1) * part_stride;
-                    const float4 c4 = __ldcg(reinterpret_cast<const float4 *>(hq));
-                    const float4 d4 = __ldcg(reinterpret_cast<const float4 *>(hq + 4));
-                    const bool use = kq < p.kp;
-                    a[q].x += use ? c4.x : 0.0f; a[q].y += use ? c4.y : 0.0f;
-                    a[q].z += use ? c4.z : 0.0f; a[q].w += use ? c4.w : 0.0f;
-                    b[q].x += use ? d4.x : 0.0f; b[q].y += use ? d4.y : 0.0f;
-                    b[q].z += use ? d4.z : 0.0f; b[q].w += use ? d4.w : 0.0f;
+                    for (int kq = 0; kq < 4; ++kq) {
+                        if (kq < p.kp) { // parts summed in part order
+                            const float *h = hrow + (size_t)kq * part_stride + rr;
+                            const float4 c4 = __ldcg(reinterpret_cast<const float4 *>(h));
+                            const float4 d4 = __ldcg(reinterpret_cast<const float4 *>(h + 4));
+                            a[u].x += c4.x; a[u].y += c4.y; a[u].z += c4.z; a[u].w += c4.w;
+                            b[u].x += d4.x; b[u].y += d4.y; b[u].z += d4.z; b[u].w += d4.w;
+                        }
+                    }
                 }
             }
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                if (r + 8 * q >= rhi)
+            for (int u = 0; u < 4; ++u) {
+                const int rr = r + 8 * tpc * u;
+                if (rr >= rhi)
                     break;
-                const float v[8] = {a[q].x * s, a[q].y * s, a[q].z * s, a[q].w * s,
-                                    b[q].x * s, b[q].y * s, b[q].z * s, b[q].w * s};
+                const float v[8] = {a[u].x * s, a[u].y * s, a[u].z * s, a[u].w * s,
+                                    b[u].x * s, b[u].y * s, b[u].z * s, b[u].w * s};
                 uint32_t h8[8], l8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     split_hi_lo(v[i], h8[i], l8[i]);
-                const int cq = (ko + r + 8 * q - r0k) >> 3;
+                const int cq = (ko + rr - r0k) >> 3;
                 uint8_t *dst = XH + (uint32_t)(cq >> 3) * xh_block + j * 128 + (((cq & 7) ^ (j & 7)) << 4);
                 *reinterpret_cast<uint4 *>(dst) = make_uint4(h8[0] | (h8[1] << 16), h8[2] | (h8[3] << 16),
                                                              h8[4] | (h8[5] << 16), h8[6] | (h8[7] << 16));
@@ -504,13 +520,23 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
     int32_t *unit_off = reinterpret_cast<int32_t *>(smem + c.meta_off); // copies of the routing
     int32_t *seg_off = unit_off + nb + 1;                                 // results, in shared memory
     float *red = reinterpret_cast<float *>(smem + c.red_off);
+    UnitMeta *um = reinterpret_cast<UnitMeta *>(smem + c.umeta_off);
 
-    grid_dependency_wait();
-    for (int q = et; q <= nb; q += EPI_THREADS) {
-        unit_off[q] = p.ws.unit_off[q];
-        seg_off[q] = p.ws.seg_off[q];
-    }
-    named_bar_sync(1, EPI_THREADS);
+    // With token tiles known on the host, the first item's column scan and B
+    // copies need nothing from the routing kernel: the wait for it (and the
+    // copy of its bucket tables) comes just before this CTA's shrink units.
+    bool routed = false;
+    auto route_wait = [&]() {
+        grid_dependency_wait();
+        for (int q = et; q <= nb; q += EPI_THREADS) {
+            unit_off[q] = p.ws.unit_off[q];
+            seg_off[q] = p.ws.seg_off[q];
+        }
+        named_bar_sync(1, EPI_THREADS);
+        routed = true;
+    };
+    if (c.static_tiles < 0)
+        route_wait();
 
     const int total = item_total(p, c);
     bool shrink_done = false;
@@ -583,6 +609,12 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         }
         named_bar_sync(1, EPI_THREADS);
         const int mode = aux->n_on > 0 ? 1 : 0;
+        if (kx > c.xblk * 64 && n < p.N) {
+            // B rows of the later rounds: warm them in L2 now
+            for (int e = 0; e < nent; ++e)
+                if (aux->ent_off[e] + aux->ent_rank[e] > c.xblk * 64)
+                    prefetch_l2(aux->ent_b[e] + (size_t)n * p.R);
+        }
 
         // (3) expand rounds: k range [r0k, r0k + kr) of the concatenated slots
         int r0k = 0;
@@ -597,7 +629,9 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
             if (kr > 0)
                 stage_b(p, aux, XB, nent, r0k, kr, n, et);
             if (!shrink_done) {
-                epi_shrink(p, unit_off, seg_off, red, et);
+                if (!routed)
+                    route_wait();
+                epi_shrink(p, unit_off, seg_off, red, um, et);
                 shrink_done = true;
             }
             if (r0k == 0 && nent > 0) { // the shrink of the staged slots has finished
@@ -713,8 +747,11 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         }
         named_bar_sync(1, EPI_THREADS); // per-item state is rewritten by the next item
     }
-    if (!shrink_done) // a CTA without items still runs its shrink units
-        epi_shrink(p, unit_off, seg_off, red, et);
+    if (!shrink_done) { // a CTA without items still runs its shrink units
+        if (!routed)
+            route_wait();
+        epi_shrink(p, unit_off, seg_off, red, um, et);
+    }
 }
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -747,6 +784,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     if (warp == 2)
         tmem_alloc(&bars->tmem_base, c.tmem_cols);
+    if (warp >= 4 && c.static_tiles >= 0) {
+        // warm L2 with what the epilogue reads first: its first tile's slots
+        // and the slot tables (one line of 32 entries per thread)
+        const int et = threadIdx.x - (TC_THREADS - EPI_THREADS);
+        const int r0 = (blockIdx.x / c.csplit) / c.n_tiles * c.tn;
+        if (et < c.tn && r0 + et < p.rows && (et & 31) == 0)
+            prefetch_l2(p.seq_slot + r0 + et);
+        for (int s = et * 32; s < p.L; s += EPI_THREADS * 32) {
+            prefetch_l2(p.tab[0].a_table + s);
+            prefetch_l2(p.tab[0].b_table + s);
+            prefetch_l2(p.tab[0].scale_table + s);
+            prefetch_l2(p.tab[0].rank_table + s);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -819,6 +870,8 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
     o = c.meta_off + 2u * (uint32_t)(p.E * (p.L + 1) + 1) * 4u;
     c.red_off = align_up(o, 16);
     o = c.red_off + (uint32_t)(SHRINK_WARPS * 32 * 4);
+    c.umeta_off = align_up(o, 16);
+    o = c.umeta_off + (uint32_t)(UNIT_BATCH * sizeof(UnitMeta));
     c.bar_off = align_up(o, 16);
     c.smem_bytes = 1024u + c.bar_off + (uint32_t)sizeof(Bars);
     c.tmem_cols = c.borrow ? 512u : pow2_at_least(3u * (uint32_t)c.tn);

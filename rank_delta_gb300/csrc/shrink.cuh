@@ -2,11 +2,11 @@
 // `LoraDelta::project`), as work units over the routing sort.
 //
 // A unit is (bucket b, rank group of 8, up to 4 rows of that bucket, one of
-// kp parts of K): four warps, warp w taking ranks 8g+2w and 8g+2w+1, lanes
-// splitting the K part in 8-element (16-byte) vectors, 4 rows per pass with
-// four K steps in flight. Each slot's A rows are read once per 16 rows rather
-// than once per row... Part q writes its partial sums to h[q][row][r] (fp32);
-// readers add the kp parts in part order, so h is the same on every run.
+// kp parts of K): four warps splitting the K part, lanes taking 8-element
+// (16-byte) vectors, each lane accumulating 8 ranks x 4 rows. A slot's A rows
+// are read once per 4 rows rather than once per row. Part q writes its
+// partial sums to h[q][row][r] (fp32); readers add the kp parts in part
+// order, so h is the same on every run.
 // Ranks between the adapter's rank and the next multiple of 8 are written as
 // zero so the expand can run in 8-wide vectors.
 #pragma once
@@ -83,70 +83,91 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
-// Unit l, executed by SHRINK_WARPS warps (w = 0..3) of one group that shares
+// What a unit needs before its loads can start: A of its slot and its x
+// rows. Built once per unit (table and perm reads) so that the loads of the
+// unit itself depend on nothing but these fields.
+struct UnitMeta {
+    const uint16_t *A;       // A of the slot, [R][K]
+    int32_t row[SHRINK_TC];  // x rows of the unit (the last one repeated past nrows)
+    int16_t b, rank, rg, kpart, nrows, pad;
+};
+
+__device__ __forceinline__ UnitMeta unit_meta(const Params &p, int u, const int32_t *unit_off,
+                                              const int32_t *seg_off)
+{
+    const UnitLoc l = locate_unit(p, u, unit_off, seg_off);
+    UnitMeta m;
+    m.A = p.tab[l.e].a_table[l.s];
+#pragma unroll
+    for (int j = 0; j < SHRINK_TC; ++j)
+        m.row[j] = p.ws.perm[l.r0 + min(j, l.nrows - 1)];
+    m.b = (int16_t)l.b;
+    m.rank = (int16_t)l.rank;
+    m.rg = (int16_t)l.rg;
+    m.kpart = (int16_t)l.kpart;
+    m.nrows = (int16_t)l.nrows;
+    m.pad = 0;
+    return m;
+}
+
+// Unit m, executed by SHRINK_WARPS warps (w = 0..3) of one group that shares
 // named barrier `bar_id` and the float scratch `red` [SHRINK_WARPS][32]: the
 // warps split the unit's K part in four, each lane accumulating 8 ranks x 4
 // rows over its 8-element K slices so every load of a pass is in flight at
 // once; lane sums are reduce-scattered, then the four warps' sums are added
 // (warp order) and written to h.
-__device__ __forceinline__ void shrink_unit(const Params &p, const UnitLoc &l, int w, int lane,
+__device__ __forceinline__ void shrink_unit(const Params &p, const UnitMeta &m, int w, int lane,
                                             float *red, int bar_id)
 {
-    const uint16_t *A = p.tab[l.e].a_table[l.s];
     int kb, ke;
-    kpart_range(p.K, p.kp, l.kpart, kb, ke);
+    kpart_range(p.K, p.kp, m.kpart, kb, ke);
     // this warp's quarter of the K part, in whole 256-element steps
     const int steps = (ke - kb + 255) / 256;
     const int s0 = kb + (steps * w / SHRINK_WARPS) * 256, s1 = min(ke, kb + (steps * (w + 1) / SHRINK_WARPS) * 256);
     const uint16_t *arow[SHRINK_RG];
 #pragma unroll
     for (int r = 0; r < SHRINK_RG; ++r) {
-        const int rr = l.rg * SHRINK_RG + r;
-        arow[r] = A + (size_t)(rr < l.rank ? rr : 0) * p.K;
+        const int rr = m.rg * SHRINK_RG + r;
+        arow[r] = m.A + (size_t)(rr < m.rank ? rr : 0) * p.K;
     }
-    float *hpart = p.ws.h + (size_t)l.kpart * p.rows * p.R;
-    for (int pass = 0; pass * 4 < l.nrows; ++pass) {
-        const int nr = min(4, l.nrows - pass * 4);
-        int row[4];
-        const uint16_t *xr[4];
+    float *hpart = p.ws.h + (size_t)m.kpart * p.rows * p.R;
+    const int nr = m.nrows;
+    const uint16_t *xr[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            row[j] = p.ws.perm[l.r0 + pass * 4 + min(j, nr - 1)];
-            xr[j] = p.x + (int64_t)row[j] * p.x_stride;
-        }
-        float acc[32]; // [rank][row]
+    for (int j = 0; j < 4; ++j)
+        xr[j] = p.x + (int64_t)m.row[j] * p.x_stride;
+    float acc[32]; // [rank][row]
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-            acc[i] = 0.0f;
+    for (int i = 0; i < 32; ++i)
+        acc[i] = 0.0f;
 #pragma unroll 2
-        for (int k0 = s0 + lane * 8; k0 < s1; k0 += 256) {
-            uint4 xv[4], av[SHRINK_RG];
+    for (int k0 = s0 + lane * 8; k0 < s1; k0 += 256) {
+        uint4 xv[4], av[SHRINK_RG];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            xv[j] = ld_nc_16(xr[j] + k0); // rows past nrows repeat the last row; their sums are dropped
+#pragma unroll
+        for (int r = 0; r < SHRINK_RG; ++r)
+            av[r] = ld_nc_16(arow[r] + k0); // ranks past the rank read row 0; their sums are dropped
+#pragma unroll
+        for (int r = 0; r < SHRINK_RG; ++r)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                xv[j] = j < nr ? ld_nc_16(xr[j] + k0) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int r = 0; r < SHRINK_RG; ++r)
-                av[r] = l.rg * SHRINK_RG + r < l.rank ? ld_nc_16(arow[r] + k0) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int r = 0; r < SHRINK_RG; ++r)
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    acc[r * 4 + j] = dot8_acc(acc[r * 4 + j], av[r], xv[j]);
-        }
-        const float mine = warp_reduce_scatter32(acc, lane); // lane = rank * 4 + row
-        red[w * 32 + lane] = mine;
-        named_bar_sync(bar_id, SHRINK_WARPS * 32);
-        if (w == 0) {
-            float t = red[lane];
-#pragma unroll
-            for (int q = 1; q < SHRINK_WARPS; ++q)
-                t += red[q * 32 + lane];
-            const int r = l.rg * SHRINK_RG + lane / 4, j = lane % 4;
-            if (j < nr)
-                hpart[(size_t)row[j] * p.R + r] = r < l.rank ? t : 0.0f;
-        }
-        named_bar_sync(bar_id, SHRINK_WARPS * 32);
+                acc[r * 4 + j] = dot8_acc(acc[r * 4 + j], av[r], xv[j]);
     }
+    const float mine = warp_reduce_scatter32(acc, lane); // lane = rank * 4 + row
+    red[w * 32 + lane] = mine;
+    named_bar_sync(bar_id, SHRINK_WARPS * 32);
+    if (w == 0) {
+        float t = red[lane];
+#pragma unroll
+        for (int q = 1; q < SHRINK_WARPS; ++q)
+            t += red[q * 32 + lane];
+        const int r = m.rg * SHRINK_RG + lane / 4, j = lane % 4;
+        if (j < nr)
+            hpart[(size_t)m.row[j] * p.R + r] = r < m.rank ? t : 0.0f;
+    }
+    named_bar_sync(bar_id, SHRINK_WARPS * 32);
 }
 
 // h[row][r..r+8) summed over the kp parts (part order), for readers running

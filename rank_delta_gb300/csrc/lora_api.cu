@@ -374,7 +374,9 @@ lora_status check_io(const char *who, const void *x, int64_t x_stride, int rows,
 }
 
 // Tensor-core path: prep (routing sort, work lists) then one fused launch
-// (shrink, base product, expand-fold). CUDA-core path: prep, shrink, GEMV.
+// (shrink, base product, expand-fold); from TC_SHRINK_MIN_ROWS rows the
+// shrink is a tensor-core launch of its own between the two. CUDA-core
+// path: prep, shrink, GEMV.
 lora_status run(Params &p, int path, cudaStream_t st, const char *who)
 {
     DevInfo di;
@@ -401,6 +403,15 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
                           (uint32_t)plan.tn);
         if (!ok)
             return fail(LORA_ERR_CUDA, "%s: encoding the x tensor map failed", who);
+        if (!moe && p.rows >= TC_SHRINK_MIN_ROWS) {
+            // h from the tensor-core shrink kernel: whole K, one part, no work units
+            CUtensorMap xm;
+            if (!make_map(&xm, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64, 128))
+                return fail(LORA_ERR_CUDA, "%s: encoding the x tensor map of the shrink failed", who);
+            e = launch_shrink_tc(p, xm, di.num_sms, st);
+            if (e != cudaSuccess)
+                return cuda_fail(e, who);
+        }
         for (int q = 0; q < p.E; ++q) {
             if (plan.use3d)
                 ok = make_map_3d(&maps.w[q], p.W[q], (uint64_t)p.K, (uint64_t)p.N, (uint64_t)p.K, 128,
@@ -465,6 +476,10 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
     if (path == LORA_PATH_AUTO)
         path = M <= SIMT_MAX_ROWS ? LORA_PATH_SIMT : LORA_PATH_TC;
     p.tn = tc_token_tile(M);
+    if (path == LORA_PATH_TC && M >= TC_SHRINK_MIN_ROWS) {
+        p.kp = 1; // the tensor-core shrink writes h over the whole K
+        p.no_units = 1;
+    }
     return run(p, path, reinterpret_cast<cudaStream_t>(stream), who);
 }
 

@@ -73,6 +73,7 @@ struct Params {
     int tn;   // token tile of the tensor-core path (rows per tile)
     int kp;   // K parts of a shrink unit (h is summed over them)
     int ncnt; // split-K tile counters the prep kernel clears
+    int no_units; // 1: h comes from the tensor-core shrink kernel (no shrink work units)
     const uint16_t *W[MAX_E];
     Tables tab[MAX_E];
     Ws ws;
@@ -122,6 +123,11 @@ struct TmapSet {
 cudaError_t launch_prep(const Params &p, cudaStream_t st);
 cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st);
 cudaError_t launch_simt(const Params &p, int num_sms, cudaStream_t st);
+// Tensor-core shrink (lora_shrink_tc.cu); xmap: x with 64 x 128 boxes.
+cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, int num_sms, cudaStream_t st);
+// Rows from which a projection call computes h with the tensor-core shrink
+// kernel (one CTA per 128 rows: enough tiles to spread over the SMs).
+constexpr int TC_SHRINK_MIN_ROWS = 2048;
 // Shape of one tensor-core launch: token tile, 64-wide K chunks per pipeline
 // stage, stages, K parts, whether the 3D tensor-map view (K a multiple of 64)
 // is used, and the expand's staging buffers.

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
     // Shrink work list from the bucket sizes (shared memory only).
     {
         int units = 0;
-        if (tid < nb && brank[tid] > 0 && cnt[tid] > 0)
+        if (tid < nb && brank[tid] > 0 && cnt[tid] > 0 && !p.no_units)
             units = bucket_units(brank[tid], cnt[tid], p.kp);
         int total;
         int ex = block_exclusive_scan(units, warp_tot, total);

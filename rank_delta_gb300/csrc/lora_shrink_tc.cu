@@ -1,0 +1,289 @@
+// Tensor-core shrink h_t = A_{s_t} x_t for batches of many rows (ferrox-core
+// `weight_matrix/lora.rs`, `LoraDelta::project`: the rank-sized projection of
+// each row through its own adapter's A).
+//
+// One CTA per tile of 128 rows of x (UMMA M = 128: TMEM lane t is row t of
+// the tile). The adapted slots present in the tile are stacked along UMMA N,
+// Rs = max_rank rounded up to 16 columns each, up to 256 columns per group:
+//   D[t, i*Rs + r] = sum_k x[t, k] A_{slot_i}[r, k]
+// so a tile whose rows share one adapter (a prefill sequence) costs one
+// 128 x Rs x K product. x tiles arrive by TMA; the A rows are copied with
+// cp.async through the slot pointer table (a_table), into the same 128-byte
+// swizzled K-major layout. The epilogue keeps, for row t, the Rs columns of
+// its own slot and writes them to h[t][0..R) in fp32 -- with K unsplit, so h
+// has one part and needs no summing.
+//
+// Roles (192 threads): warp 0 issues the x copies, warp 1 owns TMEM and
+// issues the UMMAs, warps 2..5 copy A rows and then drain TMEM (warp w reads
+// lanes 32 (w % 4)..+31). Every wait is bounded (LORA_FLAG_WAIT_TIMEOUT).
+//
+// Launched between the routing kernel and the projection kernel, with
+// programmatic dependent launch: it lets the projection kernel start at once,
+// and before it exits it waits for the routing kernel, so a kernel that waits
+// for this one also sees the routing results.
+#include "lora_internal.cuh"
+#include "ptx.cuh"
+#include "vec.cuh"
+
+namespace rd {
+
+constexpr int STC_M = 128;
+constexpr int STC_THREADS = 192;
+constexpr int STC_LOADERS = 128;
+constexpr int STC_MAX_N = 256;
+constexpr int STC_STAGES = 4;
+constexpr uint32_t STC_X_BYTES = STC_M * 128u;       // 128 rows x 64 bf16
+constexpr uint32_t STC_A_BYTES = STC_MAX_N * 128u;   // up to 256 A rows x 64 bf16
+constexpr uint32_t STC_STAGE_BYTES = STC_X_BYTES + STC_A_BYTES;
+
+struct StcShared {
+    uint64_t full[STC_STAGES];
+    uint64_t empty[STC_STAGES];
+    uint64_t acc_full;
+    uint64_t acc_empty;
+    uint32_t tmem_base;
+    int abort_flag;
+    int nslots;
+    int16_t tslot[STC_M];            // slot of row t when it takes a delta, else -1
+    int16_t slot_list[STC_M];        // the tile's adapted slots, ascending
+    int16_t slot_rank[STC_M];
+    const uint16_t *slot_a[STC_M];
+    int32_t used[1024];              // per slot: row count in this tile, then its list index
+    int32_t wsum[STC_THREADS / 32];
+};
+
+constexpr uint32_t STC_SMEM = 1024 + STC_STAGES * STC_STAGE_BYTES + sizeof(StcShared);
+
+__device__ __forceinline__ void stc_abort(const Params &p, StcShared *sh)
+{
+    *(volatile int *)&sh->abort_flag = 1;
+    atomicOr(p.ws.status, (uint32_t)LORA_FLAG_WAIT_TIMEOUT);
+}
+
+__device__ __forceinline__ bool stc_aborted(StcShared *sh) { return *(volatile int *)&sh->abort_flag != 0; }
+
+__global__ void __launch_bounds__(STC_THREADS, 1)
+    shrink_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ Params p, int Rs)
+{
+    extern __shared__ uint8_t stc_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(stc_raw) + 1023) & ~uintptr_t(1023));
+    StcShared *sh = reinterpret_cast<StcShared *>(smem + STC_STAGES * STC_STAGE_BYTES);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = STC_MAX_N / Rs; // slots per UMMA group
+    const int kchunks = (p.K + 63) / 64;
+
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid == 0) {
+        for (int i = 0; i < STC_STAGES; ++i) {
+            mbar_init(sh->full + i, 1 + STC_LOADERS); // the x copy + every A loader
+            mbar_init(sh->empty + i, 1);
+        }
+        mbar_init(&sh->acc_full, 1);
+        mbar_init(&sh->acc_empty, STC_LOADERS);
+        sh->abort_flag = 0;
+        fence_barrier_init();
+        prefetch_tmap(&xmap);
+    }
+    if (warp == 1)
+        tmem_alloc(&sh->tmem_base, STC_MAX_N);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+
+    // pipeline positions, carried across groups and tiles by each role
+    int gx = 0, gm = 0, ga = 0, groups_done = 0;
+    const int ntiles = (p.rows + STC_M - 1) / STC_M;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int r0 = tile * STC_M;
+        // (1) the tile's adapted slots, ascending (every thread takes part)
+        for (int s = tid; s < p.L; s += STC_THREADS)
+            sh->used[s] = 0;
+        __syncthreads();
+        if (tid < STC_M) {
+            int sl = -1;
+            if (r0 + tid < p.rows) {
+                const int s = p.seq_slot[r0 + tid];
+                const SlotInfo si = slot_info(p.tab[0], s, p.L);
+                if (si.on) {
+                    sl = s;
+                    sh->used[s] = 1;
+                }
+            }
+            sh->tslot[tid] = (int16_t)sl;
+        }
+        __syncthreads();
+        {
+            const int per = (p.L + STC_THREADS - 1) / STC_THREADS;
+            const int s0 = min(p.L, tid * per), s1 = min(p.L, s0 + per);
+            int cnt = 0;
+            for (int s = s0; s < s1; ++s)
+                cnt += sh->used[s];
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += v;
+            }
+            if (lane == 31)
+                sh->wsum[warp] = incl;
+            __syncthreads();
+            int ex = incl - cnt, total = 0;
+            for (int q = 0; q < STC_THREADS / 32; ++q) {
+                if (q < warp)
+                    ex += sh->wsum[q];
+                total += sh->wsum[q];
+            }
+            for (int s = s0; s < s1; ++s)
+                if (sh->used[s]) {
+                    sh->slot_list[ex] = (int16_t)s;
+                    sh->slot_a[ex] = p.tab[0].a_table[s];
+                    sh->slot_rank[ex] = (int16_t)p.tab[0].rank_table[s];
+                    sh->used[s] = ex;
+                    ++ex;
+                }
+            if (tid == 0)
+                sh->nslots = total;
+        }
+        __syncthreads();
+        const int nslots = sh->nslots;
+        const int ngroups = (nslots + G - 1) / G;
+
+        for (int grp = 0; grp < ngroups; ++grp, ++groups_done) {
+            const int gs = min(G, nslots - grp * G);
+            const int N = gs * Rs;
+            if (warp == 0) {
+                if (lane == 0) { // x copies
+                    for (int kc = 0; kc < kchunks; ++kc, ++gx) {
+                        const int st = gx % STC_STAGES;
+                        if (stc_aborted(sh) || !mbar_wait(sh->empty + st, ((uint32_t)(gx / STC_STAGES) & 1u) ^ 1u)) {
+                            stc_abort(p, sh);
+                            break;
+                        }
+                        mbar_arrive_expect_tx(sh->full + st, STC_X_BYTES);
+                        tma_load_2d(smem + (size_t)st * STC_STAGE_BYTES, &xmap, kc * 64, r0, sh->full + st);
+                    }
+                }
+            } else if (warp == 1) {
+                if (lane == 0) { // UMMAs
+                    const uint32_t idesc = idesc_bf16_f32(STC_M, (uint32_t)N);
+                    bool ok = mbar_wait(&sh->acc_empty, ((uint32_t)groups_done & 1u) ^ 1u);
+                    if (!ok)
+                        stc_abort(p, sh);
+                    tc_fence_after();
+                    uint32_t acc = 0;
+                    for (int kc = 0; ok && kc < kchunks; ++kc, ++gm) {
+                        const int st = gm % STC_STAGES;
+                        if (stc_aborted(sh) || !mbar_wait(sh->full + st, (uint32_t)(gm / STC_STAGES) & 1u)) {
+                            stc_abort(p, sh);
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t xs = smem_u32(smem + (size_t)st * STC_STAGE_BYTES);
+                        const uint32_t as = xs + STC_X_BYTES;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            umma_bf16(tmem, sw128_kmajor_desc(xs + j * 32), sw128_kmajor_desc(as + j * 32), idesc, acc);
+                            acc = 1;
+                        }
+                        umma_commit(sh->empty + st);
+                    }
+                    umma_commit(&sh->acc_full);
+                }
+            } else {
+                // A rows of the group's slots: row n = i * Rs + rr of the stage is
+                // row rr of A of slot (grp * G + i); rows past the rank, and K past
+                // the end, are zero-filled
+                const int et = tid - 64;
+                for (int kc = 0; kc < kchunks; ++kc, ++ga) {
+                    const int st = ga % STC_STAGES;
+                    if (stc_aborted(sh) || !mbar_wait(sh->empty + st, ((uint32_t)(ga / STC_STAGES) & 1u) ^ 1u)) {
+                        stc_abort(p, sh);
+                        break;
+                    }
+                    uint8_t *as = smem + (size_t)st * STC_STAGE_BYTES + STC_X_BYTES;
+                    for (int idx = et; idx < N * 8; idx += STC_LOADERS) {
+                        const int n = idx >> 3, c = idx & 7;
+                        const int i = n / Rs, rr = n - i * Rs;
+                        const int li = grp * G + i;
+                        const int k = kc * 64 + c * 8;
+                        const bool has = rr < sh->slot_rank[li] && k < p.K;
+                        const uint16_t *src = sh->slot_a[li] + (has ? (size_t)rr * p.K + k : 0);
+                        cp_async_16(as + n * 128 + ((c ^ (n & 7)) << 4), src, has ? 16u : 0u);
+                    }
+                    cp_async_wait_all();
+                    fence_proxy_async_smem(); // generic-proxy copies, read by the UMMAs
+                    mbar_arrive(sh->full + st);
+                }
+                // epilogue: row t keeps the columns of its own slot
+                const bool got = mbar_wait(&sh->acc_full, (uint32_t)groups_done & 1u);
+                tc_fence_after();
+                if (!got)
+                    stc_abort(p, sh);
+                const int t = 32 * (warp & 3) + lane;
+                const uint32_t taddr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+                const int sl = sh->tslot[t];
+                const int li = sl >= 0 ? sh->used[sl] : -1;
+                const int i = li - grp * G; // this row's slot block in the group, if any
+                const int rank = li >= 0 ? sh->slot_rank[li] : 0;
+                float *hrow = p.ws.h + (size_t)(r0 + t) * p.R;
+                const bool skip = __any_sync(0xffffffffu, stc_aborted(sh)); // warp-uniform: the loads are collective
+                for (int c0 = 0; c0 < N && !skip; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + (uint32_t)c0, v);
+                    const int r = c0 - i * Rs; // rank of column c0 for this row's slot
+                    if (i >= 0 && i < gs && r >= 0 && r < Rs && r0 + t < p.rows) {
+#pragma unroll
+                        for (int q = 0; q < 16; q += 4)
+                            if (r + q < p.R)
+                                *reinterpret_cast<float4 *>(hrow + r + q) =
+                                    make_float4(r + q + 0 < rank ? v[q + 0] : 0.0f, r + q + 1 < rank ? v[q + 1] : 0.0f,
+                                                r + q + 2 < rank ? v[q + 2] : 0.0f, r + q + 3 < rank ? v[q + 3] : 0.0f);
+                    }
+                }
+                tc_fence_before();
+                mbar_arrive(&sh->acc_empty);
+            }
+        }
+        __syncthreads(); // the tile's slot lists are rewritten by the next tile
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, STC_MAX_N);
+    }
+    // a kernel that waits for this one also sees the routing kernel's results
+    grid_dependency_wait();
+}
+
+cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, int num_sms, cudaStream_t st)
+{
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(shrink_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)STC_SMEM);
+        if (e != cudaSuccess)
+            return e;
+        attr_set = true;
+    }
+    const int Rs = (p.R + 15) & ~15;
+    const int ntiles = (p.rows + STC_M - 1) / STC_M;
+    int grid = ntiles < num_sms ? ntiles : num_sms;
+    if (grid < 1)
+        grid = 1;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(STC_THREADS);
+    cfg.dynamicSmemBytes = STC_SMEM;
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, shrink_tc_kernel, xmap, p, Rs);
+}
+
+} // namespace rd

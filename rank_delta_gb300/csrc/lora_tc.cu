@@ -24,12 +24,12 @@
 // and the MMA warp issues D'[n, t] = sum_k XB[n, k] XH[t, k] (UMMA M=128,
 // N=tokens, K=16 per instruction). D' goes to its own TMEM columns and the
 // epilogue adds it only to the columns that take a delta, so a row with no
-// delta is the base product byte for byte, and an adapted row is base + D'
-// whatever else the tile holds (a row gives the same bits alone or in a
-// batch). D' has TMEM columns of its own when three token tiles fit in the
-// 512 columns; otherwise it borrows the other accumulator, and the next item
-// waits for this one's drain. When the staged k range exceeds the buffers,
-// the expand runs in several rounds.
+// delta is the base product byte for byte. D' has TMEM columns of its own
+// when three token tiles fit in the 512 columns. Otherwise (tiles of more
+// than 170 rows): when every row of the tile takes its delta here, D'
+// accumulates straight into the base accumulator; else it borrows the other
+// accumulator and the next item waits for this one's drain. When the staged
+// k range exceeds the buffers, the expand runs in several rounds.
 //
 // Warp roles (256 threads):
 //   warps 0, 1   TMA producers of W (even / odd pipeline stages): 3D boxes
@@ -100,7 +100,7 @@ struct EpiAux {
     uint32_t onbits[MAX_TN / 32];    // bit j: column j takes its delta here
     int32_t wsum[2][4];              // scan scratch: per-warp totals
     int32_t n_on;
-    int32_t xr_mode;                 // 0 no expand, 1 expand into D'
+    int32_t xr_mode;                 // 0 no expand, 1 into D', 2 into the base accumulator
     int32_t xr_nk16, xr_last;        // K=16 steps of this round; last round of the item
 };
 
@@ -211,7 +211,7 @@ drain:
 
 
 // UMMAs of every item: the base product into accumulator it & 1, then the
-// expand rounds the epilogue stages, into D'.
+// expand rounds the epilogue stages (into D', or into the base accumulator).
 // Accumulator acquisitions are counted per buffer (acq), matching the
 // epilogue's releases in order: item i takes buffer i & 1 and, when its D'
 // borrows the other buffer, that one too.
@@ -290,8 +290,8 @@ __device__ __forceinline__ void issue_mma(const Params &p, const TcCfg &c, Bars 
                 tc_fence_after();
             }
             if (first)
-                dacc = tmem + (uint32_t)((c.borrow ? (buf ^ 1) : 2) * c.tn);
-            uint32_t dacc_on = first ? 0u : 1u;
+                dacc = mode == 2 ? acc : tmem + (uint32_t)((c.borrow ? (buf ^ 1) : 2) * c.tn);
+            uint32_t dacc_on = (mode == 2 || !first) ? 1u : 0u;
             for (int k = 0; k < nk16; ++k) {
                 const uint32_t koff = (uint32_t)(k >> 2) * XB_BLOCK + (uint32_t)(k & 3) * 32u;
                 const uint32_t hoff = (uint32_t)(k >> 2) * (uint32_t)c.tn * 128u + (uint32_t)(k & 3) * 32u;
@@ -608,7 +608,8 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
                 aux->koff[j] = aux->soff[sl];
         }
         named_bar_sync(1, EPI_THREADS);
-        const int mode = aux->n_on > 0 ? 1 : 0;
+        const int n_on = aux->n_on;
+        const int mode = n_on == 0 ? 0 : (c.borrow && n_on == ti.cnt ? 2 : 1);
         if (kx > c.xblk * 64 && n < p.N) {
             // B rows of the later rounds: warm them in L2 now
             for (int e = 0; e < nent; ++e)
@@ -679,9 +680,9 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         for (int c0 = 0; c0 < ti.cnt; c0 += 16) {
             uint32_t rb[16], rdl[16];
             tmem_ld16_nowait(tb + (uint32_t)c0, rb);
-            if (mode)
+            if (mode == 1)
                 tmem_ld16_nowait(td + (uint32_t)c0, rdl);
-            const uint32_t on16 = mode ? (aux->onbits[c0 >> 5] >> (c0 & 16)) & 0xFFFFu : 0u;
+            const uint32_t on16 = mode == 1 ? (aux->onbits[c0 >> 5] >> (c0 & 16)) & 0xFFFFu : 0u;
             tmem_wait_ld();
             float v[16];
 #pragma unroll
@@ -708,7 +709,7 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         named_bar_sync(1, EPI_THREADS);
         if (et == 0) {
             mbar_arrive(bars->acc_empty + buf);
-            if (mode && c.borrow)
+            if (mode == 1 && c.borrow)
                 mbar_arrive(bars->acc_empty + (buf ^ 1));
             if (C > 1)
                 atomicAdd(p.ws.tile_cnt + tile, 1);

@@ -177,3 +177,30 @@ def test_alpha_zero_and_rslora_scales_on_gpu():
     run = ProjRun(wl)
     for path in PATHS:
         assert_close(run.apply(path=path), oracle.workload_proj(wl), f"alpha/rslora path {path}")
+
+
+@pytest.mark.parametrize("M,K,N,L,R", [(2100, 200, 136, 5, 24), (2048, 320, 128, 40, 16),
+                                       (4096, 128, 64, 3, 64)])
+def test_large_batch_tensor_core_shrink(M, K, N, L, R):
+    """From 2048 rows h comes from the tensor-core shrink kernel: ragged row
+    tiles, K not a multiple of 64, a pool rank that is not a multiple of 16,
+    and tiles holding more slots than one UMMA group (16 slots of rank 16)."""
+    wl = workloads.random_small(seed=M + K + L, M=M, K=K, N=N, L=L, R=R)
+    run = ProjRun(wl)
+    y = run.apply(path=rd.LORA_PATH_TC)
+    assert run.last_status == 0
+    assert_close(y, oracle.workload_proj(wl), f"M{M} K{K} N{N} L{L} R{R}")
+    base = run.apply(slots=torch.full_like(run.slots, -1), path=rd.LORA_PATH_TC)
+    none = wl.seq_slot < 0
+    assert np.array_equal(y.view(np.uint16)[none], base.view(np.uint16)[none])
+
+
+def test_fully_adapted_wide_tiles_match_oracle():
+    """Token tiles of 256 rows leave no TMEM for a separate delta accumulator:
+    when every row of a tile is adapted the delta accumulates into the base
+    accumulator. All rows adapted here (no -1 slots), ragged last tile."""
+    wl = workloads.random_small(seed=600, M=600, K=192, N=160, L=4, R=32, p_none=0.0)
+    run = ProjRun(wl)
+    y = run.apply(path=rd.LORA_PATH_TC)
+    assert run.last_status == 0
+    assert_close(y, oracle.workload_proj(wl), "M600 all rows adapted")

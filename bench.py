@@ -44,6 +44,8 @@ DESCRIBE = {
            "4 adapters/expert r=16 alpha=32",
 }
 BOUND = {"tiny": "hbm", "decode": "hbm", "qkv": "hbm", "prefill": "tensor", "moe": "hbm"}
+# --small: the same kernels on fewer rows, for profiler captures only (never a bench line)
+SMALL = {"prefill": {"seq_len": 256}, "moe": {"tokens": 128}}
 
 
 def load_peaks():
@@ -233,6 +235,22 @@ class MoeSet:
                                self.rts, y, y.stride(0), self.ws, self.ws.numel(), stream)
 
 
+def max_over_ranks(ms: float, world: int, device: str) -> float:
+    """The slowest rank's time: every rank runs an independent replica, so the
+    job ends when the last one does."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(rows: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job rows/s: all ranks' rows over the slowest rank's time."""
+    return rows * steps * world / (elapsed_ms / 1e3)
+
+
 # kernels one call launches: the routing sort, then one fused tensor-core launch
 # (shrink + base + expand-fold); the CUDA-core path (<= 16 rows) runs the sort,
 # a shrink launch and the GEMV
@@ -252,7 +270,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     rd.lib()
     torch.cuda.set_device(local_rank)
-    wl = workloads.make(args.config)
+    wl = workloads.make(args.config, **(SMALL.get(args.config, {}) if args.small else {}))
     is_moe = args.config == "moe"
     rows = wl.T if is_moe else wl.M
     algo_bytes, algo_flops = moe_algorithmic(wl) if is_moe else proj_algorithmic(wl)
@@ -306,12 +324,9 @@ def run_ours(args, rank, world, local_rank):
 
     elapsed_ms = t_start.elapsed_time(t_end)
     call_ms = elapsed_ms / args.steps
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, world, "cuda")
     ms_per_step = elapsed_ms / args.steps
-    value = rows * args.steps * world / (elapsed_ms / 1e3)
+    value = job_rate(rows, args.steps, world, elapsed_ms)
     status = rd.lora_status_get(sets[0].ws)
 
     # end to end through the C ABI: pinned host x / seq_slot in, y out, every step
@@ -338,12 +353,8 @@ def run_ours(args, rank, world, local_rank):
         y_h.copy_(sets[k].y, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = rows * args.steps * world / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
+    e2e_value = job_rate(rows, args.steps, world, e2e_ms)
 
     hbm, tf_burst, tf_sus, peak_kind = load_peaks()
     avg_call_s = call_ms / 1e3
@@ -370,7 +381,8 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
         "config": {
-            "workload": DESCRIBE[args.config],
+            "workload": DESCRIBE[args.config] + (" [--small profiling case, not the benchmark]"
+                                                 if args.small and args.config in SMALL else ""),
             "rows_per_step": rows,
             "parallelism": f"replicas x{world} (rows shard, no collective)",
             "l2": f"rotating {nsets} buffer sets of {first.bytes / 1e6:.1f} MB (>= 3x L2)",
@@ -468,6 +480,8 @@ def main():
     ap.add_argument("--config", default="decode", choices=sorted(DESCRIBE))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--small", action="store_true",
+                    help="profiling case: prefill 2048 rows, MoE 128 tokens (not the benchmarked workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

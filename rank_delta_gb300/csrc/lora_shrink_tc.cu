@@ -195,8 +195,14 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
                 // A rows of the group's slots: row n = i * Rs + rr of the stage is
                 // row rr of A of slot (grp * G + i); rows past the rank, and K past
                 // the end, are zero-filled
+                // Each stage's copies form one cp.async group; a stage is
+                // signalled (after a proxy fence) once STC_STAGES - 1 later
+                // groups have been issued, so that many stages stay in flight.
                 const int et = tid - 64;
-                for (int kc = 0; kc < kchunks; ++kc, ++ga) {
+                constexpr int LAG = STC_STAGES - 1;
+                const int ga0 = ga;
+                int kc = 0;
+                for (; kc < kchunks; ++kc, ++ga) {
                     const int st = ga % STC_STAGES;
                     if (stc_aborted(sh) || !mbar_wait(sh->empty + st, ((uint32_t)(ga / STC_STAGES) & 1u) ^ 1u)) {
                         stc_abort(p, sh);
@@ -212,10 +218,18 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
                         const uint16_t *src = sh->slot_a[li] + (has ? (size_t)rr * p.K + k : 0);
                         cp_async_16(as + n * 128 + ((c ^ (n & 7)) << 4), src, has ? 16u : 0u);
                     }
-                    cp_async_wait_all();
-                    fence_proxy_async_smem(); // generic-proxy copies, read by the UMMAs
-                    mbar_arrive(sh->full + st);
+                    cp_async_commit();
+                    if (kc >= LAG) {
+                        cp_async_wait_group<LAG>();
+                        fence_proxy_async_smem(); // generic-proxy copies, read by the UMMAs
+                        mbar_arrive(sh->full + (ga - LAG) % STC_STAGES);
+                    }
                 }
+                // the last (up to LAG) stages issued
+                cp_async_wait_all();
+                fence_proxy_async_smem();
+                for (int q = max(0, kc - LAG); q < kc; ++q)
+                    mbar_arrive(sh->full + (ga0 + q) % STC_STAGES);
                 // epilogue: row t keeps the columns of its own slot
                 const bool got = mbar_wait(&sh->acc_full, (uint32_t)groups_done & 1u);
                 tc_fence_after();

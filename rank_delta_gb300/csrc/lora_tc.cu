@@ -77,7 +77,8 @@ struct TcCfg {
     int static_tiles; // total tiles when the host knows them, -1 when the prep kernel lists them
     int kchunks, kstages;
     int use3d;
-    int xblk;         // 64-wide k blocks of one expand round
+    int xblk;         // 64-wide k blocks of one expand round (dedicated buffers, region 0)
+    int xblk_b;       // k blocks that fit in the pipeline stages (region 1, a CTA's last item)
     int hl;           // XH planes: 1 (bf16) or 2 (hi + lo)
     int borrow;       // 1: no room for D' beside two accumulators; D' borrows the other one
     uint32_t x_chunk, stage_bytes;
@@ -100,8 +101,8 @@ struct EpiAux {
     uint32_t onbits[MAX_TN / 32];    // bit j: column j takes its delta here
     int32_t wsum[2][4];              // scan scratch: per-warp totals
     int32_t n_on;
-    int32_t xr_mode;                 // 0 no expand, 1 into D', 2 into the base accumulator
-    int32_t xr_nk16, xr_last;        // K=16 steps of this round; last round of the item
+    int32_t xr_mode[2];              // per staging region: 0 no expand, 1 into D', 2 into the base accumulator
+    int32_t xr_nk16[2], xr_last[2];  // K=16 steps of the region's round; last round of the item
 };
 
 struct Bars {
@@ -109,8 +110,9 @@ struct Bars {
     uint64_t empty[MAX_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
-    uint64_t x_full;   // an expand round is staged
-    uint64_t x_empty;  // the UMMAs of the last round have finished reading it
+    uint64_t x_full[2];  // an expand round is staged in region 0 / 1
+    uint64_t x_empty[2]; // the UMMAs of that region's last round have finished reading it
+    uint64_t base_done;  // the base UMMAs of an item have finished (its stages are free)
     uint64_t epi_done; // every epilogue thread has finished reading TMEM
     uint32_t tmem_base;
     int abort_flag;
@@ -221,10 +223,13 @@ __device__ __forceinline__ void issue_mma(const Params &p, const TcCfg &c, Bars 
     if (c.static_tiles < 0)
         grid_dependency_wait();
     const EpiAux *aux = reinterpret_cast<const EpiAux *>(smem + c.aux_off);
-    const uint32_t xb = smem_u32(smem + c.xb_off), xh = smem_u32(smem + c.xh_off);
-    const uint32_t xh_plane = (uint32_t)c.xblk * (uint32_t)c.tn * 128u;
+    const uint32_t xh_blk = (uint32_t)c.tn * 128u;
+    // staging regions: 0 = dedicated buffers, 1 = the pipeline stages
+    const uint32_t rxb[2] = {smem_u32(smem + c.xb_off), smem_u32(smem)};
+    const uint32_t rxh[2] = {smem_u32(smem + c.xh_off), smem_u32(smem) + (uint32_t)c.xblk_b * XB_BLOCK};
+    const uint32_t rplane[2] = {(uint32_t)c.xblk * xh_blk, (uint32_t)c.xblk_b * xh_blk};
     const int total = item_total(p, c);
-    int g = 0, it = 0, xg = 0;
+    int g = 0, it = 0, xg[2] = {0, 0};
     uint32_t acq[2] = {0u, 0u};
     TileInfo ti;
     for (int w = blockIdx.x; w < total && get_tile(p, c, w / c.csplit, total, ti); w += gridDim.x, ++it) {
@@ -265,20 +270,24 @@ __device__ __forceinline__ void issue_mma(const Params &p, const TcCfg &c, Bars 
             }
             umma_commit(bars->empty + slot);
         }
-        // expand rounds of this item
+        umma_commit(&bars->base_done);
+        // expand rounds of this item: round 1 of a CTA's last item is staged in
+        // the pipeline stages (region 1), every other round in region 0
+        const bool last_item = w + (int)gridDim.x >= total;
         bool first = true;
         uint32_t dacc = 0;
-        while (ok) {
-            if (aborted(bars) || !mbar_wait(&bars->x_full, (uint32_t)xg & 1u)) {
+        for (int round = 0; ok; ++round) {
+            const int rg = (round == 1 && last_item && c.xblk_b > 0) ? 1 : 0;
+            if (aborted(bars) || !mbar_wait(bars->x_full + rg, (uint32_t)xg[rg] & 1u)) {
                 flag_abort(p, bars);
                 ok = false;
                 break;
             }
-            ++xg;
+            ++xg[rg];
             tc_fence_after();
-            const int mode = *(volatile const int32_t *)&aux->xr_mode;
-            const int nk16 = *(volatile const int32_t *)&aux->xr_nk16;
-            const int last = *(volatile const int32_t *)&aux->xr_last;
+            const int mode = *(volatile const int32_t *)&aux->xr_mode[rg];
+            const int nk16 = *(volatile const int32_t *)&aux->xr_nk16[rg];
+            const int last = *(volatile const int32_t *)&aux->xr_last[rg];
             if (mode == 1 && first && c.borrow) {
                 const int ob = buf ^ 1;
                 if (aborted(bars) || !mbar_wait(bars->acc_empty + ob, (acq[ob] & 1u) ^ 1u)) {
@@ -294,14 +303,14 @@ __device__ __forceinline__ void issue_mma(const Params &p, const TcCfg &c, Bars 
             uint32_t dacc_on = (mode == 2 || !first) ? 1u : 0u;
             for (int k = 0; k < nk16; ++k) {
                 const uint32_t koff = (uint32_t)(k >> 2) * XB_BLOCK + (uint32_t)(k & 3) * 32u;
-                const uint32_t hoff = (uint32_t)(k >> 2) * (uint32_t)c.tn * 128u + (uint32_t)(k & 3) * 32u;
+                const uint32_t hoff = (uint32_t)(k >> 2) * xh_blk + (uint32_t)(k & 3) * 32u;
                 for (int h = 0; h < c.hl; ++h) {
-                    umma_bf16(dacc, sw128_kmajor_desc(xb + koff), sw128_kmajor_desc(xh + h * xh_plane + hoff),
-                              idesc, dacc_on);
+                    umma_bf16(dacc, sw128_kmajor_desc(rxb[rg] + koff),
+                              sw128_kmajor_desc(rxh[rg] + h * rplane[rg] + hoff), idesc, dacc_on);
                     dacc_on = 1;
                 }
             }
-            umma_commit(&bars->x_empty);
+            umma_commit(bars->x_empty + rg);
             first = false;
             if (last)
                 break;
@@ -400,49 +409,61 @@ __device__ __forceinline__ void epi_shrink(const Params &p, const int32_t *unit_
     }
 }
 
-// B rows n0 + et of the expand's slots whose k range meets [r0k, r0k + kr),
-// copied into XB (128-byte swizzle) without passing through registers; pad
-// columns of the padded rank and rows past N are zero-filled.
-__device__ __forceinline__ void stage_b(const Params &p, const EpiAux *aux, uint8_t *XB, int nent, int r0k,
-                                        int kr, int n, int et)
+// Where one staging pass writes: relative k in [0, kr0) goes to region 0,
+// [kr0, kr0 + kr1) to region 1 (kr1 = 0: one region).
+struct XDst {
+    uint8_t *xb[2];
+    uint8_t *xh[2];
+    uint32_t plane[2]; // bytes between the hi and lo planes of XH
+    int kr0, kr1;
+};
+
+// B rows n0 + et of the expand's slots, the part whose k relative to r0k lies
+// in [klo, khi), copied into XB (128-byte swizzle) of the region that k maps
+// to, without passing through registers; pad columns of the padded rank and
+// rows past N are zero-filled.
+__device__ __forceinline__ void stage_b(const Params &p, const EpiAux *aux, const XDst &d, int klo, int khi,
+                                        int nent, int r0k, int n, int et)
 {
     const bool row_ok = n < p.N;
     for (int e = 0; e < nent; ++e) {
         const int so = aux->ent_off[e] - r0k;
         const int rk = aux->ent_rank[e];
         const int pk = (rk + 15) & ~15;
-        if (so + pk <= 0 || so >= kr)
+        if (so + pk <= klo || so >= khi)
             continue;
         const uint16_t *src = aux->ent_b[e] + (size_t)(row_ok ? n : 0) * p.R;
-        for (int q = max(0, -so); q < pk && so + q < kr; q += 8) {
-            const int cq = (so + q) >> 3;
+        for (int q = max(0, klo - so); q < pk && so + q < khi; q += 8) {
+            const int k = so + q, rg = k >= d.kr0 ? 1 : 0, kl = k - (rg ? d.kr0 : 0);
+            const int cq = kl >> 3;
             const bool has = row_ok && q < rk;
-            cp_async_16(XB + (cq >> 3) * XB_BLOCK + et * 128 + (((cq & 7) ^ (et & 7)) << 4),
+            cp_async_16(d.xb[rg] + (cq >> 3) * XB_BLOCK + et * 128 + (((cq & 7) ^ (et & 7)) << 4),
                         src + (has ? q : 0), has ? 16u : 0u);
         }
     }
 }
 
-// XH rows 0..nmma-1 of the round [r0k, r0k + kr): s_t * h_t in column t's
-// slot range (hi, and lo = the bf16 remainder when hl = 2), zero elsewhere.
-// First every chunk of the round is zeroed; then each column's data chunks
-// are split over 128 / nmma threads, each issuing the loads of up to four
-// chunks (every K part of h) before converting any.
-__device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const EpiAux *aux, uint8_t *XH,
-                                        const TileInfo &ti, int nmma, int r0k, int kr, int et)
+// XH rows 0..nmma-1 of the pass [r0k, r0k + kr0 + kr1): s_t * h_t in column
+// t's slot range (hi, and lo = the bf16 remainder when hl = 2), zero
+// elsewhere. First every chunk of the pass is zeroed; then each column's data
+// chunks are split over 128 / nmma threads, each issuing the loads of up to
+// four chunks (every K part of h) before converting any.
+__device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const EpiAux *aux, const XDst &d,
+                                        const TileInfo &ti, int nmma, int r0k, int et)
 {
     const uint32_t xh_block = (uint32_t)c.tn * 128u;
-    const uint32_t xh_plane = (uint32_t)c.xblk * xh_block;
-    const int nch = ((kr + 63) >> 6) * 8;
+    const int nch0 = ((d.kr0 + 63) >> 6) * 8, nch = nch0 + ((d.kr1 + 63) >> 6) * 8;
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int idx = et; idx < nmma * nch; idx += EPI_THREADS) {
         const int j = idx / nch, cq = idx - j * nch;
-        uint8_t *dst = XH + (uint32_t)(cq >> 3) * xh_block + j * 128 + (((cq & 7) ^ (j & 7)) << 4);
+        const int rg = cq >= nch0 ? 1 : 0, cl = cq - (rg ? nch0 : 0);
+        uint8_t *dst = d.xh[rg] + (uint32_t)(cl >> 3) * xh_block + j * 128 + (((cl & 7) ^ (j & 7)) << 4);
         *reinterpret_cast<uint4 *>(dst) = z;
         if (c.hl == 2)
-            *reinterpret_cast<uint4 *>(dst + xh_plane) = z;
+            *reinterpret_cast<uint4 *>(dst + d.plane[rg]) = z;
     }
     named_bar_sync(1, EPI_THREADS);
+    const int kt = d.kr0 + d.kr1;
     const size_t part_stride = (size_t)p.rows * p.R;
     // tpc threads per column (a power of two), each taking every tpc-th chunk
     const int tpc = nmma >= EPI_THREADS ? 1 : EPI_THREADS / nmma;
@@ -453,8 +474,8 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
             continue;
         const int rk = aux->crank[j];
         const float s = aux->cscale[j];
-        // ranks r (multiples of 8, r < rank) of this slot that fall in the round
-        const int rlo = max(0, r0k - ko), rhi = min(rk, r0k + kr - ko);
+        // ranks r (multiples of 8, r < rank) of this slot that fall in the pass
+        const int rlo = max(0, r0k - ko), rhi = min(rk, r0k + kt - ko);
         const float *hrow = p.ws.h + (size_t)(ti.r0 + j) * p.R;
         for (int r = rlo + 8 * sub; r < rhi; r += 32 * tpc) {
             float4 a[4], b[4];
@@ -487,12 +508,13 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     split_hi_lo(v[i], h8[i], l8[i]);
-                const int cq = (ko + rr - r0k) >> 3;
-                uint8_t *dst = XH + (uint32_t)(cq >> 3) * xh_block + j * 128 + (((cq & 7) ^ (j & 7)) << 4);
+                const int k = ko + rr - r0k, rg = k >= d.kr0 ? 1 : 0, kl = k - (rg ? d.kr0 : 0);
+                const int cq = kl >> 3;
+                uint8_t *dst = d.xh[rg] + (uint32_t)(cq >> 3) * xh_block + j * 128 + (((cq & 7) ^ (j & 7)) << 4);
                 *reinterpret_cast<uint4 *>(dst) = make_uint4(h8[0] | (h8[1] << 16), h8[2] | (h8[3] << 16),
                                                              h8[4] | (h8[5] << 16), h8[6] | (h8[7] << 16));
                 if (c.hl == 2)
-                    *reinterpret_cast<uint4 *>(dst + xh_plane) =
+                    *reinterpret_cast<uint4 *>(dst + d.plane[rg]) =
                         make_uint4(l8[0] | (l8[1] << 16), l8[2] | (l8[3] << 16), l8[4] | (l8[5] << 16),
                                    l8[6] | (l8[7] << 16));
             }
@@ -540,7 +562,7 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
 
     const int total = item_total(p, c);
     bool shrink_done = false;
-    int it = 0, xg = 0;
+    int it = 0, xg[2] = {0, 0};
     TileInfo ti;
     for (int w = blockIdx.x; w < total && get_tile(p, c, w / c.csplit, total, ti); w += gridDim.x, ++it) {
         const int tile = w / c.csplit, part = w % c.csplit;
@@ -617,25 +639,38 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
                     prefetch_l2(aux->ent_b[e] + (size_t)n * p.R);
         }
 
-        // (3) expand rounds: k range [r0k, r0k + kr) of the concatenated slots
+        // (3) expand rounds: k range [r0k, r0k + kr) of the concatenated slots.
+        // The first pass stages round 0 in the dedicated buffers (region 0)
+        // and, on this CTA's last item, round 1 in the pipeline stages (region
+        // 1, free once the item's base UMMAs are done); each later pass stages
+        // one round in region 0.
+        const bool last_item = w + (int)gridDim.x >= total;
         int r0k = 0;
         bool stop = false;
-        do {
-            const int kr = min(kx - r0k, c.xblk * 64);
-            if (xg > 0) { // the UMMAs of the previous round have read the buffers
-                if (et == 0 && !mbar_wait(&bars->x_empty, (uint32_t)(xg - 1) & 1u))
+        for (int pass = 0; pass == 0 || r0k < kx; ++pass) {
+            XDst d;
+            d.xb[0] = XB;
+            d.xh[0] = XH;
+            d.plane[0] = (uint32_t)c.xblk * (uint32_t)c.tn * 128u;
+            d.xb[1] = smem;
+            d.xh[1] = smem + (size_t)c.xblk_b * XB_BLOCK;
+            d.plane[1] = (uint32_t)c.xblk_b * (uint32_t)c.tn * 128u;
+            d.kr0 = min(kx - r0k, c.xblk * 64);
+            d.kr1 = (pass == 0 && last_item && c.xblk_b > 0) ? min(kx - r0k - d.kr0, c.xblk_b * 64) : 0;
+            if (xg[0] > 0) { // the UMMAs of region 0's previous round have read it
+                if (et == 0 && !mbar_wait(bars->x_empty, (uint32_t)(xg[0] - 1) & 1u))
                     flag_abort(p, bars);
                 named_bar_sync(1, EPI_THREADS);
             }
-            if (kr > 0)
-                stage_b(p, aux, XB, nent, r0k, kr, n, et);
+            if (d.kr0 > 0)
+                stage_b(p, aux, d, 0, d.kr0, nent, r0k, n, et);
             if (!shrink_done) {
                 if (!routed)
                     route_wait();
                 epi_shrink(p, unit_off, seg_off, red, um, et);
                 shrink_done = true;
             }
-            if (r0k == 0 && nent > 0) { // the shrink of the staged slots has finished
+            if (pass == 0 && nent > 0) { // the shrink of the staged slots has finished
                 for (int e = et; e < nent; e += EPI_THREADS) {
                     const int b = ti.e * (p.L + 1) + aux->entry_slot[e] + 1;
                     if (!wait_bucket(p, b, unit_off))
@@ -648,20 +683,34 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
                     break;
                 }
             }
-            if (kr > 0)
-                stage_h(p, c, aux, XH, ti, nmma, r0k, kr, et);
+            if (d.kr1 > 0) { // region 1: the stages are free once the base UMMAs are done
+                if (et == 0 && !mbar_wait(&bars->base_done, (uint32_t)it & 1u))
+                    flag_abort(p, bars);
+                named_bar_sync(1, EPI_THREADS);
+                stage_b(p, aux, d, d.kr0, d.kr0 + d.kr1, nent, r0k, n, et);
+            }
+            if (d.kr0 + d.kr1 > 0)
+                stage_h(p, c, aux, d, ti, nmma, r0k, et);
             cp_async_wait_all();
             fence_proxy_async_smem(); // generic-proxy writes, read by the UMMAs
             named_bar_sync(1, EPI_THREADS);
             if (et == 0) {
-                aux->xr_mode = mode;
-                aux->xr_nk16 = kr / 16;
-                aux->xr_last = r0k + kr >= kx ? 1 : 0;
-                mbar_arrive(&bars->x_full);
+                aux->xr_mode[0] = mode;
+                aux->xr_nk16[0] = d.kr0 / 16;
+                aux->xr_last[0] = (d.kr1 == 0 && r0k + d.kr0 >= kx) ? 1 : 0;
+                mbar_arrive(bars->x_full);
+                if (d.kr1 > 0) {
+                    aux->xr_mode[1] = mode;
+                    aux->xr_nk16[1] = d.kr1 / 16;
+                    aux->xr_last[1] = r0k + d.kr0 + d.kr1 >= kx ? 1 : 0;
+                    mbar_arrive(bars->x_full + 1);
+                }
             }
-            ++xg;
-            r0k += kr;
-        } while (r0k < kx);
+            ++xg[0];
+            if (d.kr1 > 0)
+                ++xg[1];
+            r0k += d.kr0 + d.kr1;
+        }
         if (stop)
             break;
 
@@ -773,8 +822,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_init(bars->acc_full + b, 1);
             mbar_init(bars->acc_empty + b, 1);
         }
-        mbar_init(&bars->x_full, 1);
-        mbar_init(&bars->x_empty, 1);
+        for (int r = 0; r < 2; ++r) {
+            mbar_init(bars->x_full + r, 1);
+            mbar_init(bars->x_empty + r, 1);
+        }
+        mbar_init(&bars->base_done, 1);
         mbar_init(&bars->epi_done, EPI_THREADS);
         bars->abort_flag = 0;
         fence_barrier_init();
@@ -876,6 +928,8 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
     c.bar_off = align_up(o, 16);
     c.smem_bytes = 1024u + c.bar_off + (uint32_t)sizeof(Bars);
     c.tmem_cols = c.borrow ? 512u : pow2_at_least(3u * (uint32_t)c.tn);
+    // region 1: XB blocks then XH blocks (hl planes) carved from the stages
+    c.xblk_b = (int)min(8u, (uint32_t)c.stages * c.stage_bytes / (XB_BLOCK + (uint32_t)c.hl * (uint32_t)c.tn * 128u));
     const int tt = (p.rows + c.tn - 1) / c.tn;
     c.static_tiles = dyn ? -1 : tt * c.n_tiles;
     return c;

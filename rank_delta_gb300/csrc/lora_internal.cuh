@@ -26,6 +26,7 @@ struct Tables {
 // delta when its slot is negative or >= L, the slot is empty, or its scale
 // is 0 (the delta is then skipped, not multiplied by zero).
 struct SlotInfo {
+    const uint16_t *a; // A of the slot, [R][K]
     const uint16_t *b; // B of the slot, [N][R]
     float scale;
     int rank;
@@ -34,14 +35,14 @@ struct SlotInfo {
 
 __device__ __forceinline__ SlotInfo slot_info(const Tables &t, int s, int L)
 {
-    SlotInfo si{nullptr, 0.0f, 0, 0};
+    SlotInfo si{nullptr, nullptr, 0.0f, 0, 0};
     if (s < 0 || s >= L)
         return si;
-    const uint16_t *a = t.a_table[s];
+    si.a = t.a_table[s];
     si.b = t.b_table[s];
     si.scale = t.scale_table[s];
     si.rank = t.rank_table[s];
-    si.on = (a != nullptr && si.b != nullptr && si.scale != 0.0f && si.rank > 0) ? 1 : 0;
+    si.on = (si.a != nullptr && si.b != nullptr && si.scale != 0.0f && si.rank > 0) ? 1 : 0;
     return si;
 }
 

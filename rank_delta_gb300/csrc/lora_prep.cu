@@ -84,6 +84,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
     __shared__ uint32_t flags;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
+    // Launched early (programmatic dependent launch) behind whatever the
+    // stream ran before; nothing is read until that work is complete, and only
+    // then may the projection kernel launch.
+    grid_dependency_wait();
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int slot0 = tid < p.rows ? p.seq_slot[tid] : -1;
     if (tid == 0)
@@ -237,8 +241,17 @@ cudaError_t launch_prep(const Params &p, cudaStream_t st)
             return e;
         attr_set = true;
     }
-    prep_kernel<<<1, PREP_THREADS, smem, st>>>(p);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(PREP_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prep_kernel, p);
 }
 
 cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st)

@@ -13,10 +13,11 @@
 // is computed the same way whatever N is. Two TMEM accumulators let the
 // epilogue drain one item while the next accumulates.
 //
-// The expand-fold runs on the tensor cores too. For the slots whose delta an
-// item adds (adapted rows of the tile whose slot is this K part's: slot %
-// csplit), the epilogue warps stage in shared memory, in the same 128-byte
-// swizzled K-major layout TMA writes:
+// The expand-fold runs on the tensor cores too. Each adapted slot of a tile
+// is owned by one K part (slots sorted by padded rank, largest first, dealt
+// to the parts in snake order). For the slots an item owns, the
+// epilogue warps stage in shared memory, in the same 128-byte swizzled
+// K-major layout TMA writes:
 //   XB[n, k]  the B rows n0..n0+127 of those slots, concatenated along k (each
 //             slot's rank padded to 16, slots in ascending order),
 //   XH[t, k]  s_t * h_t placed in its slot's k range, zero elsewhere (bf16;
@@ -70,6 +71,7 @@ constexpr int MAX_TN = 256;
 constexpr int MAX_STAGES = 8;
 constexpr uint32_t W_CHUNK_BYTES = TC_BM * 64 * 2;
 constexpr uint32_t XB_BLOCK = TC_BM * 128; // 64 k of 128 B rows, 128 rows
+constexpr int LR_MAX_L = 64;               // slots a launch may have for local routing
 
 struct TcCfg {
     int tn, kc, stages, csplit;
@@ -81,6 +83,7 @@ struct TcCfg {
     int xblk_b;       // k blocks that fit in the pipeline stages (region 1, a CTA's last item)
     int hl;           // XH planes: 1 (bf16) or 2 (hi + lo)
     int borrow;       // 1: no room for D' beside two accumulators; D' borrows the other one
+    int local_route;  // 1: one token tile holds every row; each CTA sorts them itself for the shrink
     uint32_t x_chunk, stage_bytes;
     uint32_t xb_off, xh_off, aux_off, meta_off, red_off, umeta_off, bar_off, smem_bytes;
     uint32_t tmem_cols;
@@ -94,12 +97,23 @@ struct EpiAux {
     float cscale[MAX_TN];            // scale of column j's slot
     int16_t crank[MAX_TN];           // rank of column j's slot
     uint16_t soff[1024];             // per slot: padded rank if used (0 if not), then its k offset
+    int8_t part_of[1024];            // per used slot: the K part that adds its delta
     int16_t entry_slot[MAX_TN];      // the expand's slots, ascending
     int32_t ent_off[MAX_TN];         // k offset of entry e
     int16_t ent_rank[MAX_TN];        // rank of entry e
     const uint16_t *ent_b[MAX_TN];   // B of entry e
     uint32_t onbits[MAX_TN / 32];    // bit j: column j takes its delta here
     int32_t wsum[2][4];              // scan scratch: per-warp totals
+    // local routing (local_route): per slot s < L of the launch's one token tile
+    int32_t lr_cnt[LR_MAX_L];        // adapted rows of slot s
+    int16_t lr_rank[LR_MAX_L];
+    int16_t lr_seg[LR_MAX_L];        // first position of slot s in lr_perm
+    int16_t lr_run[LR_MAX_L];        // placement cursor
+    int32_t lr_uoff[LR_MAX_L + 1];   // first shrink unit of slot s
+    const uint16_t *lr_a[LR_MAX_L];
+    const uint16_t *lr_b[LR_MAX_L];
+    int16_t lr_wcnt[4][LR_MAX_L];    // rows of slot s in each warp's 32 (stable placement)
+    int16_t lr_perm[MAX_TN];         // tile rows grouped by slot, in row order within a slot
     int32_t n_on;
     int32_t xr_mode[2];              // per staging region: 0 no expand, 1 into D', 2 into the base accumulator
     int32_t xr_nk16[2], xr_last[2];  // K=16 steps of the region's round; last round of the item
@@ -409,6 +423,39 @@ __device__ __forceinline__ void epi_shrink(const Params &p, const int32_t *unit_
     }
 }
 
+// Metadata of shrink unit u from the local routing of a one-tile launch:
+// units are numbered as the routing kernel numbers them (slot by slot, then
+// rank group, row chunk, K part), over the tile's rows grouped by slot.
+__device__ __forceinline__ UnitMeta lr_unit_meta(const Params &p, const EpiAux *aux, int u, int r0)
+{
+    int lo = 0, hi = p.L;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (aux->lr_uoff[mid] <= u)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int s = lo, rank = aux->lr_rank[s];
+    const int nrg = (rank + SHRINK_RG - 1) / SHRINK_RG;
+    int local = u - aux->lr_uoff[s];
+    UnitMeta m;
+    m.kpart = (int16_t)(local % p.kp);
+    local /= p.kp;
+    m.rg = (int16_t)(local % nrg);
+    const int c0 = aux->lr_seg[s] + (local / nrg) * SHRINK_TC;
+    const int nrows = min(SHRINK_TC, aux->lr_seg[s] + aux->lr_cnt[s] - c0);
+#pragma unroll
+    for (int j = 0; j < SHRINK_TC; ++j)
+        m.row[j] = r0 + aux->lr_perm[c0 + min(j, nrows - 1)];
+    m.A = aux->lr_a[s];
+    m.b = (int16_t)(s + 1);
+    m.rank = (int16_t)rank;
+    m.nrows = (int16_t)nrows;
+    m.pad = 0;
+    return m;
+}
+
 // Where one staging pass writes: relative k in [0, kr0) goes to region 0,
 // [kr0, kr0 + kr1) to region 1 (kr1 = 0: one region).
 struct XDst {
@@ -522,8 +569,9 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
     }
 }
 
-// Per item: which columns take their delta here (adapted rows whose slot is
-// this K part's: slot % csplit) and the k offset of each such slot; stage the
+// Per item: which columns take their delta here (adapted rows whose slot the
+// rank-balanced assignment gives to this K part) and the k offset of each such
+// slot; stage the
 // expand operands round by round for the MMA warp (the first round of the
 // first item is issued before this CTA's shrink units, so its B copies overlap
 // them); then drain the accumulator (adding D' to those columns only), and
@@ -575,41 +623,148 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         // (1) the columns whose delta this part adds, and the slots they use
         for (int q = et; q < p.L; q += EPI_THREADS)
             aux->soff[q] = 0;
+        if (c.local_route && et < p.L)
+            aux->lr_cnt[et] = 0;
         if (et < MAX_TN / 32)
             aux->onbits[et] = 0;
         if (et == 0)
             aux->n_on = 0;
         named_bar_sync(1, EPI_THREADS);
-        int my_on = 0;
         for (int j = et; j < ti.cnt; j += EPI_THREADS) {
             const int sl = p.seq_slot[ti.r0 + j];
             const SlotInfo si = slot_info(tab, sl, p.L);
-            const bool on = si.on && sl % C == part;
-            aux->koff[j] = on ? sl : -1;
+            aux->koff[j] = si.on ? sl : -1;
             aux->cscale[j] = si.scale;
             aux->crank[j] = (int16_t)si.rank;
-            if (on) {
+            if (si.on) {
                 aux->soff[sl] = (uint16_t)((si.rank + 15) & ~15); // same value from every writer
+                if (c.local_route) {
+                    atomicAdd(&aux->lr_cnt[sl], 1);
+                    aux->lr_rank[sl] = (int16_t)si.rank;
+                    aux->lr_a[sl] = si.a;
+                    aux->lr_b[sl] = si.b;
+                }
+            }
+        }
+        named_bar_sync(1, EPI_THREADS);
+        if (c.local_route && !shrink_done) {
+            // (1a) every row of the launch is in this tile: sort them by slot
+            // here (stable, so every CTA builds the same shrink work list) and
+            // run this CTA's units without waiting for the routing kernel; only
+            // the counter updates wait for it (it clears the counters).
+            int u_s = 0, c_s = 0;
+            if (et < p.L) {
+                c_s = aux->lr_cnt[et];
+                u_s = c_s > 0 ? bucket_units(aux->lr_rank[et], c_s, p.kp) : 0;
+            }
+            int eu, ecn, tu, tcn;
+            epi_scan2(u_s, c_s, eu, ecn, tu, tcn, aux, et);
+            if (et < p.L) {
+                aux->lr_uoff[et] = eu;
+                aux->lr_seg[et] = (int16_t)ecn;
+                aux->lr_run[et] = (int16_t)ecn;
+            }
+            if (et == 0)
+                aux->lr_uoff[p.L] = tu;
+            for (int c0 = 0; c0 < ti.cnt; c0 += EPI_THREADS) {
+                for (int q = et; q < 4 * LR_MAX_L; q += EPI_THREADS)
+                    (&aux->lr_wcnt[0][0])[q] = 0;
+                named_bar_sync(1, EPI_THREADS);
+                const int j = c0 + et, lane = et & 31;
+                const int sl = j < ti.cnt ? aux->koff[j] : -1;
+                const unsigned peers = __match_any_sync(0xffffffffu, sl);
+                const int r = __popc(peers & ((1u << lane) - 1u));
+                if (sl >= 0 && r == 0)
+                    aux->lr_wcnt[ew][sl] = (int16_t)__popc(peers);
+                named_bar_sync(1, EPI_THREADS);
+                if (sl >= 0) {
+                    int pre = 0;
+                    for (int q = 0; q < ew; ++q)
+                        pre += aux->lr_wcnt[q][sl];
+                    aux->lr_perm[aux->lr_run[sl] + pre + r] = (int16_t)j;
+                }
+                named_bar_sync(1, EPI_THREADS);
+                if (et < p.L)
+                    aux->lr_run[et] = (int16_t)(aux->lr_run[et] + aux->lr_wcnt[0][et] + aux->lr_wcnt[1][et] +
+                                                aux->lr_wcnt[2][et] + aux->lr_wcnt[3][et]);
+                named_bar_sync(1, EPI_THREADS);
+            }
+            // this CTA's units, first of all the item's work (their loads
+            // should not queue behind the B copies)
+            const int mine = tu > (int)blockIdx.x ? (tu - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+            for (int k0 = 0; k0 < mine; k0 += UNIT_BATCH) {
+                const int nk = min(UNIT_BATCH, mine - k0);
+                if (et < nk)
+                    um[et] = lr_unit_meta(p, aux, (int)blockIdx.x + (k0 + et) * (int)gridDim.x, ti.r0);
+                named_bar_sync(1, EPI_THREADS);
+                for (int k = 0; k < nk; ++k)
+                    shrink_unit(p, um[k], ew, et & 31, red, 1);
+                __threadfence();
+                named_bar_sync(1, EPI_THREADS);
+                if (!routed)
+                    route_wait();
+                if (et < nk)
+                    atomicAdd(p.ws.done + um[et].b, 1);
+                named_bar_sync(1, EPI_THREADS); // um is rewritten by the next batch
+            }
+            shrink_done = true;
+        }
+        const int per = (p.L + EPI_THREADS - 1) / EPI_THREADS;
+        const int s0 = min(p.L, et * per), s1 = min(p.L, s0 + per);
+        if (C > 1) {
+            // (1b) the tile's adapted slots shared among the K parts: sorted by
+            // padded rank, largest first (ties: lower slot), and dealt in snake
+            // order 0, 1, .., C-1, C-1, .., 0, 0, 1, .. so the parts' k extents
+            // stay close. Every CTA of the tile derives the same assignment.
+            int cnt = 0;
+            for (int s = s0; s < s1; ++s)
+                cnt += aux->soff[s] != 0;
+            int ec0, dummy, nu, dummy2;
+            epi_scan2(cnt, 0, ec0, dummy, nu, dummy2, aux, et);
+            for (int s = s0; s < s1; ++s)
+                if (aux->soff[s]) {
+                    aux->entry_slot[ec0] = (int16_t)s;
+                    aux->ent_off[ec0] = aux->soff[s]; // padded rank, by list position
+                    ++ec0;
+                }
+            named_bar_sync(1, EPI_THREADS);
+            for (int i = et; i < nu; i += EPI_THREADS) {
+                const int ci = aux->ent_off[i];
+                int pos = 0;
+                for (int j = 0; j < nu; ++j) {
+                    const int cj = aux->ent_off[j];
+                    pos += (cj > ci) | ((cj == ci) & (j < i));
+                }
+                const int r = pos % (2 * C);
+                aux->part_of[aux->entry_slot[i]] = (int8_t)(r < C ? r : 2 * C - 1 - r);
+            }
+            named_bar_sync(1, EPI_THREADS);
+        }
+        int my_on = 0;
+        for (int j = et; j < ti.cnt; j += EPI_THREADS) {
+            const int sl = aux->koff[j];
+            const bool on = sl >= 0 && (C == 1 || aux->part_of[sl] == part);
+            if (on) {
                 atomicOr(&aux->onbits[j >> 5], 1u << (j & 31));
                 ++my_on;
+            } else {
+                aux->koff[j] = -1;
             }
         }
         if (my_on)
             atomicAdd(&aux->n_on, my_on);
         named_bar_sync(1, EPI_THREADS);
-        // (2) k offsets: used slots in ascending order, each rank padded to 16
-        const int per = (p.L + EPI_THREADS - 1) / EPI_THREADS;
-        const int s0 = min(p.L, et * per), s1 = min(p.L, s0 + per);
+        // (2) k offsets of this part's slots in ascending order, each rank padded to 16
         int ksum = 0, scount = 0;
         for (int s = s0; s < s1; ++s) {
-            const int v = aux->soff[s];
+            const int v = (C == 1 || aux->part_of[s] == part) ? aux->soff[s] : 0;
             ksum += v;
             scount += v != 0;
         }
         int ek, ec, kx, nent;
         epi_scan2(ksum, scount, ek, ec, kx, nent, aux, et);
         for (int s = s0; s < s1; ++s) {
-            const int v = aux->soff[s];
+            const int v = (C == 1 || aux->part_of[s] == part) ? aux->soff[s] : 0;
             if (v) {
                 aux->soff[s] = (uint16_t)ek;
                 aux->entry_slot[ec] = (int16_t)s;
@@ -621,8 +776,8 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         named_bar_sync(1, EPI_THREADS);
         for (int e = et; e < nent; e += EPI_THREADS) {
             const int s = aux->entry_slot[e];
-            aux->ent_b[e] = tab.b_table[s];
-            aux->ent_rank[e] = (int16_t)tab.rank_table[s];
+            aux->ent_b[e] = c.local_route ? aux->lr_b[s] : tab.b_table[s];
+            aux->ent_rank[e] = c.local_route ? aux->lr_rank[s] : (int16_t)tab.rank_table[s];
         }
         for (int j = et; j < ti.cnt; j += EPI_THREADS) {
             const int sl = aux->koff[j];
@@ -670,6 +825,8 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
                 epi_shrink(p, unit_off, seg_off, red, um, et);
                 shrink_done = true;
             }
+            if (!routed)
+                route_wait(); // the counters below are the routing kernel's
             if (pass == 0 && nent > 0) { // the shrink of the staged slots has finished
                 for (int e = et; e < nent; e += EPI_THREADS) {
                     const int b = ti.e * (p.L + 1) + aux->entry_slot[e] + 1;
@@ -773,25 +930,39 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
             const float *parts = p.ws.part + (size_t)tile * C * c.tn * EPI_THREADS;
             const size_t pstride = (size_t)c.tn * EPI_THREADS;
             const int cb = part * ti.cnt / C, ce = (part + 1) * ti.cnt / C;
-            for (int col = cb; col < ce; col += 16) {
-                float acc[16][4];
+            // thread = 4 consecutive features (quad) x every 4th column of the
+            // share: 16-byte loads, each warp reading whole 512-byte column rows
+            const int quad = et & 31, cg = et >> 5;
+            const int nq = ti.n0 + 4 * quad;
+            for (int col0 = cb + cg; col0 < ce; col0 += 4 * 8) {
+                float4 acc[8][4];
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj)
+                for (int jj = 0; jj < 8; ++jj)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int cc = min(col + jj, ce - 1), qq = min(q, C - 1); // clamped: in bounds
-                        acc[jj][q] = __ldcg(parts + qq * pstride + (size_t)cc * EPI_THREADS + et);
+                        const int cc = min(col0 + 4 * jj, ce - 1), qq = min(q, C - 1); // clamped: in bounds
+                        acc[jj][q] = __ldcg(reinterpret_cast<const float4 *>(parts + qq * pstride +
+                                                                             (size_t)cc * EPI_THREADS) + quad);
                     }
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    if (col + jj >= ce || n >= p.N)
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int cc = col0 + 4 * jj;
+                    if (cc >= ce)
                         continue;
-                    float y = acc[jj][0];
+                    float4 y = acc[jj][0];
 #pragma unroll
                     for (int q = 1; q < 4; ++q)
-                        if (q < C)
-                            y += acc[jj][q];
-                    p.y[(int64_t)(ti.r0 + col + jj) * p.y_stride + n] = f32_to_bf16_bits(y);
+                        if (q < C) {
+                            y.x += acc[jj][q].x;
+                            y.y += acc[jj][q].y;
+                            y.z += acc[jj][q].z;
+                            y.w += acc[jj][q].w;
+                        }
+                    uint16_t *yr = p.y + (int64_t)(ti.r0 + cc) * p.y_stride;
+                    if (nq + 0 < p.N) yr[nq + 0] = f32_to_bf16_bits(y.x);
+                    if (nq + 1 < p.N) yr[nq + 1] = f32_to_bf16_bits(y.y);
+                    if (nq + 2 < p.N) yr[nq + 2] = f32_to_bf16_bits(y.z);
+                    if (nq + 3 < p.N) yr[nq + 3] = f32_to_bf16_bits(y.w);
                 }
             }
         }
@@ -906,6 +1077,7 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
     c.xblk = plan.xblk;
     c.hl = plan.hl;
     c.borrow = 3 * c.tn > 512 ? 1 : 0;
+    c.local_route = (!dyn && p.E == 1 && p.rows <= c.tn && p.L <= LR_MAX_L && !p.no_units) ? 1 : 0;
     c.n_tiles = (p.N + TC_BM - 1) / TC_BM;
     c.kchunks = (p.K + 63) / 64;
     c.kstages = (c.kchunks + c.kc - 1) / c.kc;

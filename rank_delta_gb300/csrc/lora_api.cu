@@ -518,7 +518,11 @@ size_t lora_moe_workspace_bytes(int E, int T, const lora_route *rts)
 {
     if (rts == nullptr || E < 1 || E > MAX_E || T < 0 || rts[0].magic != ROUTE_MAGIC)
         return 0;
-    return ws_layout(T, E * (rts[0].max_loras + 1), rts[0].max_rank, shrink_kparts(rts[0].n_in))
+    size_t part_elems = 0;
+    int ncnt = 0;
+    moe_split_scratch(T, E, rts[0].n_in, rts[0].n_out, part_elems, ncnt);
+    return ws_layout(T, E * (rts[0].max_loras + 1), rts[0].max_rank, shrink_kparts(rts[0].n_in), part_elems,
+                     ncnt)
         .total;
 }
 
@@ -578,12 +582,12 @@ lora_status lora_moe_down_apply(const void *x, int64_t x_stride, const void *con
         p.tab[q] = tables_of(rts[q]);
     }
     p.kp = shrink_kparts(K);
-    p.ncnt = 0;
-    if ((s = carve_ws(ws, ws_bytes, T, E * (L + 1), R, p.kp, 0, 0, p.ws, who)) != LORA_OK)
+    size_t part_elems = 0;
+    moe_split_scratch(T, E, K, N, part_elems, p.ncnt);
+    if ((s = carve_ws(ws, ws_bytes, T, E * (L + 1), R, p.kp, part_elems, p.ncnt, p.ws, who)) != LORA_OK)
         return s;
-    // token tile: the mean expert segment with 1/8 headroom, so a typical
-    // expert is one tile
-    p.tn = tc_token_tile((T + E - 1) / E + (T + E - 1) / E / 8);
+    p.tn = moe_token_tile(T, E);
+    p.max_tiles = moe_max_tiles(T, E);
     return run(p, LORA_PATH_TC, reinterpret_cast<cudaStream_t>(stream), who);
 }
 

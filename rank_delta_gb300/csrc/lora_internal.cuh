@@ -75,6 +75,7 @@ struct Params {
     int kp;   // K parts of a shrink unit (h is summed over them)
     int ncnt; // split-K tile counters the prep kernel clears
     int no_units; // 1: h comes from the tensor-core shrink kernel (no shrink work units)
+    int max_tiles; // token tiles the routing kernel may list (0: the workspace bound)
     const uint16_t *W[MAX_E];
     Tables tab[MAX_E];
     Ws ws;
@@ -158,13 +159,38 @@ inline int tc_token_tile(int rows_per_segment)
 // CTAs splitting K for one tile, from the row count and K only -- never from
 // N -- so a fused q/k/v call and its split calls compute every element
 // identically. Several token tiles (rows > 256) or expert tiles: no split.
+// Per-expert tiles (MoE): one K part (a split leaves the in-launch shrink
+// longer than the first item's W stream).
 inline int tc_csplit(int rows, int K, bool per_expert_tiles)
 {
-    if (per_expert_tiles || rows > 256)
+    if (per_expert_tiles)
+        return 1;
+    if (rows > 256)
         return 1;
     const int cap = rows <= 64 ? 4 : 3;
     const int c = ((K + 63) / 64) / 16;
     return c < 1 ? 1 : (c > cap ? cap : c);
+}
+
+// Token tile of a MoE call: the mean expert segment with 1/8 headroom, so a
+// typical expert is one tile.
+inline int moe_token_tile(int T, int E)
+{
+    const int mean = (T + E - 1) / E;
+    return tc_token_tile(mean + mean / 8);
+}
+
+// Token tiles of a MoE call at most: each expert segment adds at most one
+// partial tile (the routing kernel never lists more).
+inline int moe_max_tiles(int T, int E) { return (T + moe_token_tile(T, E) - 1) / moe_token_tile(T, E) + E; }
+
+// Split-K scratch of a MoE call: partial tiles and tile counters.
+inline void moe_split_scratch(int T, int E, int K, int N, size_t &part_elems, int &ncnt)
+{
+    const int cs = tc_csplit(T, K, true);
+    const int tiles = ((N + 127) / 128) * moe_max_tiles(T, E);
+    part_elems = cs > 1 ? (size_t)tiles * cs * 128 * moe_token_tile(T, E) : 0;
+    ncnt = cs > 1 ? tiles : 0;
 }
 
 // Split-K scratch of a projection call: partial tiles and tile counters.

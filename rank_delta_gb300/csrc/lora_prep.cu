@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
     // Token tiles: each expert segment cut into tiles of at most tn rows,
     // expert by expert (thread e counts expert e's tiles; a scan places them).
     const int tn = p.tn > 0 ? p.tn : 256;
-    const int cap = max_token_tiles(p.rows, nb);
+    const int cap = p.max_tiles > 0 ? min(p.max_tiles, max_token_tiles(p.rows, nb)) : max_token_tiles(p.rows, nb);
     if (tid < p.E) {
         const int a = max(offs[tid], 0), b = min(offs[tid + 1], p.rows);
         etiles[tid + 1] = b > a ? (b - a + tn - 1) / tn : 0;

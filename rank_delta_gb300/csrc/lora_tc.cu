@@ -984,6 +984,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     Bars *bars = reinterpret_cast<Bars *>(smem + c.bar_off);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    // The next call's routing kernel may launch now and wait in place (it
+    // reads nothing before this kernel has completed), so its launch latency
+    // is hidden behind this one.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int i = 0; i < c.stages; ++i) {
             mbar_init(bars->full + i, 2); // the W copy and the x copy of a stage

@@ -204,3 +204,29 @@ def test_fully_adapted_wide_tiles_match_oracle():
     y = run.apply(path=rd.LORA_PATH_TC)
     assert run.last_status == 0
     assert_close(y, oracle.workload_proj(wl), "M600 all rows adapted")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_pool_rank_256_needs_several_staging_passes(path):
+    """max_rank 256 (the largest pool rank): a K part's slots span more k than
+    both staging regions hold, so the expand runs in several passes; K 2048
+    gives two K parts on the tensor-core path."""
+    wl = workloads.random_small(seed=256, M=40, K=2048, N=256, L=6, R=256,
+                                ranks=[256, 200, 129, 64, 250, 7])
+    run = ProjRun(wl)
+    y = run.apply(path=path)
+    assert run.last_status == 0
+    assert_close(y, oracle.workload_proj(wl), f"R256 path {path}")
+
+
+def test_many_slots_in_one_tile_match_oracle():
+    """200 slots, 256 rows in one token tile (more slots than the in-tile
+    routing keeps, so the routing kernel's work list is used), three K parts."""
+    wl = workloads.random_small(seed=200, M=256, K=3072, N=384, L=200, R=16)
+    run = ProjRun(wl)
+    y = run.apply(path=rd.LORA_PATH_TC)
+    assert run.last_status == 0
+    assert_close(y, oracle.workload_proj(wl), "L200 M256")
+    base = run.apply(slots=torch.full_like(run.slots, -1), path=rd.LORA_PATH_TC)
+    none = wl.seq_slot < 0
+    assert np.array_equal(y.view(np.uint16)[none], base.view(np.uint16)[none])

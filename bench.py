@@ -177,7 +177,7 @@ def source_sha():
 
 def recorded_traffic(config, kernel):
     """dram bytes per launch from a committed ncu capture, if the kernels are unchanged."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     with open(p) as f:

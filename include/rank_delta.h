@@ -64,7 +64,8 @@ enum {
     LORA_ERR_WORKSPACE = 5,   /* the workspace is smaller than required */
     LORA_ERR_CUDA = 6,        /* a CUDA runtime call failed (message has the CUDA error) */
     LORA_ERR_UNSUPPORTED = 7, /* a size beyond what the kernels handle (message says which) */
-    LORA_ERR_NOT_INIT = 8     /* the route was not set up by lora_route_init */
+    LORA_ERR_NOT_INIT = 8,    /* the route was not set up by lora_route_init */
+    LORA_ERR_POOL_FULL = 9    /* lora_select_victim_slot: every cached slot is in use */
 };
 
 /* Bits of the workspace status word (lora_status_get). */
@@ -169,6 +170,44 @@ lora_status lora_pool_unpack(const lora_route *rt, int slot, lora_stream_t strea
  */
 lora_status lora_set_scale(const lora_route *rt, int slot, float adapter_scale,
                            lora_stream_t stream);
+
+/*
+ * Set every slot's runtime scale at once (frink `lora_attach.rs`,
+ * `set_lora_scales`): slot ids[i] gets scales[i] (the last entry wins when an
+ * id is listed twice), every slot not listed gets 0; each entry becomes
+ * scale_table[slot] = scale * factor_table[slot]. Written by kernels on
+ * `stream` (one launch per 256 slots), so it takes effect for every apply
+ * enqueued after it. ids and scales are host arrays of n entries (n >= 0;
+ * n = 0 sets every scale to 0).
+ * Errors (nothing is written): NULL ids/scales with n > 0; an id outside
+ * [0, max_loras) -- the message names the id and the range.
+ */
+lora_status lora_set_scales(const lora_route *rt, const int32_t *ids, const float *scales, int n,
+                            lora_stream_t stream);
+
+/*
+ * One cached slot, as the promotion cache sees it (metrale
+ * `lora/slot_math.rs`, `select_victim_slot`): whether it holds an adapter, how
+ * many in-flight requests use it, and when it was last used (any monotone
+ * counter).
+ */
+typedef struct lora_slot_view {
+    int32_t slot;
+    int32_t filled;
+    int32_t ref_count;
+    int32_t pad;
+    uint64_t last_used;
+} lora_slot_view;
+
+/*
+ * The slot a promotion overwrites (host only): the first unfilled slot of
+ * `cache` in array order; else, among slots with ref_count == 0, the one with
+ * the smallest last_used (the first such in array order on a tie); else
+ * LORA_ERR_POOL_FULL. *victim receives the chosen entry's `slot`.
+ * Errors: NULL cache with n > 0 or NULL victim; n < 0; LORA_ERR_POOL_FULL
+ * (n = 0 included).
+ */
+lora_status lora_select_victim_slot(const lora_slot_view *cache, int n, int32_t *victim);
 
 /*
  * Workspace of lora_proj_apply for M rows on route `rt` (device scratch the

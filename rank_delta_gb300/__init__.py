@@ -25,6 +25,7 @@ LORA_ERR_WORKSPACE = 5
 LORA_ERR_CUDA = 6
 LORA_ERR_UNSUPPORTED = 7
 LORA_ERR_NOT_INIT = 8
+LORA_ERR_POOL_FULL = 9
 
 LORA_FLAG_SLOT_RANGE = 1 << 0
 LORA_FLAG_WAIT_TIMEOUT = 1 << 1
@@ -61,6 +62,16 @@ class lora_route(ctypes.Structure):
     ]
 
 
+class lora_slot_view(ctypes.Structure):
+    _fields_ = [
+        ("slot", ctypes.c_int32),
+        ("filled", ctypes.c_int32),
+        ("ref_count", ctypes.c_int32),
+        ("pad", ctypes.c_int32),
+        ("last_used", ctypes.c_uint64),
+    ]
+
+
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
 _i64 = ctypes.c_int64
@@ -77,6 +88,8 @@ _SIGNATURES = {
     "lora_pool_pack": (_i, [_rtp, _i, _vp, _vp, _i, _f, _i, _f, _vp]),
     "lora_pool_unpack": (_i, [_rtp, _i, _vp]),
     "lora_set_scale": (_i, [_rtp, _i, _f, _vp]),
+    "lora_set_scales": (_i, [_rtp, _i32p, ctypes.POINTER(ctypes.c_float), _i, _vp]),
+    "lora_select_victim_slot": (_i, [ctypes.POINTER(lora_slot_view), _i, _i32p]),
     "lora_proj_workspace_bytes": (_sz, [_i, _rtp]),
     "lora_proj_apply": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_proj_apply_ex": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _i,
@@ -168,6 +181,27 @@ def lora_pool_unpack(rt: lora_route, slot: int, stream=None) -> None:
 
 def lora_set_scale(rt: lora_route, slot: int, adapter_scale: float, stream=None) -> None:
     _check(lib().lora_set_scale(ctypes.byref(rt), slot, adapter_scale, _stream(stream)))
+
+
+def lora_set_scales(rt: lora_route, scales, stream=None) -> None:
+    """scales: (slot, adapter_scale) pairs; every slot not listed gets 0."""
+    import numpy as np
+    ids = np.ascontiguousarray([int(i) for i, _ in scales], dtype=np.int32)
+    sc = np.ascontiguousarray([float(v) for _, v in scales], dtype=np.float32)
+    _check(lib().lora_set_scales(ctypes.byref(rt), ids.ctypes.data_as(_i32p),
+                                 sc.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), len(ids),
+                                 _stream(stream)))
+
+
+def lora_select_victim_slot(cache) -> int:
+    """cache: (slot, filled, ref_count, last_used) tuples; returns the slot a
+    promotion overwrites, or raises LoraError(LORA_ERR_POOL_FULL)."""
+    arr = (lora_slot_view * max(1, len(cache)))()
+    for i, (slot, filled, ref_count, last_used) in enumerate(cache):
+        arr[i] = lora_slot_view(int(slot), int(bool(filled)), int(ref_count), 0, int(last_used))
+    out = ctypes.c_int32(-1)
+    _check(lib().lora_select_victim_slot(arr, len(cache), ctypes.byref(out)))
+    return int(out.value)
 
 
 def lora_proj_workspace_bytes(M: int, rt: lora_route) -> int:

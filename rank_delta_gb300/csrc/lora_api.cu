@@ -303,6 +303,60 @@ lora_status lora_set_scale(const lora_route *rt, int slot, float adapter_scale, 
     return ok();
 }
 
+lora_status lora_set_scales(const lora_route *rt, const int32_t *ids, const float *scales, int n,
+                            lora_stream_t stream)
+{
+    const char *who = "lora_set_scales";
+    lora_status s = check_route(rt, who);
+    if (s != LORA_OK)
+        return s;
+    if (n < 0)
+        return fail(LORA_ERR_SHAPE, "%s: n %d is negative", who, n);
+    if (n > 0 && (ids == nullptr || scales == nullptr))
+        return fail(LORA_ERR_NULL, "%s: ids and scales must be non-NULL when n > 0", who);
+    for (int i = 0; i < n; ++i)
+        if (ids[i] < 0 || ids[i] >= rt->max_loras)
+            return fail(LORA_ERR_RANGE, "%s: lora adapter id %d is out of range: %d slot(s) in the route (ids 0..%d)",
+                        who, ids[i], rt->max_loras, rt->max_loras - 1);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    for (int first = 0; first < rt->max_loras; first += SCALE_CHUNK) {
+        ScaleChunk c;
+        c.first = first;
+        c.count = rt->max_loras - first < SCALE_CHUNK ? rt->max_loras - first : SCALE_CHUNK;
+        for (int i = 0; i < SCALE_CHUNK; ++i)
+            c.s[i] = 0.0f; // not listed: scale 0
+        for (int i = 0; i < n; ++i) // in order, so the last entry of an id wins
+            if (ids[i] >= first && ids[i] < first + c.count)
+                c.s[ids[i] - first] = scales[i];
+        cudaError_t e = launch_scales_set(*rt, c, st);
+        if (e != cudaSuccess)
+            return cuda_fail(e, who);
+    }
+    return ok();
+}
+
+lora_status lora_select_victim_slot(const lora_slot_view *cache, int n, int32_t *victim)
+{
+    const char *who = "lora_select_victim_slot";
+    if (n < 0)
+        return fail(LORA_ERR_SHAPE, "%s: n %d is negative", who, n);
+    if ((n > 0 && cache == nullptr) || victim == nullptr)
+        return fail(LORA_ERR_NULL, "%s: cache and victim must be non-NULL", who);
+    for (int i = 0; i < n; ++i)
+        if (!cache[i].filled) {
+            *victim = cache[i].slot;
+            return ok();
+        }
+    int best = -1;
+    for (int i = 0; i < n; ++i)
+        if (cache[i].ref_count == 0 && (best < 0 || cache[i].last_used < cache[best].last_used))
+            best = i; // strict <: the first of equal last_used values is kept
+    if (best < 0)
+        return fail(LORA_ERR_POOL_FULL, "%s: all %d cached slots are filled and in use", who, n);
+    *victim = cache[best].slot;
+    return ok();
+}
+
 lora_status lora_build_seq_slot(const int32_t *adapter_slots, int n, int padded_n, int active,
                                 int32_t *out)
 {

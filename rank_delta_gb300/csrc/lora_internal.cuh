@@ -143,6 +143,13 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
 cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, const void *b,
                              int rank, float factor, float scale, cudaStream_t st);
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st);
+// Runtime scales of up to SCALE_CHUNK consecutive slots, passed by value.
+constexpr int SCALE_CHUNK = 256;
+struct ScaleChunk {
+    int first, count;
+    float s[SCALE_CHUNK];
+};
+cudaError_t launch_scales_set(const lora_route &rt, const ScaleChunk &c, cudaStream_t st);
 
 // Record `msg` as the thread's last error and return `code` (lora_api.cu).
 lora_status api_fail(lora_status code, const char *msg);

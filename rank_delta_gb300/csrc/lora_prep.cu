@@ -286,6 +286,20 @@ cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, cons
     return cudaGetLastError();
 }
 
+// scale_table[first + i] = s[i] * factor_table[first + i] for i < count.
+__global__ void scales_set_kernel(float *scale_table, const float *factor_table, ScaleChunk c)
+{
+    const int i = threadIdx.x;
+    if (i < c.count)
+        scale_table[c.first + i] = c.s[i] * factor_table[c.first + i];
+}
+
+cudaError_t launch_scales_set(const lora_route &rt, const ScaleChunk &c, cudaStream_t st)
+{
+    scales_set_kernel<<<1, SCALE_CHUNK, 0, st>>>(rt.scale_table, rt.factor_table, c);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st)
 {
     scale_set_kernel<<<1, 1, 0, st>>>(rt.scale_table, rt.factor_table, slot, adapter_scale);

@@ -147,3 +147,40 @@ def test_build_seq_slot_host_helper():
     assert out.tolist() == [3, 2, 0, 2, -1, -1]
     assert rd.lora_build_seq_slot([], 3, 1).tolist() == [-1, -1, -1]
     expect(rd.LORA_ERR_SHAPE, rd.lora_build_seq_slot, [1, 2, 3], 2, 0)
+
+
+def test_set_scales_refuses_an_unknown_id_naming_the_range():
+    rt = fake_route(L=4)
+    expect(rd.LORA_ERR_RANGE, rd.lora_set_scales, rt, [(1, 0.5), (9, 1.0)],
+           contains=("id 9", "4 slot"))
+    expect(rd.LORA_ERR_RANGE, rd.lora_set_scales, rt, [(-1, 0.5)], contains=("id -1",))
+
+
+def _victim_by_the_rules(cache):
+    """The promotion rule restated: first unfilled slot in order; else the
+    ref_count == 0 slot with the smallest last_used (first on a tie); else full."""
+    for slot, filled, _, _ in cache:
+        if not filled:
+            return slot
+    free = [(last, i) for i, (_, _, refs, last) in enumerate(cache) if refs == 0]
+    if not free:
+        return None
+    return cache[min(free)[1]][0]
+
+
+def test_select_victim_slot_follows_the_promotion_rules():
+    assert rd.lora_select_victim_slot([(3, True, 0, 5), (7, False, 0, 0), (9, False, 2, 0)]) == 7
+    assert rd.lora_select_victim_slot([(3, True, 1, 1), (5, True, 0, 10), (6, True, 0, 4),
+                                       (8, True, 0, 4)]) == 6
+    expect(rd.LORA_ERR_POOL_FULL, rd.lora_select_victim_slot, [(1, True, 1, 0), (2, True, 3, 0)])
+    expect(rd.LORA_ERR_POOL_FULL, rd.lora_select_victim_slot, [])
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        n = int(rng.integers(1, 9))
+        cache = [(int(s), bool(rng.random() < 0.8), int(rng.integers(0, 2)), int(rng.integers(0, 6)))
+                 for s in rng.permutation(16)[:n]]
+        want = _victim_by_the_rules(cache)
+        if want is None:
+            expect(rd.LORA_ERR_POOL_FULL, rd.lora_select_victim_slot, cache)
+        else:
+            assert rd.lora_select_victim_slot(cache) == want, cache

@@ -230,3 +230,20 @@ def test_many_slots_in_one_tile_match_oracle():
     base = run.apply(slots=torch.full_like(run.slots, -1), path=rd.LORA_PATH_TC)
     none = wl.seq_slot < 0
     assert np.array_equal(y.view(np.uint16)[none], base.view(np.uint16)[none])
+
+
+def test_set_scales_lists_some_slots_and_zeroes_the_rest(decode, decode_ref):
+    """Listed slots take their (last listed) scale, the others 0: their rows
+    become the base product byte for byte; restoring every scale restores y."""
+    wl = decode.wl
+    rd.lora_set_scales(decode.route.rt, [(0, 0.25), (2, 1.0), (0, 2.0)])
+    tab = decode.route.scale_table()
+    for s, ad in enumerate(wl.adapters):
+        want = {0: 2.0, 2: 1.0}.get(s, 0.0)
+        assert tab[s] == np.float32(oracle.scale(ad.alpha, ad.rank, ad.use_rslora, want)), s
+    y = decode.apply()
+    base = decode.apply(slots=torch.full_like(decode.slots, -1))
+    off = ~np.isin(wl.seq_slot, [0, 2])
+    assert np.array_equal(y[off], base[off])
+    rd.lora_set_scales(decode.route.rt, [(s, ad.adapter_scale) for s, ad in enumerate(wl.adapters)])
+    assert_close(decode.apply(), decode_ref, "after restoring every scale")

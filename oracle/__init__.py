@@ -73,6 +73,10 @@ def _load():
             lib.oracle_moe_slot_sort.restype = None
             lib.oracle_moe_slot_sort.argtypes = [_i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                                  _i32p, _i32p]
+            lib.oracle_embed.restype = None
+            lib.oracle_embed.argtypes = [
+                _i32p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
+                ctypes.POINTER(_u16p), ctypes.POINTER(_u16p), _i32p, _f32p, _f32p]
             _lib = lib
     return _lib
 
@@ -191,6 +195,32 @@ def moe_slot_sort(expert_offsets: np.ndarray, seq_slot: np.ndarray, max_loras: i
     return perm, seg
 
 
+def embed(tokens: np.ndarray, E: np.ndarray, seq_slot: np.ndarray, adapters: Sequence,
+          scales: Optional[Sequence[float]] = None) -> np.ndarray:
+    """Row gather of the adapted matrix: y[i] = E[t_i] + s B[t_i] A, fp32.
+
+    ``E`` [vocab][n_embd] bf16 bits; ``adapters[s]`` holds ``A`` [rank][n_embd]
+    and ``B`` [vocab][rank] (the layouts of the adapted matrix, rows = vocab).
+    """
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    E = np.ascontiguousarray(E, dtype=np.uint16)
+    ss = np.ascontiguousarray(seq_slot, dtype=np.int32)
+    vocab, n_embd = E.shape
+    M = tok.shape[0]
+    assert ss.shape[0] == M
+    t = _Tables(adapters, scales)
+    y = np.empty((M, n_embd), dtype=np.float32)
+    _load().oracle_embed(_p(tok, _i32p), _p(E, _u16p), M, vocab, n_embd, _p(ss, _i32p),
+                         len(adapters), t.A, t.B, _p(t.rank, _i32p), _p(t.scale, _f32p),
+                         _p(y, _f32p))
+    return y
+
+
+def workload_embed(wl) -> np.ndarray:
+    """Oracle output for a ``workloads.EmbedWorkload``."""
+    return embed(wl.tokens, wl.E, wl.seq_slot, wl.adapters)
+
+
 def workload_proj(wl, rows=None, cols=None) -> np.ndarray:
     """Oracle output for a ``workloads.ProjWorkload``."""
     return proj(wl.x, wl.W, wl.seq_slot, wl.adapters, rows=rows, cols=cols)
@@ -217,7 +247,7 @@ class _use_library:
         self.saved = _lib
         lib = ctypes.CDLL(self.path)
         for name in ("oracle_scale", "oracle_slot_sort", "oracle_proj", "oracle_moe",
-                     "oracle_moe_slot_sort"):
+                     "oracle_moe_slot_sort", "oracle_embed"):
             src = getattr(self.saved, name)
             dst = getattr(lib, name)
             dst.restype = src.restype

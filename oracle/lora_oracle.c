@@ -170,6 +170,47 @@ void oracle_proj(const uint16_t *x, int64_t x_stride, const uint16_t *W, int M, 
 }
 
 /*
+ * Embedding row gather through the adapted matrix E + s*B*A (ferrox-core
+ * `weight_matrix/lora.rs`, `LoraDelta::add_row_to`: the delta of ONE row r of
+ * s*B*A is s * (b_r . A), which is what a token-embedding gather needs):
+ *
+ *   y[i][e] = E[t][e] + s * sum_r B_s[t][r] * A_s[r][e],    t = tokens[i]
+ *
+ *   E     [vocab][n_embd] bf16 (the adapted matrix: rows = vocab)
+ *   A[s]  [rank[s]][n_embd] bf16, B[s] [vocab][rank[s]] bf16
+ * The low-rank term is skipped for rows with no delta, as in oracle_proj; a
+ * token outside [0, vocab) gives a zero row. y is [M][n_embd] fp32.
+ */
+void oracle_embed(const int32_t *tokens, const uint16_t *E, int M, int vocab, int n_embd,
+                  const int32_t *seq_slot, int L, const uint16_t *const *A,
+                  const uint16_t *const *B, const int32_t *rank, const float *scale, float *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < M; i++) {
+        float *yr = y + (size_t)i * n_embd;
+        int t = tokens[i];
+        if (t < 0 || t >= vocab) {
+            for (int e = 0; e < n_embd; e++)
+                yr[e] = 0.0f;
+            continue;
+        }
+        int s = seq_slot[i];
+        int on = has_delta(s, L, A, scale);
+        for (int e = 0; e < n_embd; e++) {
+            float v = widen(E[(size_t)t * n_embd + e]);
+            if (on) {
+                const uint16_t *b_of_t = B[s] + (size_t)t * rank[s];
+                float dsum = 0.0f;
+                for (int r = 0; r < rank[s]; r++)
+                    dsum += widen(b_of_t[r]) * widen(A[s][(size_t)r * n_embd + e]);
+                v += scale[s] * dsum;
+            }
+            yr[e] = v;
+        }
+    }
+}
+
+/*
  * MoE expert down projection: slot-row j with expert_offsets[e] <= j <
  * expert_offsets[e+1] is the projection above with expert e's base W[e] and
  * expert e's adapters (A[e*L + s], B[e*L + s], rank[e*L + s], scale[e*L + s]).

@@ -233,6 +233,73 @@ def check_moe_segments():
     assert np.array_equal(perm, want)
 
 
+# --------------------------------------------------------------------------
+# Embedding row gather (ferrox-core lora.rs, LoraDelta::add_row_to)
+# --------------------------------------------------------------------------
+
+
+def small_embed_cases():
+    return [
+        workloads.embed(seed=21, M=9, vocab=40, n_embd=24, L=3, ranks=[4, 8, 16]),
+        workloads.embed(seed=22, M=16, vocab=7, n_embd=33, L=4, ranks=[1, 2, 3, 5], p_none=0.25),
+    ]
+
+
+def check_embed_brute_force(tol=1e-4):
+    """y[i] = E[t_i] + s B[t_i] A in fp64 (the delta row of the materialised
+    s B A, as ferrox's add_row_to defines it)."""
+    for wl in small_embed_cases():
+        y = oracle.workload_embed(wl)
+        E = _f64(wl.E)
+        for i in range(wl.M):
+            t, s = int(wl.tokens[i]), int(wl.seq_slot[i])
+            ref = E[t].copy()
+            if 0 <= s < wl.max_loras:
+                ad = wl.adapters[s]
+                sc = oracle.scale(ad.alpha, ad.rank, ad.use_rslora, ad.adapter_scale)
+                ref += np.float64(sc) * (_f64(ad.B)[t] @ _f64(ad.A))
+            err = np.abs(y[i].astype(np.float64) - ref).max()
+            assert err <= tol * (1.0 + np.abs(ref).max()), (wl.seed, i, err)
+
+
+def check_embed_row_gather_identity():
+    """With E = 0 the gathered row t equals the projection of the unit vector
+    e_t through the flipped pair (A' = B^T, B' = A^T) with a zero base -- the
+    same products in the same order, so byte for byte."""
+    wl = small_embed_cases()[0]
+    E0 = np.zeros_like(wl.E)
+    y = oracle.embed(wl.tokens, E0, wl.seq_slot, wl.adapters)
+    flipped = [Adapter(A=np.ascontiguousarray(ad.B.T), B=np.ascontiguousarray(ad.A.T), rank=ad.rank,
+                       alpha=ad.alpha, use_rslora=ad.use_rslora, adapter_scale=ad.adapter_scale)
+               for ad in wl.adapters]
+    one = _bf([1.0])[0]
+    for i in range(wl.M):
+        x = np.zeros((1, wl.vocab), dtype=np.uint16)
+        x[0, int(wl.tokens[i])] = one
+        W0 = np.zeros((wl.n_embd, wl.vocab), dtype=np.uint16)
+        yp = oracle.proj(x, W0, wl.seq_slot[i:i + 1], flipped)
+        assert np.array_equal(y[i].view(np.uint32), yp[0].view(np.uint32)), i
+
+
+def check_embed_no_delta_rows_are_the_embedding():
+    """Slot -1, a slot >= L, scale 0: the row is E[t] exactly; a token outside
+    the vocabulary gives a zero row."""
+    wl = small_embed_cases()[1]
+    slots = wl.seq_slot.copy()
+    slots[0], slots[1] = -1, wl.max_loras + 2
+    scales = [0.0] + [oracle.scale(a.alpha, a.rank, a.use_rslora, a.adapter_scale)
+                      for a in wl.adapters[1:]]
+    toks = wl.tokens.copy()
+    toks[2] = wl.vocab
+    y = oracle.embed(toks, wl.E, slots, wl.adapters, scales=scales)
+    Ef = bf16_to_f32(wl.E)
+    for i in range(wl.M):
+        if i == 2:
+            assert not y[i].any()
+        elif slots[i] < 0 or slots[i] >= wl.max_loras or slots[i] == 0:
+            assert np.array_equal(y[i].view(np.uint32), Ef[int(toks[i])].view(np.uint32)), i
+
+
 ALL_CHECKS = [
     check_scale_examples,
     check_hand_example,
@@ -245,4 +312,7 @@ ALL_CHECKS = [
     check_batch_is_rows,
     check_slot_sort,
     check_moe_segments,
+    check_embed_brute_force,
+    check_embed_row_gather_identity,
+    check_embed_no_delta_rows_are_the_embedding,
 ]

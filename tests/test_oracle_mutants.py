@@ -36,6 +36,11 @@ MUTANTS = {
     "moe_expert_off_by_one": ("if (expert_offsets[q] <= i && i < expert_offsets[q + 1])",
                               "if (expert_offsets[q] < i && i <= expert_offsets[q + 1])"),
     "widen_wrong_shift": ("uint32_t u = ((uint32_t)b) << 16;", "uint32_t u = ((uint32_t)b) << 15;"),
+    "embed_B_row_of_the_row_index": ("const uint16_t *b_of_t = B[s] + (size_t)t * rank[s];",
+                                     "const uint16_t *b_of_t = B[s] + (size_t)(i % vocab) * rank[s];"),
+    "embed_drop_scale": ("v += scale[s] * dsum;", "v += dsum;"),
+    "embed_A_transposed": ("widen(A[s][(size_t)r * n_embd + e]);",
+                           "widen(A[s][(size_t)e * rank[s] + r]);"),
     "h_uses_pool_row_of_next_slot": ("const uint16_t *arow = A[s] + (size_t)r * K;",
                                      "const uint16_t *arow = A[(s + 1) % L] ? A[(s + 1) % L] + (size_t)r * K : A[s] + (size_t)r * K;"),
 }

@@ -75,3 +75,15 @@ def test_oracle_deterministic(name):
     a = oracle.workload_proj(wl)
     b = oracle.workload_proj(wl)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_embed_brute_force_fp64():
+    P.check_embed_brute_force()
+
+
+def test_embed_is_the_row_gather_of_the_flipped_projection():
+    P.check_embed_row_gather_identity()
+
+
+def test_embed_no_delta_rows_and_out_of_range_tokens():
+    P.check_embed_no_delta_rows_are_the_embedding()

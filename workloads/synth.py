@@ -116,6 +116,23 @@ class MoeWorkload:
     note: str = ""
 
 
+@dataclass
+class EmbedWorkload:
+    """Token-embedding gather through an adapted matrix E + s B A (rows = vocab)."""
+    name: str
+    seed: int
+    M: int
+    vocab: int
+    n_embd: int
+    max_loras: int
+    max_rank: int
+    E: np.ndarray               # [vocab][n_embd] bf16 bits
+    tokens: np.ndarray          # [M] int32 token ids
+    seq_slot: np.ndarray        # [M] int32, <0 = no adapter
+    adapters: List[Optional[Adapter]]  # A [rank][n_embd], B [vocab][rank]
+    note: str = ""
+
+
 # ----------------------------------------------------------------------------
 # Drawing helpers
 # ----------------------------------------------------------------------------
@@ -308,6 +325,28 @@ def random_small(seed: int, M: int, K: int, N: int, L: int, R: int,
     if p_none == 0.0:
         seq_slot[seq_slot < 0] = 0
     return ProjWorkload(f"random{seed}", seed, M, K, N, L, R, W, x, seq_slot, ads)
+
+
+def embed(seed: int = 5, M: int = 64, vocab: int = 32000, n_embd: int = 4096, L: int = 16,
+          R: int = 64, ranks=None, p_none: float = 0.1) -> EmbedWorkload:
+    """Token embedding [vocab][n_embd] ~ N(0, 0.02) gathered for M tokens drawn
+    uniformly from the vocabulary, L adapters (ranks from {8,16,32,64} unless
+    given; A ~ U(+-1/64), B ~ N(0, 0.02), alpha = 2 rank), slots uniform over
+    the adapters with round(p_none M) rows set to -1.
+
+    Draw order: E, then (rank, A, B) per adapter, tokens, slots, the -1 rows.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    E = _normal_bf16(rng, (vocab, n_embd), 0.02)
+    ads: List[Optional[Adapter]] = []
+    for s in range(L):
+        r = int(ranks[s]) if ranks is not None else int(rng.choice([8, 16, 32, 64]))
+        ads.append(_adapter(rng, n_embd, vocab, r, 1.0 / 64, 0.02, alpha=2.0 * r))
+    tokens = rng.integers(0, vocab, size=M, dtype=np.int64).astype(np.int32)
+    seq_slot = rng.integers(0, L, size=M, dtype=np.int64).astype(np.int32)
+    seq_slot = _mark_no_adapter(rng, seq_slot, p_none)
+    return EmbedWorkload("embed", seed, M, vocab, n_embd, L, R, E, tokens, seq_slot, ads,
+                         note="E~N(0,0.02) A~U(+-1/64) B~N(0,0.02) alpha=2r, uniform tokens")
 
 
 CONFIGS = {

@@ -3,6 +3,8 @@
 
 One step = one lora_proj_apply (or lora_moe_down_apply) call over one batch:
 the routing sort, the shrink, the base product and the fused expand-fold.
+--config embed / embed_prefill time lora_embed_apply instead (the token
+embedding row gather with the adapted rows: routing sort + one launch).
 Default workload: the decode batch (64 rows, W [4096 x 4096] bf16, 16
 adapters of ranks {8,16,32,64} in a rank-64 pool, 10% rows without adapter).
 
@@ -42,8 +44,14 @@ DESCRIBE = {
                "rsLoRA alpha=16",
     "moe": "MoE down: 8 experts W_e[4096x14336] bf16, 512 tokens top-2 = 1024 slot-rows, "
            "4 adapters/expert r=16 alpha=32",
+    "embed": "token embedding gather: 64 tokens of E[32000x4096] bf16, 16 adapters r in "
+             "{8,16,32,64} pool R=64, alpha=2r, 10% rows slot -1",
+    "embed_prefill": "token embedding gather: 4096 tokens of E[32000x4096] bf16, 16 adapters r in "
+                     "{8,16,32,64} pool R=64, alpha=2r, 10% rows slot -1",
 }
-BOUND = {"tiny": "hbm", "decode": "hbm", "qkv": "hbm", "prefill": "tensor", "moe": "hbm"}
+BOUND = {"tiny": "hbm", "decode": "hbm", "qkv": "hbm", "prefill": "tensor", "moe": "hbm",
+         "embed": "hbm", "embed_prefill": "hbm"}
+EMBED_ROWS = {"embed": 64, "embed_prefill": 4096}
 # --small: the same kernels on fewer rows, for profiler captures only (never a bench line)
 SMALL = {"prefill": {"seq_len": 256}, "moe": {"tokens": 128}}
 
@@ -82,6 +90,25 @@ def proj_algorithmic(wl):
     for s in touched:
         r = wl.adapters[s].rank
         byts += (r * K + N * r) * 2
+    return float(byts), float(flops)
+
+
+def embed_algorithmic(wl):
+    """E rows read, y rows written, tokens and slots, plus each adapted row's
+    B row and each touched slot's A (true ranks)."""
+    M, n = wl.M, wl.n_embd
+    byts = 2.0 * M * n * 2 + M * 4 * 2
+    flops = 0.0
+    touched = set()
+    for i in range(M):
+        s = int(wl.seq_slot[i])
+        if 0 <= s < wl.max_loras and _scale_on(wl.adapters[s]):
+            r = wl.adapters[s].rank
+            byts += r * 2
+            flops += 2.0 * r * n
+            touched.add(s)
+    for s in touched:
+        byts += wl.adapters[s].rank * n * 2
     return float(byts), float(flops)
 
 
@@ -235,6 +262,40 @@ class MoeSet:
                                self.rts, y, y.stride(0), self.ws, self.ws.numel(), stream)
 
 
+class EmbedSet:
+    """One buffer set of the embedding gather: its own E table, pool, tokens,
+    slots, y and workspace (`like`: copy E from this set instead of the host)."""
+
+    def __init__(self, wl, th, rd, torch, like=None):
+        self.E = like.E.clone() if like is not None else th.to_device_bf16(wl.E)
+        self.x = torch.from_numpy(wl.tokens.astype(np.int32)).cuda()  # the step's input: tokens
+        self.slots = torch.from_numpy(wl.seq_slot.astype(np.int32)).cuda()
+        self.route = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.n_embd, wl.vocab, embed=True)
+        # each adapter's flipped pair on the device once, packed from there into every set
+        if like is None:
+            self.pairs = [None if ad is None else
+                          (th.to_device_bf16(ad.B), th.to_device_bf16(np.ascontiguousarray(ad.A.T)))
+                          for ad in wl.adapters]
+        else:
+            self.pairs = like.pairs
+        for s, ad in enumerate(wl.adapters):
+            if ad is not None:
+                rows, cols = self.pairs[s]
+                rd.lora_embed_pool_pack(self.route.rt, s, rows, cols, ad.rank, ad.alpha,
+                                        ad.use_rslora, ad.adapter_scale)
+        self.y = torch.empty((wl.M, wl.n_embd), dtype=torch.bfloat16, device="cuda")
+        self.ws = th.workspace(rd.lora_embed_workspace_bytes(wl.M, self.route.rt))
+        # what one step touches (the rotation has to cover L2 with these)
+        self.bytes = embed_algorithmic(wl)[0]
+
+    def step(self, wl, rd, stream, x=None, slots=None, y=None):
+        x = self.x if x is None else x
+        slots = self.slots if slots is None else slots
+        y = self.y if y is None else y
+        rd.lora_embed_apply(x, self.E, wl.M, wl.vocab, wl.n_embd, slots, self.route.rt, y,
+                            y.stride(0), self.ws, self.ws.numel(), stream)
+
+
 def max_over_ranks(ms: float, world: int, device: str) -> float:
     """The slowest rank's time: every rank runs an independent replica, so the
     job ends when the last one does."""
@@ -252,9 +313,28 @@ def job_rate(rows: int, steps: int, world: int, elapsed_ms: float) -> float:
 
 
 # kernels one call launches: the routing sort, then one fused tensor-core launch
-# (shrink + base + expand-fold); the CUDA-core path (<= 16 rows) runs the sort,
-# a shrink launch and the GEMV
-LAUNCHES_TC, LAUNCHES_SIMT = 2, 3
+# (shrink + base + expand-fold), with a tensor-core shrink launch between the
+# two from 2048 projection rows; the CUDA-core path (<= 16 rows) runs the sort,
+# a shrink launch and the GEMV; the embedding gather runs the sort and one launch
+LAUNCHES_TC, LAUNCHES_SIMT, LAUNCHES_EMBED = 2, 3, 2
+TC_SHRINK_MIN_ROWS = 2048
+
+
+def launches_per_call(config, rows, kernel):
+    if kernel == "embed_kernel":
+        return LAUNCHES_EMBED
+    if kernel == "simt_kernel":
+        return LAUNCHES_SIMT
+    if config != "moe" and rows >= TC_SHRINK_MIN_ROWS:
+        return LAUNCHES_TC + 1
+    return LAUNCHES_TC
+
+
+def make_workload(config, small=False):
+    import workloads
+    if config in EMBED_ROWS:
+        return workloads.embed(M=EMBED_ROWS[config])
+    return workloads.make(config, **(SMALL.get(config, {}) if small else {}))
 
 
 def run_ours(args, rank, world, local_rank):
@@ -270,14 +350,21 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     rd.lib()
     torch.cuda.set_device(local_rank)
-    wl = workloads.make(args.config, **(SMALL.get(args.config, {}) if args.small else {}))
+    wl = make_workload(args.config, args.small)
     is_moe = args.config == "moe"
+    is_embed = args.config in EMBED_ROWS
     rows = wl.T if is_moe else wl.M
-    algo_bytes, algo_flops = moe_algorithmic(wl) if is_moe else proj_algorithmic(wl)
-    Set = MoeSet if is_moe else ProjSet
+    if is_embed:
+        algo_bytes, algo_flops = embed_algorithmic(wl)
+    else:
+        algo_bytes, algo_flops = moe_algorithmic(wl) if is_moe else proj_algorithmic(wl)
+    Set = MoeSet if is_moe else (EmbedSet if is_embed else ProjSet)
     first = Set(wl, th, rd, torch)
     nsets = max(1, int(np.ceil(3 * L2_BYTES / first.bytes)))
-    sets = [first] + [Set(wl, th, rd, torch) for _ in range(nsets - 1)]
+    if is_embed:
+        sets = [first] + [EmbedSet(wl, th, rd, torch, like=first) for _ in range(nsets - 1)]
+    else:
+        sets = [first] + [Set(wl, th, rd, torch) for _ in range(nsets - 1)]
     stream = torch.cuda.current_stream()
 
     # The timed region replays one CUDA graph holding the K steps (each step's
@@ -329,7 +416,8 @@ def run_ours(args, rank, world, local_rank):
     value = job_rate(rows, args.steps, world, elapsed_ms)
     status = rd.lora_status_get(sets[0].ws)
 
-    # end to end through the C ABI: pinned host x / seq_slot in, y out, every step
+    # end to end through the C ABI: pinned host x (tokens for the embedding) /
+    # seq_slot in, y out, every step
     x_h = sets[0].x.cpu().pin_memory()
     s_h = sets[0].slots.cpu().pin_memory()
     y_h = torch.empty(sets[0].y.shape, dtype=torch.bfloat16).pin_memory()
@@ -365,7 +453,10 @@ def run_ours(args, rank, world, local_rank):
     else:
         achieved = algo_flops / avg_call_s / 1e12
         peak, unit = tf_burst, "TFLOP/s"
-    kernel = "tc_kernel" if (is_moe or rows > 16) else "simt_kernel"
+    if is_embed:
+        kernel = "embed_kernel"
+    else:
+        kernel = "tc_kernel" if (is_moe or rows > 16) else "simt_kernel"
     traffic = recorded_traffic(args.config, kernel)
     out = {
         "metric": METRIC,
@@ -385,14 +476,15 @@ def run_ours(args, rank, world, local_rank):
                                                  if args.small and args.config in SMALL else ""),
             "rows_per_step": rows,
             "parallelism": f"replicas x{world} (rows shard, no collective)",
-            "l2": f"rotating {nsets} buffer sets of {first.bytes / 1e6:.1f} MB (>= 3x L2)",
+            "l2": f"rotating {nsets} buffer sets of {first.bytes / 1e6:.1f} MB "
+                  f"{'touched per step ' if is_embed else ''}(>= 3x L2)",
             "timing": "CUDA events around one replay of a graph of the K steps",
         },
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "rows/s",
-                "h2d_bytes_per_step": int(x_h.numel() * 2 + s_h.numel() * 4),
+                "h2d_bytes_per_step": int(x_h.numel() * x_h.element_size() + s_h.numel() * 4),
                 "d2h_bytes_per_step": int(y_h.numel() * 2)},
-        "gpu_launches": (LAUNCHES_TC if kernel == "tc_kernel" else LAUNCHES_SIMT) * args.steps,
+        "gpu_launches": launches_per_call(args.config, rows, kernel) * args.steps,
         "roofline": {
             "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
             "frac": achieved / peak, "traffic": traffic,
@@ -417,7 +509,11 @@ def oracle_rate(wl, config, budget_s=12.0, cap_s=30.0):
     oracle.build()
     is_moe = config == "moe"
     rows_total = wl.T if is_moe else wl.M
-    fn = oracle.workload_moe if is_moe else oracle.workload_proj
+    if config in EMBED_ROWS:
+        def fn(w, rows):
+            return oracle.embed(w.tokens[rows], w.E, w.seq_slot[rows], w.adapters)
+    else:
+        fn = oracle.workload_moe if is_moe else oracle.workload_proj
     # calibrate on a few rows, then size the sample to ~budget_s
     n0 = min(rows_total, 2)
     idx = np.arange(n0, dtype=np.int32)
@@ -438,15 +534,15 @@ def oracle_rate(wl, config, budget_s=12.0, cap_s=30.0):
     omp = os.environ.get("OMP_NUM_THREADS")
     threads = int(omp) if omp else cores
     return {"value": done / el, "unit": "rows/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} of {rows_total} rows (all {wl.N} output columns each), "
+            "sample": f"{n} of {rows_total} rows (all "
+                      f"{wl.n_embd if config in EMBED_ROWS else wl.N} output columns each), "
                       f"{done // n} pass(es), {el:.1f} s of fp32 C loops"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    import workloads
-    wl = workloads.make(args.config)
+    wl = make_workload(args.config)
     per = []
     cpu = None
     for _ in range(args.warmup):

@@ -6,7 +6,10 @@
  *   y[i,:] = W x_i + s[slot_i] * B[slot_i] (A[slot_i] x_i)        (lora_proj_apply)
  *
  * and the same per slot-row of a mixture-of-experts down projection, with the
- * expert's own base and adapters (lora_moe_down_apply).
+ * expert's own base and adapters (lora_moe_down_apply), and as a row gather of
+ * the adapted token-embedding matrix (lora_embed_apply):
+ *
+ *   y[i,:] = E[t_i,:] + s[slot_i] * B[slot_i][t_i,:] A[slot_i]        t_i = tokens[i]
  *
  * Sources (page title, section):
  *   - ferrox-core `weight_matrix/lora.rs`, module doc ("Layouts", "Scale",
@@ -72,7 +75,14 @@ enum {
 enum {
     LORA_FLAG_SLOT_RANGE = 1u << 0,   /* a seq_slot value >= max_loras was seen; those rows got no delta */
     LORA_FLAG_WAIT_TIMEOUT = 1u << 1, /* an in-kernel wait gave up; that call's output is not valid */
-    LORA_FLAG_BAD_OFFSETS = 1u << 2   /* expert_offsets not non-decreasing within [0, T]; rows outside skipped */
+    LORA_FLAG_BAD_OFFSETS = 1u << 2,  /* expert_offsets not non-decreasing within [0, T]; rows outside skipped */
+    LORA_FLAG_TOKEN_RANGE = 1u << 3   /* lora_embed_apply: a token outside [0, vocab); its row is zero */
+};
+
+/* What a route's pool holds (lora_route.kind). */
+enum {
+    LORA_ROUTE_PROJ = 0, /* a projection's pairs: A [max_rank][n_in], B [n_out][max_rank] */
+    LORA_ROUTE_EMBED = 1 /* a token embedding's pairs: A stored transposed, see lora_embed_route_init */
 };
 
 /* Path selection for lora_proj_apply_ex (lora_proj_apply uses LORA_PATH_AUTO). */
@@ -111,7 +121,9 @@ typedef struct lora_route {
     int32_t n_out;     /* N */
     int32_t max_rank;  /* R: the pool's padded rank */
     int32_t max_loras; /* L: number of slots */
-    uint64_t magic;    /* set by lora_route_init */
+    int32_t kind;      /* LORA_ROUTE_PROJ or LORA_ROUTE_EMBED */
+    int32_t reserved;
+    uint64_t magic;    /* set by lora_route_init / lora_embed_route_init */
 } lora_route;
 
 /* Bytes of one projection's pool: max_loras * (max_rank*n_in + n_out*max_rank) * 2.
@@ -306,6 +318,70 @@ lora_status lora_moe_down_apply(const void *x, int64_t x_stride, const void *con
                                 const int32_t *seq_slot, const lora_route *rts, void *y,
                                 int64_t y_stride, void *ws, size_t ws_bytes,
                                 lora_stream_t stream);
+
+/*
+ * ------------------------------------------------------------------------
+ * Token embedding: a row gather of the adapted matrix E + s B A, with E the
+ * [vocab][n_embd] embedding table (ferrox-core `weight_matrix/lora.rs`,
+ * `LoraDelta::add_row_to`; frink `lora_attach.rs`, `checked_pair`).
+ * ------------------------------------------------------------------------
+ *
+ * An embedding route holds, per slot, A TRANSPOSED as [n_embd][max_rank]
+ * followed by B as [vocab][max_rank] (bf16, zero past the adapter's rank;
+ * a_table[s] points at the first, b_table[s] at the second). Both are
+ * rank-contiguous: a token's B row is one contiguous run, and A^T is the
+ * K-major operand of the tensor-core product. Pool bytes: lora_pool_bytes(
+ * max_loras, max_rank, n_embd, vocab). Same errors as lora_route_init
+ * (n_in there is n_embd here); rt->kind = LORA_ROUTE_EMBED, rt->n_in =
+ * n_embd, rt->n_out = vocab.
+ */
+lora_status lora_embed_route_init(lora_route *rt, void *pool, size_t pool_bytes, void *tables,
+                                  size_t table_bytes, int max_loras, int max_rank, int vocab,
+                                  int n_embd, lora_stream_t stream);
+
+/*
+ * Pack one adapter of an embedding route from the flipped pair the adapter
+ * files carry (frink `lora_attach.rs`, `checked_pair`, embedding branch):
+ *   rows   [vocab][rank] bf16, row-major: the row a token gathers (the
+ *          module layout's B)
+ *   cols   [n_embd][rank] bf16, row-major: the module layout's A, transposed
+ * host or device memory. Neither is transposed: both are copied into the
+ * slot row by row. Scale, slot and rank rules and errors as lora_pool_pack;
+ * the route must be an embedding route (LORA_ERR_UNSUPPORTED otherwise).
+ * lora_pool_pack on an embedding route takes the module layout instead (A
+ * [rank][n_embd], B [vocab][rank]) and transposes A.
+ */
+lora_status lora_embed_pool_pack(const lora_route *rt, int slot, const void *rows, const void *cols,
+                                 int rank, float alpha, int use_rslora, float adapter_scale,
+                                 lora_stream_t stream);
+
+/* Workspace of lora_embed_apply for M rows on embedding route `rt` (routing
+ * sort and status word; 256-byte aligned). 0 if rt is NULL, not initialised
+ * or not an embedding route. */
+size_t lora_embed_workspace_bytes(int M, const lora_route *rt);
+
+/*
+ * y[i, :] = E[t, :] + s * B_s[t, :] A_s,  t = tokens[i], s = seq_slot[i], for i in [0, M).
+ *   tokens    device [M] int32 in [0, vocab)
+ *   E         device [vocab][n_embd] bf16 row-major, 16-byte aligned
+ *   seq_slot  device [M] int32, as for lora_proj_apply
+ *   rt        an embedding route with rt->n_out == vocab, rt->n_in == n_embd
+ *   y         device, M rows of n_embd bf16, row i at y + i*y_stride;
+ *             16-byte aligned, y_stride a multiple of 8 (rows are written by
+ *             16-byte bulk copies)
+ *   ws        device workspace of lora_embed_workspace_bytes(M, rt) bytes
+ * A row with no delta (slot negative, >= max_loras, empty, scale 0) is
+ * E[t, :] byte for byte. A token outside [0, vocab) gives a zero row and
+ * sets LORA_FLAG_TOKEN_RANGE. The delta is accumulated in fp32 over the
+ * rank and added to E in fp32; y is rounded once, to nearest even.
+ * Enqueued on `stream` only (no allocation, no synchronisation; graph-safe).
+ * Errors: NULL pointers (M > 0), a projection route, vocab or n_embd not
+ * matching the route, E or y not 16-byte aligned, y_stride < n_embd or not a
+ * multiple of 8, ws too small.
+ */
+lora_status lora_embed_apply(const int32_t *tokens, const void *E, int M, int vocab, int n_embd,
+                             const int32_t *seq_slot, const lora_route *rt, void *y,
+                             int64_t y_stride, void *ws, size_t ws_bytes, lora_stream_t stream);
 
 /* Read the status word (LORA_FLAG_* bits) of the most recent call that used
  * workspace `ws`. Synchronises `stream` (diagnostic, not a hot-path call). */

@@ -30,6 +30,10 @@ LORA_ERR_POOL_FULL = 9
 LORA_FLAG_SLOT_RANGE = 1 << 0
 LORA_FLAG_WAIT_TIMEOUT = 1 << 1
 LORA_FLAG_BAD_OFFSETS = 1 << 2
+LORA_FLAG_TOKEN_RANGE = 1 << 3
+
+LORA_ROUTE_PROJ = 0
+LORA_ROUTE_EMBED = 1
 
 LORA_PATH_AUTO = 0
 LORA_PATH_SIMT = 1
@@ -58,6 +62,8 @@ class lora_route(ctypes.Structure):
         ("n_out", ctypes.c_int32),
         ("max_rank", ctypes.c_int32),
         ("max_loras", ctypes.c_int32),
+        ("kind", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
         ("magic", ctypes.c_uint64),
     ]
 
@@ -98,6 +104,10 @@ _SIGNATURES = {
     "lora_moe_workspace_bytes": (_sz, [_i, _i, _rtp]),
     "lora_moe_down_apply": (_i, [_vp, _i64, ctypes.POINTER(_vp), _vp, _i, _i, _i, _i, _vp, _rtp,
                                  _vp, _i64, _vp, _sz, _vp]),
+    "lora_embed_route_init": (_i, [_rtp, _vp, _sz, _vp, _sz, _i, _i, _i, _i, _vp]),
+    "lora_embed_pool_pack": (_i, [_rtp, _i, _vp, _vp, _i, _f, _i, _f, _vp]),
+    "lora_embed_workspace_bytes": (_sz, [_i, _rtp]),
+    "lora_embed_apply": (_i, [_vp, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_status_get": (_i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "lora_proj_routing": (_i, [_vp, _i, _i, _i32p, _i32p, _vp]),
     "lora_last_error": (ctypes.c_char_p, []),
@@ -241,6 +251,34 @@ def lora_moe_down_apply(x, x_stride: int, W_e, expert_offsets, E: int, T: int, K
     _check(lib().lora_moe_down_apply(_ptr(x), x_stride, wp, _ptr(expert_offsets), E, T, K, N,
                                      _ptr(seq_slot), arr, _ptr(y), y_stride, _ptr(ws), ws_bytes,
                                      _stream(stream)))
+
+
+def lora_embed_route_init(rt: lora_route, pool, pool_bytes: int, tables, table_bytes: int,
+                          max_loras: int, max_rank: int, vocab: int, n_embd: int, stream=None) -> None:
+    _check(lib().lora_embed_route_init(ctypes.byref(rt), _ptr(pool), pool_bytes, _ptr(tables),
+                                       table_bytes, max_loras, max_rank, vocab, n_embd,
+                                       _stream(stream)))
+
+
+def lora_embed_pool_pack(rt: lora_route, slot: int, rows, cols, rank: int, alpha: float,
+                         use_rslora: bool, adapter_scale: float, stream=None) -> None:
+    """The flipped pair: rows [vocab][rank], cols [n_embd][rank] (device
+    pointers/tensors or host numpy arrays of bf16 bits)."""
+    r = rows.ctypes.data if hasattr(rows, "ctypes") else _ptr(rows)
+    c = cols.ctypes.data if hasattr(cols, "ctypes") else _ptr(cols)
+    _check(lib().lora_embed_pool_pack(ctypes.byref(rt), slot, r, c, rank, alpha,
+                                      int(bool(use_rslora)), adapter_scale, _stream(stream)))
+
+
+def lora_embed_workspace_bytes(M: int, rt: lora_route) -> int:
+    return int(lib().lora_embed_workspace_bytes(M, ctypes.byref(rt)))
+
+
+def lora_embed_apply(tokens, E, M: int, vocab: int, n_embd: int, seq_slot, rt: lora_route, y,
+                     y_stride: int, ws, ws_bytes: int, stream=None) -> None:
+    _check(lib().lora_embed_apply(_ptr(tokens), _ptr(E), M, vocab, n_embd, _ptr(seq_slot),
+                                  ctypes.byref(rt), _ptr(y), y_stride, _ptr(ws), ws_bytes,
+                                  _stream(stream)))
 
 
 def lora_status_get(ws, stream=None) -> int:

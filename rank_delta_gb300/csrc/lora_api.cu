@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include <cudaTypedefs.h>
 
@@ -72,6 +73,23 @@ lora_status check_route(const lora_route *rt, const char *who)
         return fail(LORA_ERR_NULL, "%s: route is NULL", who);
     if (rt->magic != ROUTE_MAGIC)
         return fail(LORA_ERR_NOT_INIT, "%s: route was not set up by lora_route_init", who);
+    return LORA_OK;
+}
+
+// A set-up route of the given kind.
+lora_status check_route_kind(const lora_route *rt, int kind, const char *who)
+{
+    lora_status s = check_route(rt, who);
+    if (s != LORA_OK)
+        return s;
+    if (rt->kind != kind)
+        return fail(LORA_ERR_UNSUPPORTED,
+                    kind == LORA_ROUTE_EMBED
+                        ? "%s: the route holds projection adapters; this call takes a token-embedding "
+                          "route (lora_embed_route_init)"
+                        : "%s: the route holds token-embedding adapters (A stored transposed); this "
+                          "call takes a projection route (lora_route_init)",
+                    who);
     return LORA_OK;
 }
 
@@ -184,42 +202,45 @@ size_t lora_route_table_bytes(int max_loras)
     return table_layout(max_loras).total;
 }
 
-lora_status lora_route_init(lora_route *rt, void *pool, size_t pool_bytes, void *tables,
-                            size_t table_bytes, int max_loras, int max_rank, int n_in, int n_out,
-                            lora_stream_t stream)
+} // extern "C"
+
+namespace {
+
+lora_status route_setup(lora_route *rt, void *pool, size_t pool_bytes, void *tables, size_t table_bytes,
+                        int max_loras, int max_rank, int n_in, int n_out, int kind, const char *who, lora_stream_t stream)
 {
     if (rt == nullptr || pool == nullptr || tables == nullptr)
-        return fail(LORA_ERR_NULL, "lora_route_init: route, pool and tables must be non-NULL");
+        return fail(LORA_ERR_NULL, "%s: route, pool and tables must be non-NULL", who);
     if (max_loras <= 0 || max_rank <= 0 || n_in <= 0 || n_out <= 0)
         return fail(LORA_ERR_SHAPE,
-                    "lora_route_init: sizes must be positive (max_loras %d, max_rank %d, n_in %d, "
+                    "%s: sizes must be positive (max_loras %d, max_rank %d, n_in %d, "
                     "n_out %d)",
-                    max_loras, max_rank, n_in, n_out);
+                    who, max_loras, max_rank, n_in, n_out);
     if (max_loras > MAX_LORAS)
-        return fail(LORA_ERR_UNSUPPORTED, "lora_route_init: max_loras %d exceeds %d", max_loras,
+        return fail(LORA_ERR_UNSUPPORTED, "%s: max_loras %d exceeds %d", who, max_loras,
                     MAX_LORAS);
     if (max_rank > MAX_RANK || max_rank % 8 != 0)
         return fail(LORA_ERR_UNSUPPORTED,
-                    "lora_route_init: max_rank %d must be a multiple of 8 and at most %d", max_rank,
+                    "%s: max_rank %d must be a multiple of 8 and at most %d", who, max_rank,
                     MAX_RANK);
     if (n_in % 8 != 0)
-        return fail(LORA_ERR_ALIGN, "lora_route_init: n_in %d must be a multiple of 8", n_in);
+        return fail(LORA_ERR_ALIGN, "%s: n_in %d must be a multiple of 8", who, n_in);
     if (!aligned16(pool))
-        return fail(LORA_ERR_ALIGN, "lora_route_init: pool must be 16-byte aligned");
+        return fail(LORA_ERR_ALIGN, "%s: pool must be 16-byte aligned", who);
     if ((reinterpret_cast<uintptr_t>(tables) & 255u) != 0)
-        return fail(LORA_ERR_ALIGN, "lora_route_init: tables must be 256-byte aligned");
+        return fail(LORA_ERR_ALIGN, "%s: tables must be 256-byte aligned", who);
     const size_t need_pool = lora_pool_bytes(max_loras, max_rank, n_in, n_out);
     const size_t need_tab = lora_route_table_bytes(max_loras);
     if (pool_bytes < need_pool || table_bytes < need_tab)
         return fail(LORA_ERR_WORKSPACE,
-                    "lora_route_init: pool has %zu bytes (needs %zu for %d slots of [%d x %d] at "
+                    "%s: pool has %zu bytes (needs %zu for %d slots of [%d x %d] at "
                     "max_rank %d), tables have %zu bytes (needs %zu)",
-                    pool_bytes, need_pool, max_loras, n_out, n_in, max_rank, table_bytes, need_tab);
+                    who, pool_bytes, need_pool, max_loras, n_out, n_in, max_rank, table_bytes, need_tab);
     const TableLayout tl = table_layout(max_loras);
     uint8_t *tb = static_cast<uint8_t *>(tables);
     cudaError_t e = cudaMemsetAsync(tables, 0, tl.total, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
-        return cuda_fail(e, "lora_route_init: clearing tables");
+        return cuda_fail(e, who);
     rt->pool = pool;
     rt->a_table = reinterpret_cast<const void **>(tb + tl.a);
     rt->b_table = reinterpret_cast<const void **>(tb + tl.b);
@@ -230,39 +251,85 @@ lora_status lora_route_init(lora_route *rt, void *pool, size_t pool_bytes, void 
     rt->n_out = n_out;
     rt->max_rank = max_rank;
     rt->max_loras = max_loras;
+    rt->kind = kind;
+    rt->reserved = 0;
     rt->magic = ROUTE_MAGIC;
     return ok();
 }
 
-lora_status lora_pool_pack(const lora_route *rt, int slot, const void *A, const void *B, int rank,
-                           float alpha, int use_rslora, float adapter_scale, lora_stream_t stream)
+// A^T [n][R] (rows R apart) of A [rank][n] held in host memory: transposed on
+// the host, then one 2D copy. Pageable sources are staged before the copy
+// call returns, so the temporary may go when it does.
+cudaError_t copy_transposed_from_host(uint16_t *At, int R, const uint16_t *A, int rank, int n,
+                                      cudaStream_t st)
 {
-    lora_status s = check_route(rt, "lora_pool_pack");
+    std::vector<uint16_t> t((size_t)n * rank);
+    for (int k = 0; k < rank; ++k)
+        for (int e = 0; e < n; ++e)
+            t[(size_t)e * rank + k] = A[(size_t)k * n + e];
+    cudaError_t e = cudaMemcpy2DAsync(At, (size_t)R * 2, t.data(), (size_t)rank * 2, (size_t)rank * 2,
+                                      (size_t)n, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st); // the temporary is read before it is freed, pinned or not
+    return e;
+}
+
+bool device_readable(const void *p)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// Copy one adapter into `slot` and publish it (spark_model `lora_delta.rs`,
+// `LoraPair`: zero padding to the pool rank, scale not folded into B).
+// Projection route: A [rank][n_in] and B [n_out][rank], both as given.
+// Embedding route: B [vocab][rank] as given; A^T [n_embd][rank] as given when
+// `a_is_transposed` (the flipped pair), else A [rank][n_embd] is transposed.
+lora_status pack_slot(const lora_route *rt, int slot, const void *A, const void *B, int rank, float alpha,
+                      int use_rslora, float adapter_scale, lora_stream_t stream, bool a_is_transposed)
+{
+    const char *who = a_is_transposed ? "lora_embed_pool_pack" : "lora_pool_pack";
+    lora_status s = a_is_transposed ? check_route_kind(rt, LORA_ROUTE_EMBED, who) : check_route(rt, who);
     if (s != LORA_OK)
         return s;
     if (slot < 0 || slot >= rt->max_loras)
-        return fail(LORA_ERR_RANGE, "lora_pool_pack: slot %d is out of range: pool has %d slot(s)",
-                    slot, rt->max_loras);
+        return fail(LORA_ERR_RANGE, "%s: slot %d is out of range: pool has %d slot(s)", who, slot,
+                    rt->max_loras);
     if (rank <= 0 || rank > rt->max_rank)
         return fail(LORA_ERR_SHAPE,
-                    "lora_pool_pack: rank %d does not fit route [n_out %d x n_in %d] with "
+                    "%s: rank %d does not fit route [n_out %d x n_in %d] with "
                     "max_rank %d (need 1 <= rank <= max_rank; A holds rank*n_in = %lld values, "
                     "B n_out*rank = %lld)",
-                    rank, rt->n_out, rt->n_in, rt->max_rank, (long long)rank * rt->n_in,
+                    who, rank, rt->n_out, rt->n_in, rt->max_rank, (long long)rank * rt->n_in,
                     (long long)rt->n_out * rank);
     if (A == nullptr || B == nullptr)
-        return fail(LORA_ERR_NULL, "lora_pool_pack: A and B must be non-NULL");
+        return fail(LORA_ERR_NULL, a_is_transposed ? "%s: rows and cols must be non-NULL"
+                                                   : "%s: A and B must be non-NULL", who);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int R = rt->max_rank, K = rt->n_in, N = rt->n_out;
+    const bool embed = rt->kind == LORA_ROUTE_EMBED;
     uint8_t *base = static_cast<uint8_t *>(rt->pool) + (size_t)slot * slot_bytes(R, K, N);
-    uint16_t *dA = reinterpret_cast<uint16_t *>(base);
+    uint16_t *dA = reinterpret_cast<uint16_t *>(base); // A [R][K], or A^T [K][R] for an embedding
     uint16_t *dB = reinterpret_cast<uint16_t *>(base + (size_t)R * K * 2);
     // Unpublish first so no apply ordered after this call sees a half-written slot.
     cudaError_t e = launch_table_set(*rt, slot, nullptr, nullptr, 0, 0.0f, 0.0f, st);
     if (e == cudaSuccess)
         e = cudaMemsetAsync(base, 0, slot_bytes(R, K, N), st);
-    if (e == cudaSuccess)
-        e = cudaMemcpyAsync(dA, A, (size_t)rank * K * 2, cudaMemcpyDefault, st);
+    if (e == cudaSuccess) {
+        if (!embed)
+            e = cudaMemcpyAsync(dA, A, (size_t)rank * K * 2, cudaMemcpyDefault, st);
+        else if (a_is_transposed)
+            e = cudaMemcpy2DAsync(dA, (size_t)R * 2, A, (size_t)rank * 2, (size_t)rank * 2, (size_t)K,
+                                  cudaMemcpyDefault, st);
+        else if (device_readable(A))
+            e = launch_transpose_pack(dA, R, static_cast<const uint16_t *>(A), rank, K, st);
+        else
+            e = copy_transposed_from_host(dA, R, static_cast<const uint16_t *>(A), rank, K, st);
+    }
     if (e == cudaSuccess)
         e = cudaMemcpy2DAsync(dB, (size_t)R * 2, B, (size_t)rank * 2, (size_t)rank * 2, (size_t)N,
                               cudaMemcpyDefault, st);
@@ -270,8 +337,43 @@ lora_status lora_pool_pack(const lora_route *rt, int slot, const void *A, const 
     if (e == cudaSuccess)
         e = launch_table_set(*rt, slot, dA, dB, rank, factor, adapter_scale * factor, st);
     if (e != cudaSuccess)
-        return cuda_fail(e, "lora_pool_pack");
+        return cuda_fail(e, who);
     return ok();
+}
+
+} // namespace
+
+extern "C" {
+
+lora_status lora_route_init(lora_route *rt, void *pool, size_t pool_bytes, void *tables,
+                            size_t table_bytes, int max_loras, int max_rank, int n_in, int n_out,
+                            lora_stream_t stream)
+{
+    return route_setup(rt, pool, pool_bytes, tables, table_bytes, max_loras, max_rank, n_in, n_out,
+                       LORA_ROUTE_PROJ, "lora_route_init", stream);
+}
+
+lora_status lora_embed_route_init(lora_route *rt, void *pool, size_t pool_bytes, void *tables,
+                                  size_t table_bytes, int max_loras, int max_rank, int vocab,
+                                  int n_embd, lora_stream_t stream)
+{
+    // the adapted matrix is [vocab][n_embd]: n_in = n_embd, n_out = vocab
+    return route_setup(rt, pool, pool_bytes, tables, table_bytes, max_loras, max_rank, n_embd, vocab,
+                       LORA_ROUTE_EMBED, "lora_embed_route_init", stream);
+}
+
+lora_status lora_pool_pack(const lora_route *rt, int slot, const void *A, const void *B, int rank,
+                           float alpha, int use_rslora, float adapter_scale, lora_stream_t stream)
+{
+    return pack_slot(rt, slot, A, B, rank, alpha, use_rslora, adapter_scale, stream, false);
+}
+
+lora_status lora_embed_pool_pack(const lora_route *rt, int slot, const void *rows, const void *cols,
+                                 int rank, float alpha, int use_rslora, float adapter_scale,
+                                 lora_stream_t stream)
+{
+    // the flipped pair: `cols` is A^T as the slot stores it, `rows` is B
+    return pack_slot(rt, slot, cols, rows, rank, alpha, use_rslora, adapter_scale, stream, true);
 }
 
 lora_status lora_pool_unpack(const lora_route *rt, int slot, lora_stream_t stream)
@@ -487,7 +589,7 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
                        void *ws, size_t ws_bytes, int path, lora_stream_t stream)
 {
     const char *who = "lora_proj_apply";
-    lora_status s = check_route(rt, who);
+    lora_status s = check_route_kind(rt, LORA_ROUTE_PROJ, who);
     if (s != LORA_OK)
         return s;
     if (M < 0)
@@ -591,7 +693,7 @@ lora_status lora_moe_down_apply(const void *x, int64_t x_stride, const void *con
     if (rts == nullptr || W_e == nullptr || expert_offsets == nullptr)
         return fail(LORA_ERR_NULL, "%s: rts, W_e and expert_offsets must be non-NULL", who);
     for (int q = 0; q < E; ++q) {
-        lora_status s = check_route(&rts[q], who);
+        lora_status s = check_route_kind(&rts[q], LORA_ROUTE_PROJ, who);
         if (s != LORA_OK)
             return s;
         if (rts[q].n_in != K || rts[q].n_out != N || rts[q].max_rank != rts[0].max_rank ||
@@ -643,6 +745,79 @@ lora_status lora_moe_down_apply(const void *x, int64_t x_stride, const void *con
     p.tn = moe_token_tile(T, E);
     p.max_tiles = moe_max_tiles(T, E);
     return run(p, LORA_PATH_TC, reinterpret_cast<cudaStream_t>(stream), who);
+}
+
+size_t lora_embed_workspace_bytes(int M, const lora_route *rt)
+{
+    if (rt == nullptr || rt->magic != ROUTE_MAGIC || rt->kind != LORA_ROUTE_EMBED || M < 0)
+        return 0;
+    return ws_layout(M, rt->max_loras + 1, 0, 1).total; // routing sort and status only
+}
+
+lora_status lora_embed_apply(const int32_t *tokens, const void *E, int M, int vocab, int n_embd,
+                             const int32_t *seq_slot, const lora_route *rt, void *y, int64_t y_stride,
+                             void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    const char *who = "lora_embed_apply";
+    lora_status s = check_route_kind(rt, LORA_ROUTE_EMBED, who);
+    if (s != LORA_OK)
+        return s;
+    if (M < 0)
+        return fail(LORA_ERR_SHAPE, "%s: M %d is negative", who, M);
+    if (vocab != rt->n_out || n_embd != rt->n_in)
+        return fail(LORA_ERR_SHAPE, "%s: E is [vocab %d][n_embd %d], but the route is [vocab %d x n_embd %d]",
+                    who, vocab, n_embd, rt->n_out, rt->n_in);
+    if (M == 0)
+        return ok();
+    if (tokens == nullptr || E == nullptr || seq_slot == nullptr || y == nullptr)
+        return fail(LORA_ERR_NULL, "%s: tokens, E, seq_slot and y must be non-NULL", who);
+    if (!aligned16(E) || !aligned16(y))
+        return fail(LORA_ERR_ALIGN, "%s: E and y must be 16-byte aligned", who);
+    if (y_stride < n_embd || y_stride % 8 != 0)
+        return fail(LORA_ERR_ALIGN, "%s: y_stride %lld must be >= n_embd %d and a multiple of 8", who,
+                    (long long)y_stride, n_embd);
+    DevInfo di;
+    if (!device_info(di))
+        return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
+    // the routing kernel: one expert segment, no shrink work units
+    Params p;
+    memset(&p, 0, sizeof p);
+    p.seq_slot = seq_slot;
+    p.expert_offsets = nullptr;
+    p.E = 1;
+    p.rows = M;
+    p.K = n_embd;
+    p.N = vocab;
+    p.L = rt->max_loras;
+    p.R = rt->max_rank;
+    p.tab[0] = tables_of(*rt);
+    p.kp = 1;
+    p.no_units = 1;
+    if ((s = carve_ws(ws, ws_bytes, M, p.L + 1, 0, 1, 0, 0, p.ws, who)) != LORA_OK)
+        return s;
+    EmbedParams ep;
+    memset(&ep, 0, sizeof ep);
+    ep.E = static_cast<const uint16_t *>(E);
+    ep.tokens = tokens;
+    ep.y = static_cast<uint16_t *>(y);
+    ep.y_stride = y_stride;
+    ep.M = M;
+    ep.vocab = vocab;
+    ep.n_embd = n_embd;
+    ep.L = rt->max_loras;
+    ep.R = rt->max_rank;
+    ep.tn = embed_chunk_rows(M, ep.R);
+    ep.nft = (n_embd + 127) / 128;
+    ep.tab = p.tab[0];
+    ep.ws = p.ws;
+    p.tn = ep.tn;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_prep(p, st);
+    if (e == cudaSuccess)
+        e = launch_embed(ep, di.num_sms, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, who);
+    return ok();
 }
 
 lora_status lora_status_get(const void *ws, uint32_t *flags, lora_stream_t stream)

@@ -143,6 +143,8 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
 cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, const void *b,
                              int rank, float factor, float scale, cudaStream_t st);
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st);
+// A^T [n][R] of a device A [rank][n], into a zeroed slot.
+cudaError_t launch_transpose_pack(uint16_t *At, int R, const uint16_t *A, int rank, int n, cudaStream_t st);
 // Runtime scales of up to SCALE_CHUNK consecutive slots, passed by value.
 constexpr int SCALE_CHUNK = 256;
 struct ScaleChunk {
@@ -150,6 +152,27 @@ struct ScaleChunk {
     float s[SCALE_CHUNK];
 };
 cudaError_t launch_scales_set(const lora_route &rt, const ScaleChunk &c, cudaStream_t st);
+
+// Embedding row gather with the adapted rows (lora_embed.cu):
+//   y[i, :] = E[t_i, :] + s * B[t_i, :] A,  t_i = tokens[i], s = the scale of seq_slot[i].
+// The pool of an embedding route stores A transposed, [n_embd][max_rank]
+// (rank contiguous: the K-major operand of the tensor-core product), then B
+// as [vocab][max_rank].
+struct EmbedParams {
+    const uint16_t *E;      // [vocab][n_embd]
+    const int32_t *tokens;  // [M]
+    uint16_t *y;
+    int64_t y_stride;
+    int M, vocab, n_embd, L, R;
+    int tn;  // rows per chunk at most (the UMMA N of a chunk), a multiple of 16
+    int nft; // feature tiles of 128
+    Tables tab;
+    Ws ws;
+};
+// Largest chunk (multiple of 16, at most 256 and at most M rounded up) whose
+// double-buffered operands and row tiles fit in shared memory.
+int embed_chunk_rows(int M, int R);
+cudaError_t launch_embed(const EmbedParams &p, int num_sms, cudaStream_t st);
 
 // Record `msg` as the thread's last error and return `code` (lora_api.cu).
 lora_status api_fail(lora_status code, const char *msg);

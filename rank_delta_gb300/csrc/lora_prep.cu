@@ -300,6 +300,33 @@ cudaError_t launch_scales_set(const lora_route &rt, const ScaleChunk &c, cudaStr
     return cudaGetLastError();
 }
 
+// At[e][k] = A[k][e] for k < rank, e < n (rows of At are R apart; the rest of
+// the slot was zeroed before). 32 x 32 tiles through shared memory, so both
+// the reads and the writes are row runs.
+__global__ void transpose_pack_kernel(uint16_t *At, int R, const uint16_t *A, int rank, int n)
+{
+    __shared__ uint16_t tile[32][33];
+    const int e0 = blockIdx.x * 32, k0 = blockIdx.y * 32;
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int k = k0 + r, e = e0 + threadIdx.x;
+        if (k < rank && e < n)
+            tile[r][threadIdx.x] = A[(size_t)k * n + e];
+    }
+    __syncthreads();
+    for (int r = threadIdx.y; r < 32; r += 8) {
+        const int e = e0 + r, k = k0 + threadIdx.x;
+        if (e < n && k < rank)
+            At[(size_t)e * R + k] = tile[threadIdx.x][r];
+    }
+}
+
+cudaError_t launch_transpose_pack(uint16_t *At, int R, const uint16_t *A, int rank, int n, cudaStream_t st)
+{
+    transpose_pack_kernel<<<dim3((unsigned)((n + 31) / 32), (unsigned)((rank + 31) / 32)), dim3(32, 8), 0, st>>>(
+        At, R, A, rank, n);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st)
 {
     scale_set_kernel<<<1, 1, 0, st>>>(rt.scale_table, rt.factor_table, slot, adapter_scale);

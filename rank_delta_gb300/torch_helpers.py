@@ -31,18 +31,33 @@ def workspace(nbytes: int, device="cuda") -> torch.Tensor:
 
 
 class DeviceRoute:
-    """A route whose pool and tables are torch allocations on one device."""
+    """A route whose pool and tables are torch allocations on one device.
+
+    ``embed=True`` makes a token-embedding route: n_in is n_embd and n_out is
+    the vocabulary (the adapted matrix is [vocab][n_embd]).
+    """
 
     def __init__(self, max_loras: int, max_rank: int, n_in: int, n_out: int, device="cuda",
-                 stream=None):
+                 stream=None, embed: bool = False):
         self.L, self.R, self.K, self.N = max_loras, max_rank, n_in, n_out
         self.pool_bytes = rd.lora_pool_bytes(max_loras, max_rank, n_in, n_out)
         self.table_bytes = rd.lora_route_table_bytes(max_loras)
         self.pool = torch.empty(self.pool_bytes, dtype=torch.uint8, device=device)
         self.tables = torch.empty(self.table_bytes, dtype=torch.uint8, device=device)
         self.rt = rd.lora_route()
-        rd.lora_route_init(self.rt, self.pool, self.pool_bytes, self.tables, self.table_bytes,
-                           max_loras, max_rank, n_in, n_out, stream)
+        if embed:
+            rd.lora_embed_route_init(self.rt, self.pool, self.pool_bytes, self.tables,
+                                     self.table_bytes, max_loras, max_rank, n_out, n_in, stream)
+        else:
+            rd.lora_route_init(self.rt, self.pool, self.pool_bytes, self.tables, self.table_bytes,
+                               max_loras, max_rank, n_in, n_out, stream)
+
+    def pack_flipped(self, slot: int, adapter, stream=None) -> None:
+        """Pack a ``workloads.Adapter`` of an embedding route through the
+        flipped pair: rows = B [vocab][rank], cols = A^T [n_embd][rank]."""
+        rd.lora_embed_pool_pack(self.rt, slot, np.ascontiguousarray(adapter.B),
+                                np.ascontiguousarray(np.asarray(adapter.A).T), adapter.rank,
+                                adapter.alpha, adapter.use_rslora, adapter.adapter_scale, stream)
 
     def pack(self, slot: int, adapter, stream=None) -> None:
         """Pack a ``workloads.Adapter`` (host bf16 bits) into `slot`."""

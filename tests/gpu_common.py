@@ -60,3 +60,37 @@ class ProjRun:
         torch.cuda.synchronize()
         self.last_status = rd.lora_status_get(ws)
         return th.to_numpy_bf16(y)
+
+
+class EmbedRun:
+    """Device-resident copy of an EmbedWorkload with its embedding route packed."""
+
+    def __init__(self, wl, device="cuda", flipped=False):
+        self.wl = wl
+        self.E = th.to_device_bf16(wl.E, device)
+        self.tokens = torch.from_numpy(np.ascontiguousarray(wl.tokens, np.int32)).to(device)
+        self.slots = torch.from_numpy(np.ascontiguousarray(wl.seq_slot, np.int32)).to(device)
+        self.route = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.n_embd, wl.vocab, device,
+                                    embed=True)
+        for s, ad in enumerate(wl.adapters):
+            if ad is not None:
+                if flipped:
+                    self.route.pack_flipped(s, ad)
+                else:
+                    self.route.pack(s, ad)
+        self.ws = th.workspace(rd.lora_embed_workspace_bytes(wl.M, self.route.rt), device)
+        self.device = device
+
+    def apply(self, tokens=None, slots=None, y_stride=None):
+        wl = self.wl
+        tok = self.tokens if tokens is None else tokens
+        s = self.slots if slots is None else slots
+        M = tok.shape[0]
+        ys = wl.n_embd if y_stride is None else y_stride
+        y = torch.full((M, ys), SENTINEL, dtype=torch.int16, device=self.device)
+        ws = self.ws if M <= wl.M else th.workspace(rd.lora_embed_workspace_bytes(M, self.route.rt))
+        rd.lora_embed_apply(tok, self.E, M, wl.vocab, wl.n_embd, s, self.route.rt, y, ys, ws,
+                            ws.numel())
+        torch.cuda.synchronize()
+        self.last_status = rd.lora_status_get(ws)
+        return th.to_numpy_bf16(y.view(torch.bfloat16)[:, :wl.n_embd])

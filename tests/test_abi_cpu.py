@@ -47,10 +47,11 @@ def test_pool_bytes_layout():
     assert rd.lora_route_table_bytes(0) == 0
 
 
-def fake_route(L=4, R=8, K=256, N=256):
+def fake_route(L=4, R=8, K=256, N=256, kind=rd.LORA_ROUTE_PROJ):
     rt = rd.lora_route()
     rt.pool = rt.a_table = rt.b_table = rt.scale_table = rt.factor_table = rt.rank_table = 256
     rt.n_in, rt.n_out, rt.max_rank, rt.max_loras, rt.magic = K, N, R, L, MAGIC
+    rt.kind = kind
     return rt
 
 
@@ -184,3 +185,47 @@ def test_select_victim_slot_follows_the_promotion_rules():
             expect(rd.LORA_ERR_POOL_FULL, rd.lora_select_victim_slot, cache)
         else:
             assert rd.lora_select_victim_slot(cache) == want, cache
+
+
+def test_embed_argument_checks():
+    # an embedding route: the adapted matrix is [vocab 1000][n_embd 256]
+    rt = fake_route(L=4, R=16, K=256, N=1000, kind=rd.LORA_ROUTE_EMBED)
+    need = rd.lora_embed_workspace_bytes(8, rt)
+    assert need > 0
+    assert rd.lora_embed_workspace_bytes(8, fake_route()) == 0  # a projection route
+
+    def call(**kw):
+        a = dict(dict(tokens=4096, E=8192, M=8, vocab=1000, n_embd=256, seq_slot=4096, rt=rt,
+                      y=4096, y_stride=256, ws=1 << 20, ws_bytes=need), **kw)
+        return lambda: rd.lora_embed_apply(a["tokens"], a["E"], a["M"], a["vocab"], a["n_embd"],
+                                           a["seq_slot"], a["rt"], a["y"], a["y_stride"], a["ws"],
+                                           a["ws_bytes"])
+
+    expect(rd.LORA_ERR_SHAPE, call(vocab=999), contains=("vocab 999", "vocab 1000", "n_embd 256"))
+    expect(rd.LORA_ERR_NULL, call(tokens=0))
+    expect(rd.LORA_ERR_NULL, call(E=0))
+    expect(rd.LORA_ERR_ALIGN, call(E=8200))
+    expect(rd.LORA_ERR_ALIGN, call(y=4100))
+    expect(rd.LORA_ERR_ALIGN, call(y_stride=260))
+    expect(rd.LORA_ERR_ALIGN, call(y_stride=128))
+    expect(rd.LORA_ERR_UNSUPPORTED, call(rt=fake_route(K=256, N=1000)), contains=("embedding",))
+    # and the projection calls refuse an embedding route
+    expect(rd.LORA_ERR_UNSUPPORTED, rd.lora_proj_apply, 4096, 256, 8192, 8, 256, 1000, 4096, rt,
+           4096, 1000, 1 << 20, 1 << 20, contains=("token-embedding",))
+    expect(rd.LORA_ERR_UNSUPPORTED, rd.lora_embed_pool_pack, fake_route(), 0,
+           np.zeros((256, 8), np.uint16), np.zeros((256, 8), np.uint16), 8, 1.0, False, 1.0)
+    expect(rd.LORA_ERR_RANGE, rd.lora_embed_pool_pack, rt, 4, np.zeros((1000, 8), np.uint16),
+           np.zeros((256, 8), np.uint16), 8, 1.0, False, 1.0, contains=("slot 4",))
+    expect(rd.LORA_ERR_SHAPE, rd.lora_embed_pool_pack, rt, 0, np.zeros((1000, 32), np.uint16),
+           np.zeros((256, 32), np.uint16), 32, 1.0, False, 1.0, contains=("max_rank 16",))
+    # M = 0 is a no-op that launches nothing
+    rd.lora_embed_apply(0, 0, 0, 1000, 256, 0, rt, 0, 256, 0, 0)
+
+
+def test_embed_route_init_refusals_name_the_call():
+    rt = rd.lora_route()
+    expect(rd.LORA_ERR_ALIGN, rd.lora_embed_route_init, rt, 256, 1 << 30, 256, 1 << 20, 4, 8, 1000,
+           250, contains=("lora_embed_route_init", "250"))
+    msg = expect(rd.LORA_ERR_WORKSPACE, rd.lora_embed_route_init, rt, 256, 100, 256, 1 << 20, 4, 8,
+                 1000, 256)
+    assert "[1000 x 256]" in msg

@@ -799,6 +799,7 @@ lora_status lora_embed_apply(const int32_t *tokens, const void *E, int M, int vo
     memset(&ep, 0, sizeof ep);
     ep.E = static_cast<const uint16_t *>(E);
     ep.tokens = tokens;
+    ep.seq_slot = seq_slot;
     ep.y = static_cast<uint16_t *>(y);
     ep.y_stride = y_stride;
     ep.M = M;
@@ -806,13 +807,15 @@ lora_status lora_embed_apply(const int32_t *tokens, const void *E, int M, int vo
     ep.n_embd = n_embd;
     ep.L = rt->max_loras;
     ep.R = rt->max_rank;
-    ep.tn = embed_chunk_rows(M, ep.R);
-    ep.nft = (n_embd + 127) / 128;
+    ep.ft = embed_tile_features(ep.R);
+    ep.nft = (n_embd + ep.ft - 1) / ep.ft;
     ep.tab = p.tab[0];
     ep.ws = p.ws;
-    p.tn = ep.tn;
+    p.tn = EMBED_CHUNK_ROWS;
+    // up to EMBED_LOCAL_ROWS rows every CTA sorts the batch itself: one launch
+    ep.local = embed_local_fits(M, ep.ft, ep.R, ep.L) ? 1 : 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_prep(p, st);
+    cudaError_t e = ep.local ? cudaSuccess : launch_prep(p, st);
     if (e == cudaSuccess)
         e = launch_embed(ep, di.num_sms, st);
     if (e != cudaSuccess)

@@ -161,17 +161,25 @@ cudaError_t launch_scales_set(const lora_route &rt, const ScaleChunk &c, cudaStr
 struct EmbedParams {
     const uint16_t *E;      // [vocab][n_embd]
     const int32_t *tokens;  // [M]
+    const int32_t *seq_slot; // [M]
     uint16_t *y;
     int64_t y_stride;
     int M, vocab, n_embd, L, R;
-    int tn;  // rows per chunk at most (the UMMA N of a chunk), a multiple of 16
-    int nft; // feature tiles of 128
+    int ft;  // embedding features per work item (the UMMA N), a multiple of 32
+    int nft; // feature tiles: n_embd / ft rounded up
+    int local; // 1: every CTA sorts the rows itself (no routing kernel); M <= EMBED_LOCAL_ROWS
     Tables tab;
     Ws ws;
 };
-// Largest chunk (multiple of 16, at most 256 and at most M rounded up) whose
-// double-buffered operands and row tiles fit in shared memory.
-int embed_chunk_rows(int M, int R);
+// Rows per chunk of the embedding gather: the UMMA M.
+constexpr int EMBED_CHUNK_ROWS = 128;
+// Features per work item for pool rank R: the widest of 128 / 64 / 32 whose
+// double-buffered operands and E rows fit in shared memory.
+int embed_tile_features(int R);
+// Rows up to which each CTA of the gather sorts the batch by slot itself.
+constexpr int EMBED_LOCAL_ROWS = 4096;
+// Whether the sorted rows of an M-row batch fit in shared memory beside the buffers.
+bool embed_local_fits(int M, int ft, int R, int L);
 cudaError_t launch_embed(const EmbedParams &p, int num_sms, cudaStream_t st);
 
 // Record `msg` as the thread's last error and return `code` (lora_api.cu).

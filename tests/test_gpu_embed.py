@@ -61,6 +61,7 @@ def test_embed_decode_batch_matches_oracle(embed_run):
     (3000, 5000, 384, 4, 64, [64, 8, 32, 16]),   # several chunks per slot
     (300, 2000, 136, 3, 256, [256, 100, 17]),    # four k blocks, ragged ranks
     (1, 64, 8, 1, 8, [8]),                       # one row, one narrow tile
+    (5000, 3000, 256, 6, 16, [16, 8, 16, 4, 12, 16]),  # past the in-kernel sort: routing kernel
 ])
 def test_embed_ragged_shapes_match_oracle(M, vocab, n_embd, L, R, ranks):
     wl = workloads.embed(seed=M + n_embd, M=M, vocab=vocab, n_embd=n_embd, L=L, R=R, ranks=ranks)
@@ -99,8 +100,9 @@ def test_embed_device_pack_transposes_like_host_pack():
     assert torch.equal(host.route.pool, route.pool)
 
 
-def test_embed_out_of_range_tokens_and_slots():
-    wl = workloads.embed(seed=13, M=50, vocab=900, n_embd=256, L=4, R=16, ranks=[16, 8, 16, 4])
+@pytest.mark.parametrize("M", [50, 4500])  # in-kernel sort / routing kernel
+def test_embed_out_of_range_tokens_and_slots(M):
+    wl = workloads.embed(seed=13, M=M, vocab=900, n_embd=256, L=4, R=16, ranks=[16, 8, 16, 4])
     run = EmbedRun(wl)
     tok = wl.tokens.copy()
     tok[[3, 17]] = [wl.vocab, -5]

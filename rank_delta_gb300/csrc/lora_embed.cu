@@ -22,12 +22,13 @@
 // row from TMEM 16 columns at a time, adds, rounds and stores 32 bytes of y.
 //
 // Warps 0-3 (loader): per delta item the B rows of the chunk, the A^T tile
-// (cp.async into the 128-byte-swizzled K-major layout) and the E rows; thread
-// 0 issues the UMMAs. Warps 4-7 (epilogue): TMEM -> scale -> add -> store, and
-// the copy chunks. Two buffers of each kind: one item loads while the previous
-// one drains. Every wait is bounded; a wait that gives up sets
-// LORA_FLAG_WAIT_TIMEOUT and the CTA unwinds (its copies and UMMAs in flight
-// are waited for first).
+// (cp.async into the 128-byte-swizzled K-major layout) and the E rows, without
+// waiting for any of them: the copies' completion is counted on mbarriers.
+// Warp 8 (one thread) issues the UMMAs once an item's operands have landed.
+// Warps 4-7 (epilogue): TMEM -> scale -> add -> store, and the copy chunks.
+// Two buffers of each kind: the loader runs up to two items ahead. Every wait
+// is bounded; a wait that gives up sets LORA_FLAG_WAIT_TIMEOUT and the CTA
+// unwinds (its copies and UMMAs in flight are waited for first).
 #include <cstring>
 
 #include "lora_internal.cuh"
@@ -37,13 +38,18 @@ namespace rd {
 
 namespace {
 
-constexpr int EMB_THREADS = 256;
-constexpr int GRP = 128;                     // threads of the loader and of the epilogue group
+constexpr int LOADERS = 256;                 // warps 0-7: the loader group
+constexpr int GRP = 128;                     // warps 8-11: the epilogue group
+constexpr int EPI0 = LOADERS;                // first epilogue thread
+constexpr int MMA_WARP = (LOADERS + GRP) / 32; // warp 12: the UMMA issuer
+constexpr int EMB_THREADS = LOADERS + GRP + 32;
+constexpr int SORTERS = 256;                 // threads of the in-kernel routing sort
 constexpr int CH = EMBED_CHUNK_ROWS;         // rows per chunk (UMMA M)
 constexpr uint32_t KB_BYTES_G = CH * 128;    // one 64-wide k block of the chunk's B rows
 constexpr int BAR_LOAD = 1, BAR_EPI = 2;     // named barriers of the two groups
 
 struct EmbBars {
+    uint64_t op_full[2];   // operands of buffer b have landed (one arrival per loader thread)
     uint64_t op_empty[2];  // the UMMAs that read operand buffer b are done
     uint64_t acc_full[2];  // accumulator b holds an item's D
     uint64_t acc_empty[2]; // the epilogue has read accumulator b
@@ -58,7 +64,8 @@ struct EmbBars {
 struct EmbCfg {
     uint32_t g_bytes, a_bytes, e_bytes; // one buffer of B rows / of the A^T tile / of E rows
     uint32_t g_off[2], a_off[2], e_off[2];
-    uint32_t seg_off, cpre_off, act_off, ltok_off, crow_off, sperm_off, stok_off, bar_off;
+    uint32_t seg_off, cpre_off, act_off, cbase_off, crem_off, ltok_off, crow_off, sperm_off, stok_off, slot_off,
+        bar_off;
     uint32_t smem_bytes, tmem_cols;
 };
 
@@ -83,37 +90,71 @@ __device__ __forceinline__ void flag_abort(const EmbedParams &p, EmbBars *b)
     atomicOr(p.ws.status, (uint32_t)LORA_FLAG_WAIT_TIMEOUT);
 }
 
-// Item w: chunk w / nft of the bucket list, feature tile w % nft. Bucket b
-// holds cpre[b+1] - cpre[b] chunks of its seg[b+1] - seg[b] rows, balanced
-// (chunk q gets rows [q*cnt/nch, (q+1)*cnt/nch) of the bucket).
-__device__ __forceinline__ Item get_item(const EmbedParams &p, const int *seg, const int *cpre,
-                                         const uint8_t *act, int nb, int w)
+// The bucket list: bucket b holds seg[b+1] - seg[b] rows in
+// cpre[b+1] - cpre[b] chunks, balanced: chunk q has cbase[b] rows, plus one
+// for q < crem[b].
+struct Buckets {
+    const int *seg, *cpre, *cbase, *crem;
+    const uint8_t *act;
+};
+
+// A CTA's work items in order: item w = chunk w / nft x feature tile w % nft,
+// for w = blockIdx.x, + gridDim.x, ... Stepped without dividing; the bucket of
+// the current chunk is a cursor that only moves forward.
+struct ItemIter {
+    int c, f, b;
+    int dc, df; // gridDim.x / nft, gridDim.x % nft
+};
+
+__device__ __forceinline__ ItemIter iter_begin(int nft)
 {
-    Item it;
-    const int c = w / p.nft, f = w % p.nft;
-    int lo = 0, hi = nb; // largest b with cpre[b] <= c (cpre non-decreasing, cpre[0] = 0)
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cpre[mid] <= c)
-            lo = mid;
-        else
-            hi = mid;
+    ItemIter r;
+    r.c = (int)blockIdx.x / nft;
+    r.f = (int)blockIdx.x - r.c * nft;
+    r.dc = (int)gridDim.x / nft;
+    r.df = (int)gridDim.x - r.dc * nft;
+    r.b = 0;
+    return r;
+}
+
+__device__ __forceinline__ void iter_next(ItemIter &r, int nft)
+{
+    r.c += r.dc;
+    r.f += r.df;
+    if (r.f >= nft) {
+        r.f -= nft;
+        ++r.c;
     }
-    const int b = lo;
-    const int q = c - cpre[b], nch = cpre[b + 1] - cpre[b];
-    const long long cnt = seg[b + 1] - seg[b];
-    const int r0 = seg[b] + (int)(q * cnt / nch), r1 = seg[b] + (int)((q + 1) * cnt / nch);
-    it.delta = act[b];
+}
+
+// The item at the iterator (chunk c < the chunk count).
+__device__ __forceinline__ Item iter_item(const EmbedParams &p, const Buckets &bk, ItemIter &r)
+{
+    while (bk.cpre[r.b + 1] <= r.c)
+        ++r.b;
+    const int b = r.b, q = r.c - bk.cpre[b];
+    const int base = bk.cbase[b], rem = bk.crem[b];
+    Item it;
+    it.delta = bk.act[b];
     it.slot = b - 1;
-    it.lo = r0;
-    it.n = r1 - r0;
-    it.f0 = f * p.ft;
+    it.lo = bk.seg[b] + q * base + min(q, rem);
+    it.n = base + (q < rem ? 1 : 0);
+    it.f0 = r.f * p.ft;
     it.fw = min(p.ft, p.n_embd - it.f0);
     return it;
 }
 
-// Exclusive scan of one value per thread over the 256-thread block.
-__device__ __forceinline__ int block_scan_256(int v, int *tmp, int &total)
+// What a delta chunk needs of its slot, read once per CTA from the tables
+// (bucket b = slot b - 1).
+struct SlotRec {
+    const uint16_t *at; // A^T [n_embd][R]
+    const uint16_t *b;  // B [vocab][R]
+    float scale;
+    int rank;
+};
+
+// Exclusive scan of one value per thread over the block.
+__device__ __forceinline__ int block_scan(int v, int *tmp, int &total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
@@ -187,25 +228,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 namespace {
 
-// Loader group (threads 0 .. 127) over the delta chunks: the leader waits
-// until buffer b is free (its UMMAs done, its E rows read); the group reads
-// the chunk's tokens (one row per thread), stages the B rows and the A^T tile
-// (one cp.async group, waited for before the UMMAs) and the E rows (a second
-// group, whose landing the epilogue waits for on e_full); thread 0 issues the
-// UMMAs.
+// Loader group (threads 0 .. 255) over the delta chunks. Per item the leader
+// waits until buffer b is free (its UMMAs done, its E rows read); the group
+// reads the chunk's tokens (one row per thread), then issues the operand
+// copies (B rows, A^T tile; their landing counted on op_full[b]) and the E row
+// copies (counted on e_full[b]), and moves on without waiting for them.
 __device__ void embed_loader(const EmbedParams &p, const EmbCfg &c, EmbBars *bars, uint8_t *smem,
-                             uint32_t tmem, const int *seg, const int *cpre, const uint8_t *act, int nb,
-                             int total, const RowView rv)
+                             const SlotRec *srec, const Buckets &bk, int chunks, const RowView rv)
 {
     const int t = threadIdx.x;
     int32_t *tok = reinterpret_cast<int32_t *>(smem + c.ltok_off); // [128]: token of each chunk row, -1 = out of range
     const int ecpr = p.ft >> 3;                                    // 16-byte chunks of a row in the row buffer
     const uint32_t a_kb = (uint32_t)p.ft * 128u;                   // one 64-wide k block of the A^T tile
+    // the E-row copy of thread t: chunk eq of rows ej0 + estep * i (estep a
+    // multiple of the swizzle period, so the chunk's place is fixed)
+    const int lg = 31 - __clz(ecpr);
+    const int eq = t & (ecpr - 1), ej0 = t >> lg, estep = LOADERS >> lg;
+    const uint32_t erow_bytes = (uint32_t)ecpr * 16u;
+    const uint32_t eswz = erow_chunk(ej0, eq, ecpr) - (uint32_t)ej0 * erow_bytes;
     int u[2] = {0, 0};
     int d = 0;
-    bool issued = false;
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
-        const Item it = get_item(p, seg, cpre, act, nb, w);
+    for (ItemIter r = iter_begin(p.nft); r.c < chunks; iter_next(r, p.nft)) {
+        const Item it = iter_item(p, bk, r);
         if (!it.delta)
             continue; // copy chunks are the epilogue's alone
         const int b = d & 1;
@@ -217,7 +261,7 @@ __device__ void embed_loader(const EmbedParams &p, const EmbCfg &c, EmbBars *bar
                 flag_abort(p, bars);
             *(volatile int *)&bars->go[0] = ok ? 1 : 0;
         }
-        named_bar_sync(BAR_LOAD, GRP);
+        named_bar_sync(BAR_LOAD, LOADERS);
         if (*(volatile int *)&bars->go[0] == 0)
             break;
         if (t < it.n) {
@@ -225,71 +269,91 @@ __device__ void embed_loader(const EmbedParams &p, const EmbCfg &c, EmbBars *bar
             row_at(p, rv, it.lo + t, row, tk);
             tok[t] = tk;
         }
-        named_bar_sync(BAR_LOAD, GRP); // tok[] complete
+        named_bar_sync(BAR_LOAD, LOADERS); // tok[] complete
 
-        const int rank = p.tab.rank_table[it.slot];
-        const int pk = (rank + 15) & ~15; // UMMA K granularity; k >= rank is zero-filled
-        const int cpr = pk >> 3;          // 16-byte chunks of a staged operand row
-        const uint16_t *At = p.tab.a_table[it.slot];
-        const uint16_t *Bt = p.tab.b_table[it.slot];
+        const SlotRec sr = srec[it.slot + 1];
+        const int pk = (sr.rank + 15) & ~15; // UMMA K granularity; k >= rank is zero-filled
+        const int cpr = pk >> 3;             // 16-byte chunks of a staged operand row
         uint8_t *gbuf = smem + c.g_off[b], *abuf = smem + c.a_off[b], *eb = smem + c.e_off[b];
-        // B rows of the chunk (the UMMA's A operand). Rows past n are not
-        // staged: the D rows they feed are never read.
-        for (int f = t; f < it.n * cpr; f += GRP) {
-            const int j = f / cpr, q = f - j * cpr;
-            const int tk = tok[j];
-            const bool has = tk >= 0 && q * 8 < rank;
-            cp_async_16(gbuf + (q >> 3) * KB_BYTES_G + j * 128 + (((q & 7) ^ (j & 7)) << 4),
-                        Bt + (has ? (size_t)tk * p.R + q * 8 : 0), has ? 16u : 0u);
+        // Operands: thread t copies 16-byte chunk t & 7 of each 64-wide k block
+        // of rows t / 8, t / 8 + 32, ... (a row's eight chunks on consecutive
+        // threads; the swizzle term (chunk ^ row) & 7 is the same for all of a
+        // thread's rows). B rows of the chunk are the UMMA's A operand, A^T
+        // rows f0 .. f0 + fw - 1 its B operand; rows past n and past fw are not
+        // staged: the D rows and columns they feed are never read.
+        const int q8 = t & 7, r16 = t >> 3;
+        const uint32_t swz = (uint32_t)((q8 ^ (r16 & 7)) << 4);
+        for (int kb = 0; kb * 8 < cpr; ++kb) {
+            const int q = kb * 8 + q8; // 16-byte chunk along k
+            if (q >= cpr)
+                break;
+            const bool kin = q * 8 < sr.rank;
+            uint8_t *gdst = gbuf + kb * KB_BYTES_G + swz;
+            for (int j = r16; j < it.n; j += LOADERS / 8) {
+                const int tk = tok[j];
+                const bool has = kin && tk >= 0;
+                cp_async_16(gdst + j * 128, sr.b + (has ? (size_t)tk * p.R + q * 8 : 0), has ? 16u : 0u);
+            }
+            uint8_t *adst = abuf + kb * a_kb + swz;
+            const uint16_t *asrc = sr.at + (size_t)it.f0 * p.R + q * 8;
+            for (int e = r16; e < it.fw; e += LOADERS / 8)
+                cp_async_16(adst + e * 128, kin ? asrc + (size_t)e * p.R : sr.at, kin ? 16u : 0u);
         }
-        // A^T rows f0 .. f0 + fw - 1 (the UMMA's B operand); columns past fw
-        // of D are never read either.
-        for (int f = t; f < it.fw * cpr; f += GRP) {
-            const int e = f / cpr, q = f - e * cpr;
-            const bool has = q * 8 < rank;
-            cp_async_16(abuf + (q >> 3) * a_kb + e * 128 + (((q & 7) ^ (e & 7)) << 4),
-                        At + (has ? (size_t)(it.f0 + e) * p.R + q * 8 : 0), has ? 16u : 0u);
-        }
-        cp_async_commit();
-        const int epr = it.fw >> 3;
-        for (int f = t; f < it.n * ecpr; f += GRP) {
-            const int j = f / ecpr, q = f - j * ecpr;
-            const int tk = tok[j];
-            if (q < epr && tk >= 0)
-                cp_async_16(eb + erow_chunk(j, q, ecpr), p.E + (size_t)tk * p.n_embd + it.f0 + q * 8, 16u);
-        }
-        cp_async_commit();
-        cp_async_mbar_arrive_noinc(&bars->e_full[b]);
-        cp_async_wait_group<1>(); // the operand group (the E rows may still be in flight)
-        fence_proxy_async_smem();  // generic-proxy copies, read by the UMMAs
-        named_bar_sync(BAR_LOAD, GRP);
-        if (t == 0) {
-            // A failed wait only skips the issue: the group learns of the abort
-            // at the next item's leader wait, so no thread leaves a barrier early.
-            if (!aborted(bars) && mbar_wait(&bars->acc_empty[b], ((uint32_t)u[b] & 1u) ^ 1u)) {
-                tc_fence_after();
-                const uint32_t acc = tmem + (uint32_t)(b * p.ft);
-                const uint32_t idesc = idesc_bf16_f32(CH, (uint32_t)p.ft);
-                const uint32_t gb = smem_u32(gbuf), ab = smem_u32(abuf);
-                for (int k16 = 0; k16 < pk / 16; ++k16) {
-                    const uint32_t kb = (uint32_t)k16 >> 2, kk = ((uint32_t)k16 & 3u) * 32u;
-                    umma_bf16(acc, sw128_kmajor_desc(gb + kb * KB_BYTES_G + kk),
-                              sw128_kmajor_desc(ab + kb * a_kb + kk), idesc, k16 > 0 ? 1u : 0u);
-                }
-                umma_commit(&bars->op_empty[b]);
-                umma_commit(&bars->acc_full[b]);
-                issued = true;
-            } else if (!aborted(bars)) {
-                flag_abort(p, bars);
+        cp_async_mbar_arrive_noinc(&bars->op_full[b]);
+        // E rows: thread t copies chunk t % ecpr of rows t / ecpr, + 256 / ecpr, ...
+        if (eq < (it.fw >> 3)) {
+            const uint16_t *esrc = p.E + it.f0 + eq * 8;
+            for (int j = ej0; j < it.n; j += estep) {
+                const int tk = tok[j];
+                if (tk >= 0)
+                    cp_async_16(eb + (uint32_t)j * erow_bytes + eswz, esrc + (size_t)tk * p.n_embd, 16u);
             }
         }
+        cp_async_mbar_arrive_noinc(&bars->e_full[b]);
         ++u[b];
         ++d;
     }
-    // Nothing of this CTA may still be in flight when it exits: the cp.async
-    // copies, the UMMAs.
-    cp_async_wait_all();
-    if (t == 0 && issued) {
+    cp_async_wait_all(); // nothing of this CTA may be in flight when it exits
+}
+
+// UMMA issuer (one thread of warp 8): per delta item, once its operands have
+// landed and its accumulator is free, D = B rows x A^T^T over the slot's rank.
+__device__ void embed_mma(const EmbedParams &p, const EmbCfg &c, EmbBars *bars, uint8_t *smem, uint32_t tmem,
+                          const SlotRec *srec, const Buckets &bk, int chunks)
+{
+    const uint32_t a_kb = (uint32_t)p.ft * 128u;
+    const uint32_t idesc = idesc_bf16_f32(CH, (uint32_t)p.ft);
+    int u[2] = {0, 0};
+    int d = 0;
+    bool issued = false;
+    for (ItemIter r = iter_begin(p.nft); r.c < chunks; iter_next(r, p.nft)) {
+        const Item it = iter_item(p, bk, r);
+        if (!it.delta)
+            continue;
+        const int b = d & 1;
+        const uint32_t par = (uint32_t)u[b] & 1u;
+        if (aborted(bars) || !mbar_wait(&bars->op_full[b], par) || !mbar_wait(&bars->acc_empty[b], par ^ 1u)) {
+            if (!aborted(bars))
+                flag_abort(p, bars);
+            break;
+        }
+        fence_proxy_async_smem(); // the copies landed through the generic proxy; the UMMAs read through the async one
+        tc_fence_after();
+        const int pk = (srec[it.slot + 1].rank + 15) & ~15;
+        const uint32_t acc = tmem + (uint32_t)(b * p.ft);
+        const uint32_t gb = smem_u32(smem + c.g_off[b]), ab = smem_u32(smem + c.a_off[b]);
+        for (int k16 = 0; k16 < pk / 16; ++k16) {
+            const uint32_t kb = (uint32_t)k16 >> 2, kk = ((uint32_t)k16 & 3u) * 32u;
+            umma_bf16(acc, sw128_kmajor_desc(gb + kb * KB_BYTES_G + kk), sw128_kmajor_desc(ab + kb * a_kb + kk),
+                      idesc, k16 > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->op_empty[b]);
+        umma_commit(&bars->acc_full[b]);
+        issued = true;
+        ++u[b];
+        ++d;
+    }
+    if (issued) { // every UMMA done before the CTA frees TMEM and exits
         umma_commit(&bars->fin);
         if (!mbar_wait(&bars->fin, 0))
             flag_abort(p, bars);
@@ -307,25 +371,26 @@ __device__ __forceinline__ uint4 add_scaled8(uint4 e, const uint32_t *d, float s
     return o;
 }
 
-// Epilogue group (threads 128 .. 255). Thread et owns row et of a delta chunk
-// (warp 4 + q reads TMEM lanes 32q .. 32q + 31): D row from TMEM 32 columns at
+// Epilogue group (threads 256 .. 383). Thread et owns row et of a delta chunk
+// (warp 8 + q reads TMEM lanes 32q .. 32q + 31): D row from TMEM 32 columns at
 // a time, E row from the row buffer, 16-byte stores of y. Copy chunks: the
 // group copies the E rows to y, 16 bytes per thread, a row's chunks on
 // consecutive threads.
 __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *bars, uint8_t *smem,
-                               uint32_t tmem, const int *seg, const int *cpre, const uint8_t *act, int nb,
-                               int total, const RowView rv)
+                               uint32_t tmem, const SlotRec *srec, const Buckets &bk, int chunks,
+                               const RowView rv)
 {
-    const int et = threadIdx.x - GRP;
+    const int et = threadIdx.x - EPI0;
     const int wq = (threadIdx.x >> 5) & 3;
     int32_t *crow = reinterpret_cast<int32_t *>(smem + c.crow_off); // [128] y row of a copy chunk's row
     int32_t *ctok = crow + CH;                                      // [128] its token, -1 = out of range
     const int ecpr = p.ft >> 3;
+    const int cq = et & (ecpr - 1), cj0 = et >> (31 - __clz(ecpr)), cstep = GRP / ecpr;
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     int u[2] = {0, 0};
     int d = 0;
-    for (int w = blockIdx.x; w < total; w += gridDim.x) {
-        const Item it = get_item(p, seg, cpre, act, nb, w);
+    for (ItemIter r = iter_begin(p.nft); r.c < chunks; iter_next(r, p.nft)) {
+        const Item it = iter_item(p, bk, r);
         if (!it.delta) {
             if (et < it.n) {
                 int i, tk;
@@ -334,14 +399,26 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
                 ctok[et] = tk;
             }
             named_bar_sync(BAR_EPI, GRP);
-            const int epr = it.fw >> 3;
-            for (int f = et; f < it.n * epr; f += GRP) {
-                const int j = f / epr, q = f - j * epr;
-                const int tk = ctok[j];
-                const uint4 v = tk >= 0 ? __ldg(reinterpret_cast<const uint4 *>(
-                                              p.E + (size_t)tk * p.n_embd + it.f0 + q * 8))
-                                        : zero;
-                *reinterpret_cast<uint4 *>(p.y + (size_t)crow[j] * p.y_stride + it.f0 + q * 8) = v;
+            // thread et copies chunk cq of rows cj0, cj0 + cstep, ...; four
+            // loads in flight before their stores
+            if (cq < (it.fw >> 3)) {
+                const uint16_t *src = p.E + it.f0 + cq * 8;
+                uint16_t *dst = p.y + it.f0 + cq * 8;
+                for (int j0 = cj0; j0 < it.n; j0 += 4 * cstep) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int j = j0 + k * cstep;
+                        const int tk = j < it.n ? ctok[j] : -1;
+                        v[k] = tk >= 0 ? __ldg(reinterpret_cast<const uint4 *>(src + (size_t)tk * p.n_embd)) : zero;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int j = j0 + k * cstep;
+                        if (j < it.n)
+                            *reinterpret_cast<uint4 *>(dst + (size_t)crow[j] * p.y_stride) = v[k];
+                    }
+                }
             }
             named_bar_sync(BAR_EPI, GRP); // crow / ctok are rewritten by the next copy chunk
             continue;
@@ -354,6 +431,7 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
             row_at(p, rv, it.lo + et, yrow, tk);
             tvalid = tk >= 0;
         }
+        const float sc = srec[it.slot + 1].scale;
         if (et == 0) {
             const uint32_t par = (uint32_t)u[b] & 1u;
             const bool ok = !aborted(bars) && mbar_wait(&bars->e_full[b], par) &&
@@ -368,25 +446,28 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
         mbar_wait(&bars->e_full[b], (uint32_t)u[b] & 1u); // complete: the copied rows are visible here
         tc_fence_after();
         if (wq * 32 < it.n) { // TMEM loads are per warp: a warp with no row of the chunk skips them
-            const float sc = p.tab.scale_table[it.slot];
             const uint32_t tb = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(b * p.ft);
             const uint8_t *eb = smem + c.e_off[b];
             uint16_t *yr = p.y + (size_t)yrow * p.y_stride + it.f0;
             const bool mine = et < it.n;
-            for (int c0 = 0; c0 < it.fw; c0 += 32) {
-                uint32_t r[2][16];
-                tmem_ld16_nowait(tb + (uint32_t)c0, r[0]);
-                tmem_ld16_nowait(tb + (uint32_t)c0 + 16u, r[1]);
+            for (int c0 = 0; c0 < it.fw; c0 += 64) {
+                // up to four 16-column loads in flight per wait (ft is a
+                // multiple of 32, so column c0 + 16g < ft is a whole load)
+                uint32_t r[4][16];
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    if (c0 + 16 * g < p.ft)
+                        tmem_ld16_nowait(tb + (uint32_t)(c0 + 16 * g), r[g]);
                 tmem_wait_ld();
                 if (mine) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = c0 + 8 * g;
+                    for (int h = 0; h < 8; ++h) {
+                        const int col = c0 + 8 * h;
                         if (col < it.fw) {
                             const uint4 e = tvalid ? *reinterpret_cast<const uint4 *>(
                                                          eb + erow_chunk(et, col >> 3, ecpr))
                                                    : zero;
-                            *reinterpret_cast<uint4 *>(yr + col) = add_scaled8(e, &r[g >> 1][(g & 1) * 8], sc);
+                            *reinterpret_cast<uint4 *>(yr + col) = add_scaled8(e, &r[h >> 1][(h & 1) * 8], sc);
                         }
                     }
                 }
@@ -403,96 +484,113 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
     }
 }
 
-// This CTA's own routing pass over a batch of at most EMBED_LOCAL_ROWS rows:
-// a stable counting sort of the rows by bucket (0 = no valid slot, s + 1 =
-// slot s) into sperm / stok, bucket starts into seg. Stable, so every CTA
-// cuts a bucket into the same chunks (a chunk's feature tiles run on
-// different CTAs). Rows go in rounds of 256 in input order; inside a round a
-// row's place among equal keys is the count in earlier warps (per-warp counts
-// tagged with the round, so they need no clearing) plus its rank in its own
-// warp. CTA 0 writes the call's status word (there is no routing kernel).
-// fill: [nb] scratch; wc: [8][nb] scratch.
-__device__ void local_route(const EmbedParams &p, int *seg, int *fill, uint32_t *wc, int32_t *sperm,
-                            int32_t *stok, int nb, int *scan_tmp)
+// This CTA's own routing pass over a batch of at most EMBED_LOCAL_ROWS rows
+// and EMBED_LOCAL_BUCKETS buckets: a counting sort of the rows by
+// bucket (0 = no valid slot, s + 1 = slot s) into sperm / stok, bucket starts
+// into seg. Deterministic, so every CTA cuts a bucket into the same chunks
+// (a chunk's feature tiles run on different CTAs): thread t of the first 256
+// owns rows t, t + 256, ... (coalesced loads); it counts its keys in its own
+// column of cnt[nb][256] (no atomics), one warp per bucket turns the bucket's
+// counts into exclusive starts, warp 0 scans the bucket totals, and each
+// thread places its rows in its own order, so a bucket lists thread 0's rows,
+// then thread 1's, and so on. CTA 0 writes the call's status word (there is no
+// routing kernel). cnt: [nb][256] and tot: [nb] scratch.
+__device__ void local_route(const EmbedParams &p, int *seg, uint16_t *cnt, int *tot, int32_t *sperm,
+                            int32_t *stok, int nb)
 {
-    constexpr int LR = EMBED_LOCAL_ROWS / EMB_THREADS;
+    constexpr int LR = EMBED_LOCAL_ROWS / SORTERS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int b = tid; b < nb; b += EMB_THREADS)
-        fill[b] = 0;
-    for (int q = tid; q < (EMB_THREADS / 32) * nb; q += EMB_THREADS)
-        wc[q] = 0; // tag 0: no round
+    const bool sorter = tid < SORTERS;
+    uint32_t *cnt32 = reinterpret_cast<uint32_t *>(cnt);
+    for (int q = tid; q < nb * SORTERS / 2; q += EMB_THREADS)
+        cnt32[q] = 0;
     int key[LR], tok[LR];
 #pragma unroll
     for (int k = 0; k < LR; ++k) { // every load issued before any is used
-        const int i = tid + k * EMB_THREADS;
-        key[k] = i < p.M ? p.seq_slot[i] : -1;
-        tok[k] = i < p.M ? p.tokens[i] : 0;
+        const int i = tid + k * SORTERS;
+        const bool in = sorter && i < p.M;
+        key[k] = in ? p.seq_slot[i] : -1;
+        tok[k] = in ? p.tokens[i] : 0;
     }
-    __syncthreads();
     uint32_t fl = 0;
 #pragma unroll
     for (int k = 0; k < LR; ++k) {
-        const int i = tid + k * EMB_THREADS;
-        if (i < p.M) {
+        const int i = tid + k * SORTERS;
+        if (sorter && i < p.M) {
             const int sl = key[k];
             if (sl >= p.L)
                 fl |= LORA_FLAG_SLOT_RANGE;
             key[k] = (sl >= 0 && sl < p.L) ? sl + 1 : 0;
-            atomicAdd(&fill[key[k]], 1);
             if (tok[k] < 0 || tok[k] >= p.vocab) {
                 fl |= LORA_FLAG_TOKEN_RANGE;
                 tok[k] = -1;
             }
+        } else {
+            key[k] = -1;
         }
     }
     __syncthreads();
-    int cnt[4], sum = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int b = tid * 4 + q;
-        cnt[q] = b < nb ? fill[b] : 0;
-        sum += cnt[q];
-    }
-    int total;
-    int ex = block_scan_256(sum, scan_tmp, total);
+    for (int k = 0; k < LR; ++k)
+        if (key[k] >= 0)
+            ++cnt[key[k] * SORTERS + tid];
+    __syncthreads();
+    // bucket b's counts -> exclusive starts, one warp per bucket (lane: 8 entries)
+    for (int b = warp; b < nb; b += EMB_THREADS / 32) {
+        uint4 *rowv = reinterpret_cast<uint4 *>(cnt + b * SORTERS) + lane;
+        const uint4 v = *rowv;
+        uint32_t e[4] = {v.x, v.y, v.z, v.w};
+        int sum = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int b = tid * 4 + q;
-        if (b < nb) {
-            seg[b] = ex;
-            fill[b] = ex; // next free position of the bucket
-            ex += cnt[q];
+        for (int h = 0; h < 4; ++h)
+            sum += (int)(e[h] & 0xffffu) + (int)(e[h] >> 16);
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t2 = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += t2;
         }
+        int run = incl - sum;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int lo = (int)(e[h] & 0xffffu), hi = (int)(e[h] >> 16);
+            e[h] = (uint32_t)run | ((uint32_t)(run + lo) << 16);
+            run += lo + hi;
+        }
+        *rowv = make_uint4(e[0], e[1], e[2], e[3]);
+        if (lane == 31)
+            tot[b] = incl;
     }
-    if (tid == 0)
-        seg[nb] = total;
+    __syncthreads();
+    if (warp == 0) { // bucket starts (two buckets per lane: nb <= 64)
+        const int b0 = lane * 2;
+        const int t0 = b0 < nb ? tot[b0] : 0, t1 = b0 + 1 < nb ? tot[b0 + 1] : 0;
+        int incl = t0 + t1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t2 = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += t2;
+        }
+        const int ex = incl - t0 - t1;
+        if (b0 < nb)
+            seg[b0] = ex;
+        if (b0 + 1 < nb)
+            seg[b0 + 1] = ex + t0;
+        if (lane == 31)
+            seg[nb] = incl;
+    }
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < LR; ++k) {
-        if (k * EMB_THREADS >= p.M)
-            break; // uniform
-        const int i = tid + k * EMB_THREADS;
-        const int b = i < p.M ? key[k] : -1;
-        const unsigned peers = __match_any_sync(0xffffffffu, b);
-        const int rk = __popc(peers & ((1u << lane) - 1u));
-        const uint32_t tag = (uint32_t)(k + 1) << 16;
-        if (b >= 0 && rk == 0)
-            wc[warp * nb + b] = tag | (uint32_t)__popc(peers);
-        __syncthreads();
-        if (b >= 0) {
-            int pos = fill[b] + rk;
-            for (int w = 0; w < warp; ++w) {
-                const uint32_t v = wc[w * nb + b];
-                if ((v & 0xffff0000u) == tag)
-                    pos += (int)(v & 0xffffu);
-            }
-            sperm[pos] = i;
+        if (key[k] >= 0) {
+            uint16_t &c = cnt[key[k] * SORTERS + tid];
+            const int pos = seg[key[k]] + (int)c;
+            c = (uint16_t)(c + 1);
+            sperm[pos] = tid + k * SORTERS;
             stok[pos] = tok[k];
         }
-        __syncthreads();
-        if (b >= 0 && rk == 0)
-            atomicAdd(&fill[b], __popc(peers));
-        __syncthreads();
     }
     const int any_slot = __syncthreads_or((int)(fl & LORA_FLAG_SLOT_RANGE));
     const int any_tok = __syncthreads_or((int)(fl & LORA_FLAG_TOKEN_RANGE));
@@ -513,6 +611,7 @@ __global__ void __launch_bounds__(EMB_THREADS, 1)
     int *seg = reinterpret_cast<int *>(smem + c.seg_off);
     int *cpre = reinterpret_cast<int *>(smem + c.cpre_off);
     uint8_t *act = smem + c.act_off;
+    SlotRec *srec = reinterpret_cast<SlotRec *>(smem + c.slot_off);
     const int warp = threadIdx.x >> 5;
 
     // The next call's routing kernel may launch now; it reads nothing before
@@ -520,10 +619,11 @@ __global__ void __launch_bounds__(EMB_THREADS, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars->op_full[b], LOADERS); // one cp.async arrival per loader thread
             mbar_init(&bars->op_empty[b], 1);
             mbar_init(&bars->acc_full[b], 1);
             mbar_init(&bars->acc_empty[b], 1);
-            mbar_init(&bars->e_full[b], GRP); // one cp.async arrival per loader thread
+            mbar_init(&bars->e_full[b], LOADERS);
             mbar_init(&bars->e_empty[b], 1);
         }
         mbar_init(&bars->fin, 1);
@@ -534,20 +634,29 @@ __global__ void __launch_bounds__(EMB_THREADS, 1)
     if (warp == 0)
         tmem_alloc(&bars->tmem_base, c.tmem_cols);
 
-    // The routing sort: this CTA's own pass over the batch (small batches),
-    // or the routing kernel's result. Then the active flag and chunk count of
-    // each bucket (four buckets per thread, one scan).
     grid_dependency_wait();
     const int nb = p.L + 1;
+    // Each bucket's slot record (the tables are read here once), loads issued
+    // before the routing sort so their latency overlaps it.
+    for (int b = threadIdx.x; b < nb; b += EMB_THREADS) {
+        SlotRec r{nullptr, nullptr, 0.0f, 0};
+        if (b > 0) {
+            r.at = p.tab.a_table[b - 1];
+            r.b = p.tab.b_table[b - 1];
+            r.scale = p.tab.scale_table[b - 1];
+            r.rank = p.tab.rank_table[b - 1];
+        }
+        srec[b] = r;
+    }
+    // The routing sort: this CTA's own pass over the batch (up to
+    // EMBED_LOCAL_ROWS rows), or the routing kernel's result.
     RowView rv;
     if (p.local) {
         int32_t *sperm = reinterpret_cast<int32_t *>(smem + c.sperm_off);
         int32_t *stok = reinterpret_cast<int32_t *>(smem + c.stok_off);
-        // scratch: the row and operand buffers hold nothing yet (fill [nb] in
-        // the first row buffer, the per-warp counts [8][nb] from the first
-        // operand buffer on, at least 32 KB of buffers)
-        local_route(p, seg, reinterpret_cast<int *>(smem + c.e_off[0]),
-                    reinterpret_cast<uint32_t *>(smem + c.g_off[0]), sperm, stok, nb, scan_tmp);
+        // scratch: the operand buffers hold nothing yet
+        uint16_t *cnt = reinterpret_cast<uint16_t *>(smem + c.g_off[0]);
+        local_route(p, seg, cnt, reinterpret_cast<int *>(cnt + (size_t)nb * SORTERS), sperm, stok, nb);
         rv.perm = sperm;
         rv.stok = stok;
     } else {
@@ -557,6 +666,10 @@ __global__ void __launch_bounds__(EMB_THREADS, 1)
         rv.stok = nullptr;
         __syncthreads();
     }
+    // active flag, chunk count and chunk size of each bucket (four per
+    // thread, one scan)
+    int *cbase = reinterpret_cast<int *>(smem + c.cbase_off);
+    int *crem = reinterpret_cast<int *>(smem + c.crem_off);
     int nch[4], sum = 0;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -564,19 +677,16 @@ __global__ void __launch_bounds__(EMB_THREADS, 1)
         nch[q] = 0;
         if (b < nb) {
             const int cnt = seg[b + 1] - seg[b];
-            bool on = false;
-            if (b > 0) {
-                const int s = b - 1;
-                on = p.tab.a_table[s] != nullptr && p.tab.b_table[s] != nullptr &&
-                     p.tab.scale_table[s] != 0.0f && p.tab.rank_table[s] > 0;
-            }
-            act[b] = on ? 1 : 0;
+            const SlotRec r = srec[b];
+            act[b] = (b > 0 && r.at != nullptr && r.b != nullptr && r.scale != 0.0f && r.rank > 0) ? 1 : 0;
             nch[q] = cnt > 0 ? (cnt + CH - 1) / CH : 0;
+            cbase[b] = nch[q] > 0 ? cnt / nch[q] : 0;
+            crem[b] = nch[q] > 0 ? cnt - cbase[b] * nch[q] : 0;
             sum += nch[q];
         }
     }
     int chunks;
-    int ex = block_scan_256(sum, scan_tmp, chunks);
+    int ex = block_scan(sum, scan_tmp, chunks);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const int b = threadIdx.x * 4 + q;
@@ -591,12 +701,14 @@ __global__ void __launch_bounds__(EMB_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const int total = chunks * p.nft;
+    const Buckets bk{seg, cpre, cbase, crem, act};
 
-    if (threadIdx.x < GRP)
-        embed_loader(p, c, bars, smem, tmem, seg, cpre, act, nb, total, rv);
-    else
-        embed_epilogue(p, c, bars, smem, tmem, seg, cpre, act, nb, total, rv);
+    if (threadIdx.x < LOADERS)
+        embed_loader(p, c, bars, smem, srec, bk, chunks, rv);
+    else if (warp < MMA_WARP)
+        embed_epilogue(p, c, bars, smem, tmem, srec, bk, chunks, rv);
+    else if (threadIdx.x == MMA_WARP * 32)
+        embed_mma(p, c, bars, smem, tmem, srec, bk, chunks);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -643,9 +755,12 @@ EmbCfg make_embed_cfg(int ft, int R, int L, int local_rows)
         o += c.e_bytes;
     }
     const uint32_t nb = (uint32_t)L + 1;
+    c.slot_off = o; o = au(o + (uint32_t)sizeof(SlotRec) * nb, 16);
     c.seg_off = o;  o = au(o + 4u * (nb + 1), 16);
     c.cpre_off = o; o = au(o + 4u * (nb + 1), 16);
     c.act_off = o;  o = au(o + nb, 16);
+    c.cbase_off = o; o = au(o + 4u * nb, 16);
+    c.crem_off = o;  o = au(o + 4u * nb, 16);
     c.ltok_off = o; o = au(o + 4u * CH, 16);
     c.crow_off = o; o = au(o + 8u * CH, 16);
     c.sperm_off = o; o = au(o + 4u * (uint32_t)local_rows, 16);
@@ -669,7 +784,10 @@ int embed_tile_features(int R)
 
 bool embed_local_fits(int M, int ft, int R, int L)
 {
-    return M <= EMBED_LOCAL_ROWS && make_embed_cfg(ft, R, L, M).smem_bytes <= SMEM_LIMIT;
+    // the sort's scratch ([L + 1][256] counts and L + 1 totals) lives in the buffers
+    const EmbCfg c = make_embed_cfg(ft, R, L, M);
+    return M <= EMBED_LOCAL_ROWS && L + 1 <= EMBED_LOCAL_BUCKETS && c.smem_bytes <= SMEM_LIMIT &&
+           (uint32_t)(L + 1) * (SORTERS * 2u + 4u) <= c.e_off[0];
 }
 
 cudaError_t launch_embed(const EmbedParams &p, int num_sms, cudaStream_t st)

@@ -176,8 +176,10 @@ constexpr int EMBED_CHUNK_ROWS = 128;
 // Features per work item for pool rank R: the widest of 128 / 64 / 32 whose
 // double-buffered operands and E rows fit in shared memory.
 int embed_tile_features(int R);
-// Rows up to which each CTA of the gather sorts the batch by slot itself.
+// Rows and buckets (max_loras + 1) up to which each CTA of the gather sorts
+// the batch by slot itself.
 constexpr int EMBED_LOCAL_ROWS = 4096;
+constexpr int EMBED_LOCAL_BUCKETS = 64;
 // Whether the sorted rows of an M-row batch fit in shared memory beside the buffers.
 bool embed_local_fits(int M, int ft, int R, int L);
 cudaError_t launch_embed(const EmbedParams &p, int num_sms, cudaStream_t st);

@@ -62,6 +62,7 @@ def test_embed_decode_batch_matches_oracle(embed_run):
     (300, 2000, 136, 3, 256, [256, 100, 17]),    # four k blocks, ragged ranks
     (1, 64, 8, 1, 8, [8]),                       # one row, one narrow tile
     (5000, 3000, 256, 6, 16, [16, 8, 16, 4, 12, 16]),  # past the in-kernel sort: routing kernel
+    (300, 2000, 256, 100, 64, None),             # more slots than the in-kernel sort takes
 ])
 def test_embed_ragged_shapes_match_oracle(M, vocab, n_embd, L, R, ranks):
     wl = workloads.embed(seed=M + n_embd, M=M, vocab=vocab, n_embd=n_embd, L=L, R=R, ranks=ranks)

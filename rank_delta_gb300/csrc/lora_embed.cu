@@ -39,10 +39,11 @@ namespace rd {
 namespace {
 
 constexpr int LOADERS = 256;                 // warps 0-7: the loader group
-constexpr int GRP = 128;                     // warps 8-11: the epilogue group
+constexpr int EPIS = 128;                    // warps 8-11: the epilogue group
 constexpr int EPI0 = LOADERS;                // first epilogue thread
-constexpr int MMA_WARP = (LOADERS + GRP) / 32; // warp 12: the UMMA issuer
-constexpr int EMB_THREADS = LOADERS + GRP + 32;
+constexpr int MMA_WARP = (LOADERS + EPIS) / 32; // warp 12: the UMMA issuer
+constexpr int COL_SPLIT = EPIS / EMBED_CHUNK_ROWS; // epilogue threads per chunk row (each a share of the columns)
+constexpr int EMB_THREADS = LOADERS + EPIS + 32;
 constexpr int SORTERS = 256;                 // threads of the in-kernel routing sort
 constexpr int CH = EMBED_CHUNK_ROWS;         // rows per chunk (UMMA M)
 constexpr uint32_t KB_BYTES_G = CH * 128;    // one 64-wide k block of the chunk's B rows
@@ -371,8 +372,9 @@ __device__ __forceinline__ uint4 add_scaled8(uint4 e, const uint32_t *d, float s
     return o;
 }
 
-// Epilogue group (threads 256 .. 383). Thread et owns row et of a delta chunk
-// (warp 8 + q reads TMEM lanes 32q .. 32q + 31): D row from TMEM 32 columns at
+// Epilogue group (threads 256 .. 383). Thread et owns row et % 128 of a delta
+// chunk, its columns' share et / 128 (warp 8 + q reads TMEM lanes 32q ..
+// 32q + 31): D row from TMEM 32 columns at
 // a time, E row from the row buffer, 16-byte stores of y. Copy chunks: the
 // group copies the E rows to y, 16 bytes per thread, a row's chunks on
 // consecutive threads.
@@ -381,11 +383,18 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
                                const RowView rv)
 {
     const int et = threadIdx.x - EPI0;
-    const int wq = (threadIdx.x >> 5) & 3;
-    int32_t *crow = reinterpret_cast<int32_t *>(smem + c.crow_off); // [128] y row of a copy chunk's row
+    const int wq = (threadIdx.x >> 5) & 3; // TMEM lane quarter of this warp
+    const int er = et & (CH - 1);          // chunk row of this thread in a delta item
+    const int hh = et / CH;                // which share of the item's columns
+    const int half = p.ft / COL_SPLIT;     // columns per share, a multiple of 16
+    int32_t *crow = reinterpret_cast<int32_t *>(smem + c.crow_off); // [128] y row of each chunk row
     int32_t *ctok = crow + CH;                                      // [128] its token, -1 = out of range
     const int ecpr = p.ft >> 3;
-    const int cq = et & (ecpr - 1), cj0 = et >> (31 - __clz(ecpr)), cstep = GRP / ecpr;
+    // copying rows out, thread et takes 16-byte chunk cq of rows cj0, + cstep, ...
+    // (cstep a multiple of the swizzle period: the chunk's place in a row is fixed)
+    const int cq = et & (ecpr - 1), cj0 = et >> (31 - __clz(ecpr)), cstep = EPIS / ecpr;
+    const uint32_t erow_bytes = (uint32_t)ecpr * 16u;
+    const uint32_t cswz = erow_chunk(cj0, cq, ecpr) - (uint32_t)cj0 * erow_bytes;
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     int u[2] = {0, 0};
     int d = 0;
@@ -398,7 +407,7 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
                 crow[et] = i;
                 ctok[et] = tk;
             }
-            named_bar_sync(BAR_EPI, GRP);
+            named_bar_sync(BAR_EPI, EPIS);
             // thread et copies chunk cq of rows cj0, cj0 + cstep, ...; four
             // loads in flight before their stores
             if (cq < (it.fw >> 3)) {
@@ -420,16 +429,17 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
                     }
                 }
             }
-            named_bar_sync(BAR_EPI, GRP); // crow / ctok are rewritten by the next copy chunk
+            named_bar_sync(BAR_EPI, EPIS); // crow / ctok are rewritten by the next copy chunk
             continue;
         }
         const int b = d & 1;
-        int yrow = 0;
         bool tvalid = false;
-        if (et < it.n) {
-            int tk;
-            row_at(p, rv, it.lo + et, yrow, tk);
+        if (er < it.n) {
+            int yrow, tk;
+            row_at(p, rv, it.lo + er, yrow, tk);
             tvalid = tk >= 0;
+            if (hh == 0)
+                crow[er] = yrow;
         }
         const float sc = srec[it.slot + 1].scale;
         if (et == 0) {
@@ -440,45 +450,52 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
                 flag_abort(p, bars);
             *(volatile int *)&bars->go[1] = ok ? 1 : 0;
         }
-        named_bar_sync(BAR_EPI, GRP);
+        named_bar_sync(BAR_EPI, EPIS);
         if (*(volatile int *)&bars->go[1] == 0)
             break;
         mbar_wait(&bars->e_full[b], (uint32_t)u[b] & 1u); // complete: the copied rows are visible here
         tc_fence_after();
+        uint8_t *eb = smem + c.e_off[b];
         if (wq * 32 < it.n) { // TMEM loads are per warp: a warp with no row of the chunk skips them
             const uint32_t tb = tmem + ((uint32_t)(wq * 32) << 16) + (uint32_t)(b * p.ft);
-            const uint8_t *eb = smem + c.e_off[b];
-            uint16_t *yr = p.y + (size_t)yrow * p.y_stride + it.f0;
-            const bool mine = et < it.n;
-            for (int c0 = 0; c0 < it.fw; c0 += 64) {
-                // up to four 16-column loads in flight per wait (ft is a
-                // multiple of 32, so column c0 + 16g < ft is a whole load)
+            const bool mine = er < it.n;
+            const int cend = min(it.fw, (hh + 1) * half);
+            for (int c0 = hh * half; c0 < cend; c0 += 64) {
+                // up to four 16-column loads in flight per wait (half is a
+                // multiple of 16, so column c0 + 16g below the half's end is a
+                // whole load)
                 uint32_t r[4][16];
 #pragma unroll
                 for (int g = 0; g < 4; ++g)
-                    if (c0 + 16 * g < p.ft)
+                    if (c0 + 16 * g < (hh + 1) * half)
                         tmem_ld16_nowait(tb + (uint32_t)(c0 + 16 * g), r[g]);
                 tmem_wait_ld();
                 if (mine) {
 #pragma unroll
                     for (int h = 0; h < 8; ++h) {
                         const int col = c0 + 8 * h;
-                        if (col < it.fw) {
-                            const uint4 e = tvalid ? *reinterpret_cast<const uint4 *>(
-                                                         eb + erow_chunk(et, col >> 3, ecpr))
-                                                   : zero;
-                            *reinterpret_cast<uint4 *>(yr + col) = add_scaled8(e, &r[h >> 1][(h & 1) * 8], sc);
+                        if (col < cend) {
+                            uint4 *ep = reinterpret_cast<uint4 *>(eb + erow_chunk(er, col >> 3, ecpr));
+                            *ep = add_scaled8(tvalid ? *ep : zero, &r[h >> 1][(h & 1) * 8], sc);
                         }
                     }
                 }
             }
         }
         tc_fence_before();
-        named_bar_sync(BAR_EPI, GRP); // accumulator b and row buffer b are read
-        if (et == 0) {
+        named_bar_sync(BAR_EPI, EPIS); // accumulator b is read; the y rows are final in row buffer b
+        if (et == 0)
             mbar_arrive(&bars->acc_empty[b]);
-            mbar_arrive(&bars->e_empty[b]);
+        // y rows out with 16 threads (or fewer) per row: whole rows per store
+        if (cq < (it.fw >> 3)) {
+            uint16_t *dst = p.y + it.f0 + cq * 8;
+            for (int j = cj0; j < it.n; j += cstep)
+                *reinterpret_cast<uint4 *>(dst + (size_t)crow[j] * p.y_stride) =
+                    *reinterpret_cast<const uint4 *>(eb + (uint32_t)j * erow_bytes + cswz);
         }
+        named_bar_sync(BAR_EPI, EPIS); // row buffer b is read; crow is rewritten by the next item
+        if (et == 0)
+            mbar_arrive(&bars->e_empty[b]);
         ++u[b];
         ++d;
     }
@@ -494,9 +511,9 @@ __device__ void embed_epilogue(const EmbedParams &p, const EmbCfg &c, EmbBars *b
 // counts into exclusive starts, warp 0 scans the bucket totals, and each
 // thread places its rows in its own order, so a bucket lists thread 0's rows,
 // then thread 1's, and so on. CTA 0 writes the call's status word (there is no
-// routing kernel). cnt: [nb][256] and tot: [nb] scratch.
+// routing kernel). cnt: [nb][256] and tot: [nb] scratch; sflags: a word.
 __device__ void local_route(const EmbedParams &p, int *seg, uint16_t *cnt, int *tot, int32_t *sperm,
-                            int32_t *stok, int nb)
+                            int32_t *stok, int nb, uint32_t *sflags)
 {
     constexpr int LR = EMBED_LOCAL_ROWS / SORTERS;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -504,6 +521,8 @@ __device__ void local_route(const EmbedParams &p, int *seg, uint16_t *cnt, int *
     uint32_t *cnt32 = reinterpret_cast<uint32_t *>(cnt);
     for (int q = tid; q < nb * SORTERS / 2; q += EMB_THREADS)
         cnt32[q] = 0;
+    if (tid == 0)
+        *sflags = 0;
     int key[LR], tok[LR];
 #pragma unroll
     for (int k = 0; k < LR; ++k) { // every load issued before any is used
@@ -592,11 +611,11 @@ __device__ void local_route(const EmbedParams &p, int *seg, uint16_t *cnt, int *
             stok[pos] = tok[k];
         }
     }
-    const int any_slot = __syncthreads_or((int)(fl & LORA_FLAG_SLOT_RANGE));
-    const int any_tok = __syncthreads_or((int)(fl & LORA_FLAG_TOKEN_RANGE));
+    if (fl != 0)
+        atomicOr(sflags, fl);
+    __syncthreads();
     if (blockIdx.x == 0 && tid == 0)
-        *p.ws.status = (any_slot ? (uint32_t)LORA_FLAG_SLOT_RANGE : 0u) |
-                       (any_tok ? (uint32_t)LORA_FLAG_TOKEN_RANGE : 0u);
+        *p.ws.status = *sflags;
 }
 
 } // namespace
@@ -656,7 +675,8 @@ __global__ void __launch_bounds__(EMB_THREADS, 1)
         int32_t *stok = reinterpret_cast<int32_t *>(smem + c.stok_off);
         // scratch: the operand buffers hold nothing yet
         uint16_t *cnt = reinterpret_cast<uint16_t *>(smem + c.g_off[0]);
-        local_route(p, seg, cnt, reinterpret_cast<int *>(cnt + (size_t)nb * SORTERS), sperm, stok, nb);
+        __shared__ uint32_t s_flags;
+        local_route(p, seg, cnt, reinterpret_cast<int *>(cnt + (size_t)nb * SORTERS), sperm, stok, nb, &s_flags);
         rv.perm = sperm;
         rv.stok = stok;
     } else {
@@ -666,42 +686,71 @@ __global__ void __launch_bounds__(EMB_THREADS, 1)
         rv.stok = nullptr;
         __syncthreads();
     }
-    // active flag, chunk count and chunk size of each bucket (four per
-    // thread, one scan)
+    // active flag, chunk count and chunk size of each bucket, then the chunk
+    // starts: warp 0 alone for up to 64 buckets (two per lane), else four
+    // buckets per thread and a block scan
     int *cbase = reinterpret_cast<int *>(smem + c.cbase_off);
     int *crem = reinterpret_cast<int *>(smem + c.crem_off);
-    int nch[4], sum = 0;
+    __shared__ int s_chunks;
+    auto bucket_chunks = [&](int b) {
+        const int cnt = seg[b + 1] - seg[b];
+        const SlotRec r = srec[b];
+        act[b] = (b > 0 && r.at != nullptr && r.b != nullptr && r.scale != 0.0f && r.rank > 0) ? 1 : 0;
+        const int n = cnt > 0 ? (cnt + CH - 1) / CH : 0;
+        cbase[b] = n > 0 ? cnt / n : 0;
+        crem[b] = n > 0 ? cnt - cbase[b] * n : 0;
+        return n;
+    };
+    if (nb <= 64) {
+        if (warp == 0) {
+            const int lane = threadIdx.x & 31, b0 = 2 * lane;
+            const int n0 = b0 < nb ? bucket_chunks(b0) : 0, n1 = b0 + 1 < nb ? bucket_chunks(b0 + 1) : 0;
+            int incl = n0 + n1;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int b = threadIdx.x * 4 + q;
-        nch[q] = 0;
-        if (b < nb) {
-            const int cnt = seg[b + 1] - seg[b];
-            const SlotRec r = srec[b];
-            act[b] = (b > 0 && r.at != nullptr && r.b != nullptr && r.scale != 0.0f && r.rank > 0) ? 1 : 0;
-            nch[q] = cnt > 0 ? (cnt + CH - 1) / CH : 0;
-            cbase[b] = nch[q] > 0 ? cnt / nch[q] : 0;
-            crem[b] = nch[q] > 0 ? cnt - cbase[b] * nch[q] : 0;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t2 = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += t2;
+            }
+            const int ex = incl - n0 - n1;
+            if (b0 < nb)
+                cpre[b0] = ex;
+            if (b0 + 1 < nb)
+                cpre[b0 + 1] = ex + n0;
+            if (lane == 31) {
+                cpre[nb] = incl;
+                s_chunks = incl;
+            }
+        }
+    } else {
+        int nch[4], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int b = threadIdx.x * 4 + q;
+            nch[q] = b < nb ? bucket_chunks(b) : 0;
             sum += nch[q];
         }
-    }
-    int chunks;
-    int ex = block_scan(sum, scan_tmp, chunks);
+        int total;
+        int ex = block_scan(sum, scan_tmp, total);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int b = threadIdx.x * 4 + q;
-        if (b < nb) {
-            cpre[b] = ex;
-            ex += nch[q];
+        for (int q = 0; q < 4; ++q) {
+            const int b = threadIdx.x * 4 + q;
+            if (b < nb) {
+                cpre[b] = ex;
+                ex += nch[q];
+            }
+        }
+        if (threadIdx.x == 0) {
+            cpre[nb] = total;
+            s_chunks = total;
         }
     }
-    if (threadIdx.x == 0)
-        cpre[nb] = chunks;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     const Buckets bk{seg, cpre, cbase, crem, act};
+    const int chunks = s_chunks;
 
     if (threadIdx.x < LOADERS)
         embed_loader(p, c, bars, smem, srec, bk, chunks, rv);

@@ -77,6 +77,8 @@ def _load():
             lib.oracle_embed.argtypes = [
                 _i32p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
                 ctypes.POINTER(_u16p), ctypes.POINTER(_u16p), _i32p, _f32p, _f32p]
+            lib.oracle_silu_mul.restype = None
+            lib.oracle_silu_mul.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _f32p]
             _lib = lib
     return _lib
 
@@ -216,6 +218,25 @@ def embed(tokens: np.ndarray, E: np.ndarray, seq_slot: np.ndarray, adapters: Seq
     return y
 
 
+def silu_mul(y: np.ndarray, I: int) -> np.ndarray:
+    """act = silu(y[:, :I]) * y[:, I:2I] in fp32 (y: fp32 [M][2I] projection output)."""
+    y = np.ascontiguousarray(y, dtype=np.float32)
+    M = y.shape[0]
+    assert y.shape[1] >= 2 * I
+    act = np.empty((M, I), dtype=np.float32)
+    _load().oracle_silu_mul(_p(y, _f32p), M, I, y.shape[1], _p(act, _f32p))
+    return act
+
+
+def gate_up(x: np.ndarray, W: np.ndarray, seq_slot: np.ndarray, adapters: Sequence,
+            rows=None, scales: Optional[Sequence[float]] = None) -> np.ndarray:
+    """Gated MLP input: the fused [gate|up] projection (W [2I][K], adapters'
+    B [2I][r]) followed by silu(gate) * up, fp32 [rows][I]."""
+    I = W.shape[0] // 2
+    y = proj(x, W, seq_slot, adapters, rows=rows, scales=scales)
+    return silu_mul(y, I)
+
+
 def workload_embed(wl) -> np.ndarray:
     """Oracle output for a ``workloads.EmbedWorkload``."""
     return embed(wl.tokens, wl.E, wl.seq_slot, wl.adapters)
@@ -247,7 +268,7 @@ class _use_library:
         self.saved = _lib
         lib = ctypes.CDLL(self.path)
         for name in ("oracle_scale", "oracle_slot_sort", "oracle_proj", "oracle_moe",
-                     "oracle_moe_slot_sort", "oracle_embed"):
+                     "oracle_moe_slot_sort", "oracle_embed", "oracle_silu_mul"):
             src = getattr(self.saved, name)
             dst = getattr(lib, name)
             dst.restype = src.restype

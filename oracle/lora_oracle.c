@@ -218,6 +218,27 @@ void oracle_embed(const int32_t *tokens, const uint16_t *E, int M, int vocab, in
  * the expert through expert_offsets).
  * rows/cols select outputs as in oracle_proj; y is [n_rows][n_cols].
  */
+/*
+ * Gated MLP input from a fused [gate|up] projection (frink `lora_attach.rs`,
+ * `parts_mut`: a fused ffn_up holds the gate rows first, then the up rows, and
+ * its adapter's B rows split the same way over one A). y is the projection's
+ * output, [M][2I] at row stride y_stride: columns [0, I) are the gate g,
+ * [I, 2I) the up u. act[i][n] = silu(g) * u with silu(g) = g / (1 + e^-g),
+ * in fp32.
+ */
+void oracle_silu_mul(const float *y, int M, int I, int64_t y_stride, float *act)
+{
+    for (int i = 0; i < M; i++) {
+        const float *gr = y + (size_t)i * y_stride;
+        const float *ur = gr + I;
+        for (int n = 0; n < I; n++) {
+            float g = gr[n];
+            float sg = g / (1.0f + expf(-g));
+            act[(size_t)i * I + n] = sg * ur[n];
+        }
+    }
+}
+
 void oracle_moe(const uint16_t *x, int64_t x_stride, const uint16_t *const *W, const int32_t *expert_offsets,
                 int E, int T, int K, int N, const int32_t *seq_slot, int L,
                 const uint16_t *const *A, const uint16_t *const *B, const int32_t *rank,

@@ -300,6 +300,56 @@ def check_embed_no_delta_rows_are_the_embedding():
             assert np.array_equal(y[i].view(np.uint32), Ef[int(toks[i])].view(np.uint32)), i
 
 
+# --------------------------------------------------------------------------
+# Gated MLP input: fused [gate|up] projection, then silu(gate) * up
+# (frink lora_attach.rs, parts_mut: the fused ffn_up is gate rows then up rows)
+# --------------------------------------------------------------------------
+
+
+def small_gate_up(seed=31, M=9, K=40, I=24, L=3, R=16):
+    """A fused [gate|up] workload: W [2I][K], adapters with B [2I][r]."""
+    return workloads.random_small(seed, M=M, K=K, N=2 * I, L=L, R=R)
+
+
+def check_silu_mul_closed_forms():
+    """silu(g) * u against g * (1 + tanh(g/2)) / 2 * u in fp64 (the logistic
+    function written through tanh), and the exact points silu(0) = 0, u = 0."""
+    rng = np.random.default_rng(7)
+    I = 16
+    y = rng.normal(0.0, 3.0, size=(5, 2 * I)).astype(np.float32)
+    y[0, :I] = 0.0
+    y[1, I:] = 0.0
+    y[2, :4] = [30.0, -30.0, 1e-3, -1e-3]
+    act = oracle.silu_mul(y, I)
+    g = y[:, :I].astype(np.float64)
+    u = y[:, I:].astype(np.float64)
+    ref = g * (1.0 + np.tanh(g / 2.0)) / 2.0 * u
+    assert np.all(act[0] == 0.0) and np.all(act[1] == 0.0)
+    err = np.abs(act.astype(np.float64) - ref)
+    assert np.all(err <= 1e-6 * (1.0 + np.abs(ref))), err.max()
+
+
+def check_gate_up_is_the_split_projections():
+    """The gate half of the fused projection is the projection through the gate
+    rows of W and of every B (one shared A), the up half likewise, byte for
+    byte; act is silu of the one times the other."""
+    wl = small_gate_up()
+    I = wl.N // 2
+    act = oracle.gate_up(wl.x, wl.W, wl.seq_slot, wl.adapters)
+    halves = []
+    for lo in (0, I):
+        ads = [None if a is None else Adapter(A=a.A, B=np.ascontiguousarray(a.B[lo:lo + I]), rank=a.rank,
+                                              alpha=a.alpha, use_rslora=a.use_rslora,
+                                              adapter_scale=a.adapter_scale) for a in wl.adapters]
+        halves.append(oracle.proj(wl.x, np.ascontiguousarray(wl.W[lo:lo + I]), wl.seq_slot, ads))
+    both = np.concatenate(halves, axis=1)
+    assert np.array_equal(act.view(np.uint32), oracle.silu_mul(both, I).view(np.uint32))
+    g, u = halves[0].astype(np.float64), halves[1].astype(np.float64)
+    ref = g * (1.0 + np.tanh(g / 2.0)) / 2.0 * u
+    with np.errstate(invalid="ignore", over="ignore"):
+        assert np.all(np.abs(act - ref) <= 1e-5 * (1.0 + np.abs(ref)))
+
+
 ALL_CHECKS = [
     check_scale_examples,
     check_hand_example,
@@ -315,4 +365,6 @@ ALL_CHECKS = [
     check_embed_brute_force,
     check_embed_row_gather_identity,
     check_embed_no_delta_rows_are_the_embedding,
+    check_silu_mul_closed_forms,
+    check_gate_up_is_the_split_projections,
 ]

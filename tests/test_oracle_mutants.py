@@ -41,6 +41,10 @@ MUTANTS = {
     "embed_drop_scale": ("v += scale[s] * dsum;", "v += dsum;"),
     "embed_A_transposed": ("widen(A[s][(size_t)r * n_embd + e]);",
                            "widen(A[s][(size_t)e * rank[s] + r]);"),
+    "silu_sign": ("float sg = g / (1.0f + expf(-g));", "float sg = g / (1.0f + expf(g));"),
+    "silu_halves_swapped": ("act[(size_t)i * I + n] = sg * ur[n];",
+                            "act[(size_t)i * I + n] = gr[n] / (1.0f + expf(-ur[n])) * gr[n];"),
+    "silu_without_up": ("act[(size_t)i * I + n] = sg * ur[n];", "act[(size_t)i * I + n] = sg;"),
     "h_uses_pool_row_of_next_slot": ("const uint16_t *arow = A[s] + (size_t)r * K;",
                                      "const uint16_t *arow = A[(s + 1) % L] ? A[(s + 1) % L] + (size_t)r * K : A[s] + (size_t)r * K;"),
 }

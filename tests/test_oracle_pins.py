@@ -87,3 +87,11 @@ def test_embed_is_the_row_gather_of_the_flipped_projection():
 
 def test_embed_no_delta_rows_and_out_of_range_tokens():
     P.check_embed_no_delta_rows_are_the_embedding()
+
+
+def test_silu_mul_closed_forms():
+    P.check_silu_mul_closed_forms()
+
+
+def test_gate_up_is_the_split_projections():
+    P.check_gate_up_is_the_split_projections()

@@ -289,6 +289,29 @@ lora_status lora_proj_apply_static_ws(const void *x, int64_t x_stride, const voi
                                       int N, const int32_t *seq_slot, const lora_route *rt,
                                       void *y, int64_t y_stride, lora_stream_t stream);
 
+/*
+ * Gated MLP input through a fused [gate|up] projection (frink
+ * `lora_attach.rs`, `parts_mut`: a fused ffn_up holds the gate rows first,
+ * then the up rows, and its adapter's B rows split the same way over one A):
+ *
+ *   g = (W x_i + s B (A x_i))[0 .. I),  u = (...)[I .. 2I),
+ *   act[i][n] = silu(g[n]) * u[n],  silu(g) = g / (1 + e^-g).
+ *
+ *   W      device [2I][K] bf16: gate rows, then up rows
+ *   rt     a projection route with n_out = 2I (each adapter's B is [2I][rank])
+ *   act    device, M rows of I bf16, row i at act + i*act_stride
+ *   ws     lora_gate_up_workspace_bytes(M, rt) bytes: the projection's
+ *          workspace followed by its [M][2I] bf16 output
+ * The projection is lora_proj_apply (every row rule and the status word
+ * included: lora_status_get(ws) reads it); the halves are rounded to bf16,
+ * then silu(g) * u is formed in fp32 and rounded once to bf16. Errors: those
+ * of lora_proj_apply, a route whose n_out is not 2I, act_stride < I.
+ */
+size_t lora_gate_up_workspace_bytes(int M, const lora_route *rt);
+lora_status lora_gate_up_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int I,
+                               const int32_t *seq_slot, const lora_route *rt, void *act,
+                               int64_t act_stride, void *ws, size_t ws_bytes, lora_stream_t stream);
+
 /* Largest expert count lora_moe_down_apply takes in one call. */
 #define LORA_MAX_EXPERTS 16
 

@@ -101,6 +101,8 @@ _SIGNATURES = {
     "lora_proj_apply_ex": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _i,
                                 _vp]),
     "lora_proj_apply_static_ws": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp]),
+    "lora_gate_up_workspace_bytes": (_sz, [_i, _rtp]),
+    "lora_gate_up_apply": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_moe_workspace_bytes": (_sz, [_i, _i, _rtp]),
     "lora_moe_down_apply": (_i, [_vp, _i64, ctypes.POINTER(_vp), _vp, _i, _i, _i, _i, _vp, _rtp,
                                  _vp, _i64, _vp, _sz, _vp]),
@@ -237,6 +239,17 @@ def lora_proj_apply_static_ws(x, x_stride: int, W, M: int, K: int, N: int, seq_s
     allocate device memory: the library's built-in scratch array is used."""
     _check(lib().lora_proj_apply_static_ws(_ptr(x), x_stride, _ptr(W), M, K, N, _ptr(seq_slot),
                                            ctypes.byref(rt), _ptr(y), y_stride, _stream(stream)))
+
+
+def lora_gate_up_workspace_bytes(M: int, rt: lora_route) -> int:
+    return int(lib().lora_gate_up_workspace_bytes(M, ctypes.byref(rt)))
+
+
+def lora_gate_up_apply(x, x_stride: int, W, M: int, K: int, I: int, seq_slot, rt: lora_route, act,
+                       act_stride: int, ws, ws_bytes: int, stream=None) -> None:
+    _check(lib().lora_gate_up_apply(_ptr(x), x_stride, _ptr(W), M, K, I, _ptr(seq_slot),
+                                    ctypes.byref(rt), _ptr(act), act_stride, _ptr(ws), ws_bytes,
+                                    _stream(stream)))
 
 
 def lora_moe_workspace_bytes(E: int, T: int, rts) -> int:

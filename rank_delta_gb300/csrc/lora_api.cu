@@ -670,6 +670,59 @@ lora_status lora_proj_apply_ex(const void *x, int64_t x_stride, const void *W, i
     return proj_apply(x, x_stride, W, M, K, N, seq_slot, rt, y, y_stride, ws, ws_bytes, path, stream);
 }
 
+size_t lora_gate_up_workspace_bytes(int M, const lora_route *rt)
+{
+    if (rt == nullptr || rt->magic != ROUTE_MAGIC || rt->kind != LORA_ROUTE_PROJ || M < 0 || rt->n_out % 2 != 0)
+        return 0;
+    // the projection's workspace, then its [M][2I] bf16 output
+    return align256(lora_proj_workspace_bytes(M, rt)) + align256((size_t)M * (size_t)rt->n_out * 2);
+}
+
+lora_status lora_gate_up_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int I,
+                               const int32_t *seq_slot, const lora_route *rt, void *act, int64_t act_stride,
+                               void *ws, size_t ws_bytes, lora_stream_t stream)
+{
+    const char *who = "lora_gate_up_apply";
+    lora_status s = check_route_kind(rt, LORA_ROUTE_PROJ, who);
+    if (s != LORA_OK)
+        return s;
+    if (M < 0)
+        return fail(LORA_ERR_SHAPE, "%s: M %d is negative", who, M);
+    if (I <= 0 || (int64_t)rt->n_out != 2 * (int64_t)I || K != rt->n_in)
+        return fail(LORA_ERR_SHAPE,
+                    "%s: a fused [gate|up] of I %d over K %d needs a route of [n_out 2I = %lld x n_in %d], "
+                    "the route is [n_out %d x n_in %d]",
+                    who, I, K, 2 * (long long)I, K, rt->n_out, rt->n_in);
+    if (M == 0)
+        return ok();
+    if (act == nullptr)
+        return fail(LORA_ERR_NULL, "%s: act is NULL", who);
+    if (act_stride < I)
+        return fail(LORA_ERR_SHAPE, "%s: act_stride %lld must be >= I %d", who, (long long)act_stride, I);
+    const size_t need = lora_gate_up_workspace_bytes(M, rt);
+    if (ws == nullptr)
+        return fail(LORA_ERR_NULL, "%s: workspace is NULL", who);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return fail(LORA_ERR_ALIGN, "%s: workspace must be 256-byte aligned", who);
+    if (ws_bytes < need)
+        return fail(LORA_ERR_WORKSPACE, "%s: workspace has %zu bytes, needs %zu (%d rows, 2I = %d)", who,
+                    ws_bytes, need, M, 2 * I);
+    DevInfo di;
+    if (!device_info(di))
+        return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
+    const size_t proj_ws = align256(lora_proj_workspace_bytes(M, rt));
+    uint16_t *gu = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + proj_ws);
+    s = proj_apply(x, x_stride, W, M, K, 2 * I, seq_slot, rt, gu, 2 * (int64_t)I, ws, proj_ws,
+                   LORA_PATH_AUTO, stream);
+    if (s != LORA_OK)
+        return s;
+    cudaError_t e = launch_silu_mul(gu, 2 * (int64_t)I, M, I, static_cast<uint16_t *>(act), act_stride,
+                                    di.num_sms, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, who);
+    return ok();
+}
+
 size_t lora_moe_workspace_bytes(int E, int T, const lora_route *rts)
 {
     if (rts == nullptr || E < 1 || E > MAX_E || T < 0 || rts[0].magic != ROUTE_MAGIC)

@@ -184,6 +184,10 @@ constexpr int EMBED_LOCAL_BUCKETS = 64;
 bool embed_local_fits(int M, int ft, int R, int L);
 cudaError_t launch_embed(const EmbedParams &p, int num_sms, cudaStream_t st);
 
+// act[i][n] = silu(y[i][n]) * y[i][I + n] (lora_act.cu).
+cudaError_t launch_silu_mul(const uint16_t *y, int64_t y_stride, int M, int I, uint16_t *act,
+                            int64_t act_stride, int num_sms, cudaStream_t st);
+
 // Record `msg` as the thread's last error and return `code` (lora_api.cu).
 lora_status api_fail(lora_status code, const char *msg);
 

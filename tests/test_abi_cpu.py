@@ -229,3 +229,24 @@ def test_embed_route_init_refusals_name_the_call():
     msg = expect(rd.LORA_ERR_WORKSPACE, rd.lora_embed_route_init, rt, 256, 100, 256, 1 << 20, 4, 8,
                  1000, 256)
     assert "[1000 x 256]" in msg
+
+
+def test_gate_up_argument_checks():
+    rt = fake_route(L=4, R=8, K=256, N=512)
+    need = rd.lora_gate_up_workspace_bytes(8, rt)
+    assert need >= rd.lora_proj_workspace_bytes(8, rt) + 8 * 512 * 2
+    assert rd.lora_gate_up_workspace_bytes(8, fake_route(N=511)) == 0
+
+    def call(**kw):
+        a = dict(dict(x=4096, x_stride=256, W=8192, M=8, K=256, I=256, seq_slot=4096, rt=rt, act=4096,
+                      act_stride=256, ws=1 << 20, ws_bytes=need), **kw)
+        return lambda: rd.lora_gate_up_apply(a["x"], a["x_stride"], a["W"], a["M"], a["K"], a["I"],
+                                             a["seq_slot"], a["rt"], a["act"], a["act_stride"], a["ws"],
+                                             a["ws_bytes"])
+
+    expect(rd.LORA_ERR_SHAPE, call(I=200), contains=("I 200", "n_out 512"))
+    expect(rd.LORA_ERR_NULL, call(act=0))
+    expect(rd.LORA_ERR_SHAPE, call(act_stride=100))
+    expect(rd.LORA_ERR_WORKSPACE, call(ws_bytes=need - 1))
+    expect(rd.LORA_ERR_UNSUPPORTED, call(rt=fake_route(K=256, N=512, kind=rd.LORA_ROUTE_EMBED)))
+    rd.lora_gate_up_apply(0, 256, 0, 0, 256, 256, 0, rt, 0, 256, 0, 0)  # M = 0: nothing

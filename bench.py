@@ -48,9 +48,14 @@ DESCRIBE = {
              "{8,16,32,64} pool R=64, alpha=2r, 10% rows slot -1",
     "embed_prefill": "token embedding gather: 4096 tokens of E[32000x4096] bf16, 16 adapters r in "
                      "{8,16,32,64} pool R=64, alpha=2r, 10% rows slot -1",
+    "gate_up": "gated MLP input: 8192 rows (8 seqs x 1024) x fused W[14336x4096] bf16 = gate 7168 | up 7168, "
+               "8 adapters r=64 rsLoRA alpha=16 (B rows split the same way), act = silu(gate) * up",
+    "gate_up_decode": "gated MLP input: 64 rows x fused W[4096x4096] bf16 = gate 2048 | up 2048, 16 adapters "
+                      "r in {8,16,32,64} pool R=64, alpha=2r, 10% rows slot -1, act = silu(gate) * up",
 }
 BOUND = {"tiny": "hbm", "decode": "hbm", "qkv": "hbm", "prefill": "tensor", "moe": "hbm",
-         "embed": "hbm", "embed_prefill": "hbm"}
+         "embed": "hbm", "embed_prefill": "hbm", "gate_up": "tensor", "gate_up_decode": "hbm"}
+GATE_UP = {"gate_up": "prefill", "gate_up_decode": "decode"}  # the projection workload each one reads
 EMBED_ROWS = {"embed": 64, "embed_prefill": 4096}
 # --small: the same kernels on fewer rows, for profiler captures only (never a bench line)
 SMALL = {"prefill": {"seq_len": 256}, "moe": {"tokens": 128}}
@@ -110,6 +115,13 @@ def embed_algorithmic(wl):
     for s in touched:
         byts += wl.adapters[s].rank * n * 2
     return float(byts), float(flops)
+
+
+def gate_up_algorithmic(wl):
+    """The fused projection's bytes and flops with act [M][I] written instead
+    of y [M][2I] (the halves are an intermediate)."""
+    byts, flops = proj_algorithmic(wl)
+    return byts - wl.M * wl.N * 2 + wl.M * (wl.N // 2) * 2, flops
 
 
 def moe_algorithmic(wl):
@@ -193,24 +205,33 @@ class ClockSampler:
 # our arm
 # ----------------------------------------------------------------------------
 
-def source_sha():
+# the sources each timed kernel is compiled from (a recorded DRAM figure holds
+# while these are unchanged)
+KERNEL_SOURCES = {
+    "tc_kernel": ["lora_tc.cu", "shrink.cuh", "ptx.cuh", "vec.cuh", "lora_internal.cuh"],
+    "simt_kernel": ["lora_simt.cu", "shrink.cuh", "vec.cuh", "lora_internal.cuh"],
+    "embed_kernel": ["lora_embed.cu", "ptx.cuh", "lora_internal.cuh"],
+}
+
+
+def source_sha(kernel):
     h = hashlib.sha256()
     cdir = os.path.join(ROOT, "rank_delta_gb300", "csrc")
-    for f in sorted(os.listdir(cdir)):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(cdir, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(config, kernel):
-    """dram bytes per launch from a committed ncu capture, if the kernels are unchanged."""
+    """dram bytes per launch from a committed ncu capture, if the kernel's sources are unchanged."""
     p = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     ent = d.get(config)
-    if not ent or ent.get("source_sha") != source_sha() or ent.get("kernel") != kernel:
+    if not ent or ent.get("kernel") != kernel or ent.get("source_sha") != source_sha(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -296,6 +317,25 @@ class EmbedSet:
                             y.stride(0), self.ws, self.ws.numel(), stream)
 
 
+class GateUpSet(ProjSet):
+    """A projection buffer set whose output is act [M][I]."""
+
+    def __init__(self, wl, th, rd, torch):
+        super().__init__(wl, th, rd, torch)
+        self.I = wl.N // 2
+        self.y = torch.empty((wl.M, self.I), dtype=torch.bfloat16, device="cuda")
+        self.ws = th.workspace(rd.lora_gate_up_workspace_bytes(wl.M, self.route.rt))
+        self.bytes = (self.W.numel() * 2 + self.route.pool_bytes + self.x.numel() * 2 +
+                      self.y.numel() * 2 + self.ws.numel())
+
+    def step(self, wl, rd, stream, x=None, slots=None, y=None):
+        x = self.x if x is None else x
+        slots = self.slots if slots is None else slots
+        y = self.y if y is None else y
+        rd.lora_gate_up_apply(x, x.stride(0), self.W, wl.M, wl.K, self.I, slots, self.route.rt, y,
+                              y.stride(0), self.ws, self.ws.numel(), stream)
+
+
 def max_over_ranks(ms: float, world: int, device: str) -> float:
     """The slowest rank's time: every rank runs an independent replica, so the
     job ends when the last one does."""
@@ -323,6 +363,8 @@ TC_SHRINK_MIN_ROWS = 2048
 def launches_per_call(config, rows, kernel):
     if kernel == "embed_kernel":
         return LAUNCHES_EMBED
+    if config in GATE_UP: # the projection, then the activation kernel
+        return launches_per_call(GATE_UP[config], rows, kernel) + 1
     if kernel == "simt_kernel":
         return LAUNCHES_SIMT
     if config != "moe" and rows >= TC_SHRINK_MIN_ROWS:
@@ -334,6 +376,9 @@ def make_workload(config, small=False):
     import workloads
     if config in EMBED_ROWS:
         return workloads.embed(M=EMBED_ROWS[config])
+    if config in GATE_UP:
+        base = GATE_UP[config]
+        return workloads.make(base, **(SMALL.get(base, {}) if small else {}))
     return workloads.make(config, **(SMALL.get(config, {}) if small else {}))
 
 
@@ -354,11 +399,14 @@ def run_ours(args, rank, world, local_rank):
     is_moe = args.config == "moe"
     is_embed = args.config in EMBED_ROWS
     rows = wl.T if is_moe else wl.M
+    is_gate_up = args.config in GATE_UP
     if is_embed:
         algo_bytes, algo_flops = embed_algorithmic(wl)
+    elif is_gate_up:
+        algo_bytes, algo_flops = gate_up_algorithmic(wl)
     else:
         algo_bytes, algo_flops = moe_algorithmic(wl) if is_moe else proj_algorithmic(wl)
-    Set = MoeSet if is_moe else (EmbedSet if is_embed else ProjSet)
+    Set = MoeSet if is_moe else (EmbedSet if is_embed else (GateUpSet if is_gate_up else ProjSet))
     first = Set(wl, th, rd, torch)
     nsets = max(1, int(np.ceil(3 * L2_BYTES / first.bytes)))
     if is_embed:
@@ -473,7 +521,8 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
         "config": {
             "workload": DESCRIBE[args.config] + (" [--small profiling case, not the benchmark]"
-                                                 if args.small and args.config in SMALL else ""),
+                                                 if args.small and GATE_UP.get(args.config, args.config) in SMALL
+                                                 else ""),
             "rows_per_step": rows,
             "parallelism": f"replicas x{world} (rows shard, no collective)",
             "l2": f"rotating {nsets} buffer sets of {first.bytes / 1e6:.1f} MB "
@@ -512,6 +561,9 @@ def oracle_rate(wl, config, budget_s=12.0, cap_s=30.0):
     if config in EMBED_ROWS:
         def fn(w, rows):
             return oracle.embed(w.tokens[rows], w.E, w.seq_slot[rows], w.adapters)
+    elif config in GATE_UP:
+        def fn(w, rows):
+            return oracle.gate_up(w.x, w.W, w.seq_slot, w.adapters, rows=rows)
     else:
         fn = oracle.workload_moe if is_moe else oracle.workload_proj
     # calibrate on a few rows, then size the sample to ~budget_s
@@ -535,7 +587,8 @@ def oracle_rate(wl, config, budget_s=12.0, cap_s=30.0):
     threads = int(omp) if omp else cores
     return {"value": done / el, "unit": "rows/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} of {rows_total} rows (all "
-                      f"{wl.n_embd if config in EMBED_ROWS else wl.N} output columns each), "
+                      f"{wl.n_embd if config in EMBED_ROWS else (wl.N // 2 if config in GATE_UP else wl.N)} "
+                      f"output columns each), "
                       f"{done // n} pass(es), {el:.1f} s of fp32 C loops"}
 
 

@@ -77,6 +77,11 @@ def _load():
             lib.oracle_embed.argtypes = [
                 _i32p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
                 ctypes.POINTER(_u16p), ctypes.POINTER(_u16p), _i32p, _f32p, _f32p]
+            lib.oracle_moe_gather.restype = None
+            lib.oracle_moe_gather.argtypes = [
+                _u16p, ctypes.c_int64, ctypes.POINTER(_u16p), _i32p, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, ctypes.POINTER(_u16p),
+                ctypes.POINTER(_u16p), _i32p, _f32p, _f32p, ctypes.c_int, _f32p]
             lib.oracle_silu_mul.restype = None
             lib.oracle_silu_mul.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _f32p]
             _lib = lib
@@ -185,6 +190,40 @@ def moe(x: np.ndarray, W: List[np.ndarray], expert_offsets: np.ndarray, seq_slot
     return y
 
 
+def moe_gather(x: np.ndarray, W: List[np.ndarray], indices: np.ndarray, seq_slot: np.ndarray,
+               adapters: Sequence[Sequence], combine: Optional[np.ndarray] = None,
+               top_k: int = 1) -> np.ndarray:
+    """Decode-path MoE fold keyed by a per-slot-row expert index; with combine
+    weights, each token's top_k slot-rows summed with their weights."""
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    T, K = x.shape
+    E = len(W)
+    N = W[0].shape[0]
+    L = len(adapters[0])
+    Ws = [np.ascontiguousarray(w, dtype=np.uint16) for w in W]
+    Wp = (_u16p * E)(*[_p(w, _u16p) for w in Ws])
+    t = _Tables([ad for per_e in adapters for ad in per_e])
+    idx = np.ascontiguousarray(indices, dtype=np.int32)
+    ss = np.ascontiguousarray(seq_slot, dtype=np.int32)
+    if combine is None:
+        y = np.empty((T, N), dtype=np.float32)
+        cw = None
+    else:
+        assert T % top_k == 0
+        y = np.empty((T // top_k, N), dtype=np.float32)
+        cw = np.ascontiguousarray(combine, dtype=np.float32)
+    _load().oracle_moe_gather(_p(x, _u16p), K, Wp, _p(idx, _i32p), E, T, K, N, _p(ss, _i32p), L,
+                              t.A, t.B, _p(t.rank, _i32p), _p(t.scale, _f32p),
+                              _p(cw, _f32p) if cw is not None else None, int(top_k), _p(y, _f32p))
+    return y
+
+
+def workload_moe_gather(wl, with_combine: bool = True) -> np.ndarray:
+    """Oracle output for a ``workloads.MoeGatherWorkload``."""
+    return moe_gather(wl.x, wl.W, wl.indices, wl.seq_slot, wl.adapters,
+                      combine=wl.combine if with_combine else None, top_k=wl.top_k)
+
+
 def moe_slot_sort(expert_offsets: np.ndarray, seq_slot: np.ndarray, max_loras: int):
     """Stable grouping of slot-rows by (expert, slot) -> (perm, seg_off [E*(L+1)+1])."""
     off = np.ascontiguousarray(expert_offsets, dtype=np.int32)
@@ -268,7 +307,7 @@ class _use_library:
         self.saved = _lib
         lib = ctypes.CDLL(self.path)
         for name in ("oracle_scale", "oracle_slot_sort", "oracle_proj", "oracle_moe",
-                     "oracle_moe_slot_sort", "oracle_embed", "oracle_silu_mul"):
+                     "oracle_moe_slot_sort", "oracle_embed", "oracle_silu_mul", "oracle_moe_gather"):
             src = getattr(self.saved, name)
             dst = getattr(lib, name)
             dst.restype = src.restype

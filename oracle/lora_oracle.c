@@ -268,6 +268,50 @@ void oracle_moe(const uint16_t *x, int64_t x_stride, const uint16_t *const *W, c
     }
 }
 
+/*
+ * Decode-path MoE fold keyed on the expert through a per-slot-row index
+ * (spark_model `lora_delta.rs`, `LoraKernels`, moe_gather: the unsorted,
+ * slot-major analogue of the expert_offsets fold). Slot-row j = token
+ * j / top_k, choice j % top_k; its expert is indices[j]. Slot-row value:
+ *
+ *   v_j = W_e x_j + s B_{e,s} (A_{e,s} x_j),  e = indices[j], s = seq_slot[j]
+ *
+ * (zero when e is outside [0, E)). Without combine weights y[j] = v_j; with
+ * them y[t] = sum_{i < top_k} combine[t*top_k + i] * v_{t*top_k + i}, the
+ * weighted sum of a token's expert outputs, accumulated in choice order, fp32.
+ * Adapters are indexed e*L + s like oracle_moe.
+ */
+void oracle_moe_gather(const uint16_t *x, int64_t x_stride, const uint16_t *const *W, const int32_t *indices,
+                       int E, int T, int K, int N, const int32_t *seq_slot, int L,
+                       const uint16_t *const *A, const uint16_t *const *B, const int32_t *rank,
+                       const float *scale, const float *combine, int top_k, float *y)
+{
+    float *v = (float *)malloc(sizeof(float) * (size_t)N);
+    for (int j = 0; j < T; j++) {
+        int e = indices[j];
+        if (e < 0 || e >= E) {
+            for (int n = 0; n < N; n++)
+                v[n] = 0.0f;
+        } else {
+            int32_t one = j;
+            oracle_proj(x, x_stride, W[e], T, K, N, seq_slot, L, A + (size_t)e * L, B + (size_t)e * L,
+                        rank + (size_t)e * L, scale + (size_t)e * L, &one, 1, NULL, N, v);
+        }
+        if (combine == NULL) {
+            memcpy(y + (size_t)j * N, v, sizeof(float) * (size_t)N);
+        } else {
+            float *yt = y + (size_t)(j / top_k) * N;
+            if (j % top_k == 0)
+                for (int n = 0; n < N; n++)
+                    yt[n] = 0.0f;
+            float w = combine[j];
+            for (int n = 0; n < N; n++)
+                yt[n] += w * v[n];
+        }
+    }
+    free(v);
+}
+
 /* Stable grouping of MoE slot-rows by (expert, slot): for expert e, bucket
  * e*(L+1) holds the segment's rows with no valid slot, bucket e*(L+1)+1+s the
  * rows of slot s. seg_off has E*(L+1)+1 entries. */

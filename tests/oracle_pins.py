@@ -350,6 +350,56 @@ def check_gate_up_is_the_split_projections():
         assert np.all(np.abs(act - ref) <= 1e-5 * (1.0 + np.abs(ref)))
 
 
+# --------------------------------------------------------------------------
+# Decode-path MoE fold keyed by per-slot-row expert indices, with combine
+# weights (spark_model lora_delta.rs, LoraKernels moe_gather)
+# --------------------------------------------------------------------------
+
+
+def small_moe_gather(seed=51, tokens=5, E=3, top_k=2, K=24, N=16):
+    return workloads.moe_gather(seed=seed, tokens=tokens, E=E, top_k=top_k, K=K, N=N, n_adapters=3, rank=4)
+
+
+def check_moe_gather_brute_force(tol=1e-4):
+    """y[t] = sum_i w_ti (W_e + s B A) x_ti in fp64 with the delta matrix
+    materialised; an index outside [0, E) contributes nothing."""
+    wl = small_moe_gather()
+    wl.indices[3] = wl.E  # out of range: that slot-row adds nothing
+    y = oracle.workload_moe_gather(wl)
+    x = _f64(wl.x)
+    for t in range(wl.T // wl.top_k):
+        ref = np.zeros(wl.N)
+        for i in range(wl.top_k):
+            j = t * wl.top_k + i
+            e, s = int(wl.indices[j]), int(wl.seq_slot[j])
+            if not 0 <= e < wl.E:
+                continue
+            Weff = _f64(wl.W[e])
+            if 0 <= s < wl.max_loras:
+                ad = wl.adapters[e][s]
+                sc = oracle.scale(ad.alpha, ad.rank, ad.use_rslora, ad.adapter_scale)
+                Weff = Weff + np.float64(sc) * (_f64(ad.B) @ _f64(ad.A))
+            ref += np.float64(wl.combine[j]) * (Weff @ x[j])
+        assert np.abs(y[t] - ref).max() <= tol * (1.0 + np.abs(ref).max()), t
+
+
+def check_moe_gather_is_the_grouped_fold():
+    """Without combine weights the slot-rows equal the grouped (expert_offsets)
+    fold over the same rows sorted stably by expert, byte for byte; with
+    one-hot weights a token's row is its chosen slot-row exactly."""
+    wl = small_moe_gather(seed=52, tokens=7)
+    rows = oracle.workload_moe_gather(wl, with_combine=False)
+    order = np.argsort(wl.indices, kind="stable").astype(np.int32)
+    offs = np.zeros(wl.E + 1, dtype=np.int32)
+    offs[1:] = np.cumsum(np.bincount(wl.indices, minlength=wl.E))
+    grouped = oracle.moe(wl.x[order], wl.W, offs, wl.seq_slot[order], wl.adapters)
+    assert np.array_equal(rows[order].view(np.uint32), grouped.view(np.uint32))
+    onehot = np.zeros_like(wl.combine)
+    onehot[1::wl.top_k] = 1.0  # every token's second choice
+    y = oracle.moe_gather(wl.x, wl.W, wl.indices, wl.seq_slot, wl.adapters, combine=onehot, top_k=wl.top_k)
+    assert np.array_equal(y.view(np.uint32), (rows[1::wl.top_k] + 0.0).view(np.uint32))
+
+
 ALL_CHECKS = [
     check_scale_examples,
     check_hand_example,
@@ -367,4 +417,6 @@ ALL_CHECKS = [
     check_embed_no_delta_rows_are_the_embedding,
     check_silu_mul_closed_forms,
     check_gate_up_is_the_split_projections,
+    check_moe_gather_brute_force,
+    check_moe_gather_is_the_grouped_fold,
 ]

@@ -45,6 +45,10 @@ MUTANTS = {
     "silu_halves_swapped": ("act[(size_t)i * I + n] = sg * ur[n];",
                             "act[(size_t)i * I + n] = gr[n] / (1.0f + expf(-ur[n])) * gr[n];"),
     "silu_without_up": ("act[(size_t)i * I + n] = sg * ur[n];", "act[(size_t)i * I + n] = sg;"),
+    "gather_weight_of_the_token": ("float w = combine[j];", "float w = combine[j / top_k];"),
+    "gather_expert_ignored": ("int e = indices[j];", "int e = indices[j] >= 0 ? 0 : -1;"),
+    "gather_no_reset_per_token": ("if (j % top_k == 0)\n                for (int n = 0; n < N; n++)\n                    yt[n] = 0.0f;",
+                                  "if (j == 0)\n                for (int n = 0; n < N; n++)\n                    yt[n] = 0.0f;"),
     "h_uses_pool_row_of_next_slot": ("const uint16_t *arow = A[s] + (size_t)r * K;",
                                      "const uint16_t *arow = A[(s + 1) % L] ? A[(s + 1) % L] + (size_t)r * K : A[s] + (size_t)r * K;"),
 }

@@ -95,3 +95,11 @@ def test_silu_mul_closed_forms():
 
 def test_gate_up_is_the_split_projections():
     P.check_gate_up_is_the_split_projections()
+
+
+def test_moe_gather_brute_force_fp64():
+    P.check_moe_gather_brute_force()
+
+
+def test_moe_gather_is_the_grouped_fold():
+    P.check_moe_gather_is_the_grouped_fold()

@@ -117,6 +117,27 @@ class MoeWorkload:
 
 
 @dataclass
+class MoeGatherWorkload:
+    """Decode-path MoE fold: slot-rows in token order, expert per slot-row."""
+    name: str
+    seed: int
+    E: int
+    T: int                      # slot-rows = tokens x top_k, token-major
+    K: int
+    N: int
+    max_loras: int
+    max_rank: int
+    top_k: int
+    W: List[np.ndarray]         # E x [N][K] bf16 bits
+    x: np.ndarray               # [T][K] bf16 bits, slot-row j = token j // top_k
+    indices: np.ndarray         # [T] int32 expert of each slot-row
+    seq_slot: np.ndarray        # [T] int32 (a token's slot on all its rows)
+    combine: np.ndarray         # [T] float32 combine weight of each slot-row
+    adapters: List[List[Optional[Adapter]]]  # [E][max_loras]
+    note: str = ""
+
+
+@dataclass
 class EmbedWorkload:
     """Token-embedding gather through an adapted matrix E + s B A (rows = vocab)."""
     name: str
@@ -299,6 +320,40 @@ def moe(seed: int = 4, tokens: int = 512, E: int = 8, top_k: int = 2,
                        token_of_row=token_of_row,
                        note="W_e~N(0,1/14336) x~N(0,1) per slot-row, top-2 of N(0,1) logits, "
                             "r=16 alpha=32 A~U(+-1/64) B~N(0,0.02), slot~U{-1,0..3} per token")
+
+
+def moe_gather(seed: int = 6, tokens: int = 64, E: int = 8, top_k: int = 2, K: int = 14336,
+               N: int = 4096, n_adapters: int = 4, rank: int = 16) -> MoeGatherWorkload:
+    """Decode-path MoE down projection, slot-rows left in token order.
+
+    Routing as in ``moe``: logits [tokens][E] ~ N(0,1), a token's top_k
+    largest (ties to the lower id); slot-row t*top_k + i holds the token's
+    i-th choice. Combine weights: the softmax of the token's top_k logits (the
+    chosen experts' probabilities renormalised to sum 1), in fp32. Each
+    slot-row has its own input row ~ N(0,1); a token's slot (uniform over
+    {-1, 0..n_adapters-1}) is shared by its top_k slot-rows.
+
+    Draw order: per expert W_e; logits; token slots; x; per expert and
+    adapter (A, B).
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    W = [_normal_bf16(rng, (N, K), 1.0 / K) for _ in range(E)]
+    logits = rng.standard_normal((tokens, E), dtype=np.float32)
+    order = np.argsort(-logits, axis=1, kind="stable")[:, :top_k]
+    tok_slot = rng.integers(-1, n_adapters, size=tokens, dtype=np.int64).astype(np.int32)
+    T = tokens * top_k
+    indices = order.reshape(T).astype(np.int32)
+    top = np.take_along_axis(logits, order, axis=1).astype(np.float64)
+    w = np.exp(top - top.max(axis=1, keepdims=True))
+    combine = (w / w.sum(axis=1, keepdims=True)).reshape(T).astype(np.float32)
+    seq_slot = np.repeat(tok_slot, top_k).astype(np.int32)
+    x = _normal_bf16(rng, (T, K), 1.0)
+    ads = [[_adapter(rng, K, N, rank, 1.0 / 64, 0.02, alpha=32.0) for _ in range(n_adapters)]
+           for _ in range(E)]
+    return MoeGatherWorkload("moe_gather", seed, E, T, K, N, n_adapters, rank, top_k, W, x, indices,
+                             seq_slot, combine, ads,
+                             note="W_e~N(0,1/14336) x~N(0,1) per slot-row, top-2 of N(0,1) logits in "
+                                  "token order, combine = softmax of the top-2, r=16 alpha=32")
 
 
 def random_small(seed: int, M: int, K: int, N: int, L: int, R: int,

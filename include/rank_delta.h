@@ -76,7 +76,8 @@ enum {
     LORA_FLAG_SLOT_RANGE = 1u << 0,   /* a seq_slot value >= max_loras was seen; those rows got no delta */
     LORA_FLAG_WAIT_TIMEOUT = 1u << 1, /* an in-kernel wait gave up; that call's output is not valid */
     LORA_FLAG_BAD_OFFSETS = 1u << 2,  /* expert_offsets not non-decreasing within [0, T]; rows outside skipped */
-    LORA_FLAG_TOKEN_RANGE = 1u << 3   /* lora_embed_apply: a token outside [0, vocab); its row is zero */
+    LORA_FLAG_TOKEN_RANGE = 1u << 3,  /* lora_embed_apply: a token outside [0, vocab); its row is zero */
+    LORA_FLAG_EXPERT_RANGE = 1u << 4  /* lora_moe_gather_apply: an expert index outside [0, E); that slot-row adds nothing */
 };
 
 /* What a route's pool holds (lora_route.kind). */
@@ -405,6 +406,43 @@ size_t lora_embed_workspace_bytes(int M, const lora_route *rt);
 lora_status lora_embed_apply(const int32_t *tokens, const void *E, int M, int vocab, int n_embd,
                              const int32_t *seq_slot, const lora_route *rt, void *y,
                              int64_t y_stride, void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
+ * ------------------------------------------------------------------------
+ * Decode-path MoE fold keyed on the expert through a per-slot-row index
+ * (spark_model `lora_delta.rs`, `LoraKernels`, moe_gather: the unsorted,
+ * slot-major analogue of lora_moe_down_apply), with the top-k combine.
+ * ------------------------------------------------------------------------
+ *
+ * Slot-row j (token j / top_k, choice j % top_k) has input x_j and expert
+ * e = indices[j]:
+ *   v_j = W_e x_j + s B_{e,s} (A_{e,s} x_j),  s = seq_slot[j]
+ * (zero when e is outside [0, E): LORA_FLAG_EXPERT_RANGE is set).
+ *   combine == NULL   y[j, :] = v_j for j in [0, T), byte for byte what
+ *                     lora_moe_down_apply gives for that row
+ *   combine != NULL   y[t, :] = sum_i combine[t*top_k + i] * v_{t*top_k + i}
+ *                     for t in [0, T / top_k): fp32 sum of the slot-rows (each
+ *                     rounded to bf16), rounded once
+ *   x          device, T rows of K bf16 in token order, stride x_stride
+ *   W_e, rts   as lora_moe_down_apply (host arrays of E device pointers / routes)
+ *   indices    device [T] int32
+ *   seq_slot   device [T] int32
+ *   combine    device [T] f32 or NULL; top_k >= 1 and T a multiple of top_k
+ *              when given
+ *   y          device, stride y_stride >= N
+ *   ws         lora_moe_gather_workspace_bytes(E, T, rts) bytes
+ * The rows are sorted by expert on the device (stable), copied into expert
+ * order, folded by the grouped path, and combined. T <= LORA_GATHER_MAX_ROWS.
+ * Same conventions and errors as lora_moe_down_apply, plus: T above the
+ * limit, a top_k that does not divide T.
+ */
+#define LORA_GATHER_MAX_ROWS 8192
+size_t lora_moe_gather_workspace_bytes(int E, int T, const lora_route *rts);
+lora_status lora_moe_gather_apply(const void *x, int64_t x_stride, const void *const *W_e,
+                                  const int32_t *indices, int E, int T, int K, int N,
+                                  const int32_t *seq_slot, const lora_route *rts, const float *combine,
+                                  int top_k, void *y, int64_t y_stride, void *ws, size_t ws_bytes,
+                                  lora_stream_t stream);
 
 /* Read the status word (LORA_FLAG_* bits) of the most recent call that used
  * workspace `ws`. Synchronises `stream` (diagnostic, not a hot-path call). */

@@ -31,6 +31,8 @@ LORA_FLAG_SLOT_RANGE = 1 << 0
 LORA_FLAG_WAIT_TIMEOUT = 1 << 1
 LORA_FLAG_BAD_OFFSETS = 1 << 2
 LORA_FLAG_TOKEN_RANGE = 1 << 3
+LORA_FLAG_EXPERT_RANGE = 1 << 4
+LORA_GATHER_MAX_ROWS = 8192
 
 LORA_ROUTE_PROJ = 0
 LORA_ROUTE_EMBED = 1
@@ -104,6 +106,9 @@ _SIGNATURES = {
     "lora_gate_up_workspace_bytes": (_sz, [_i, _rtp]),
     "lora_gate_up_apply": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_moe_workspace_bytes": (_sz, [_i, _i, _rtp]),
+    "lora_moe_gather_workspace_bytes": (_sz, [_i, _i, _rtp]),
+    "lora_moe_gather_apply": (_i, [_vp, _i64, ctypes.POINTER(_vp), _vp, _i, _i, _i, _i, _vp, _rtp,
+                                   _vp, _i, _vp, _i64, _vp, _sz, _vp]),
     "lora_moe_down_apply": (_i, [_vp, _i64, ctypes.POINTER(_vp), _vp, _i, _i, _i, _i, _vp, _rtp,
                                  _vp, _i64, _vp, _sz, _vp]),
     "lora_embed_route_init": (_i, [_rtp, _vp, _sz, _vp, _sz, _i, _i, _i, _i, _vp]),
@@ -292,6 +297,20 @@ def lora_embed_apply(tokens, E, M: int, vocab: int, n_embd: int, seq_slot, rt: l
     _check(lib().lora_embed_apply(_ptr(tokens), _ptr(E), M, vocab, n_embd, _ptr(seq_slot),
                                   ctypes.byref(rt), _ptr(y), y_stride, _ptr(ws), ws_bytes,
                                   _stream(stream)))
+
+
+def lora_moe_gather_workspace_bytes(E: int, T: int, rts) -> int:
+    arr = (lora_route * E)(*rts)
+    return int(lib().lora_moe_gather_workspace_bytes(E, T, arr))
+
+
+def lora_moe_gather_apply(x, x_stride: int, W_e, indices, E: int, T: int, K: int, N: int, seq_slot, rts,
+                          combine, top_k: int, y, y_stride: int, ws, ws_bytes: int, stream=None) -> None:
+    wp = (_vp * E)(*[_ptr(w) for w in W_e])
+    arr = (lora_route * E)(*rts)
+    _check(lib().lora_moe_gather_apply(_ptr(x), x_stride, wp, _ptr(indices), E, T, K, N, _ptr(seq_slot), arr,
+                                       _ptr(combine), top_k, _ptr(y), y_stride, _ptr(ws), ws_bytes,
+                                       _stream(stream)))
 
 
 def lora_status_get(ws, stream=None) -> int:

@@ -876,6 +876,119 @@ lora_status lora_embed_apply(const int32_t *tokens, const void *E, int M, int vo
     return ok();
 }
 
+namespace {
+
+struct GatherWs {
+    size_t moe, x_sorted, y_sorted, perm, inv, slots, offsets, total;
+};
+
+GatherWs gather_ws(int E, int T, const lora_route *rts)
+{
+    GatherWs l;
+    const int K = rts[0].n_in, N = rts[0].n_out;
+    size_t o = align256(lora_moe_workspace_bytes(E, T, rts));
+    l.moe = o;
+    l.x_sorted = o; o = align256(o + (size_t)T * K * 2);
+    l.y_sorted = o; o = align256(o + (size_t)T * N * 2);
+    l.perm = o;     o = align256(o + (size_t)T * 4);
+    l.inv = o;      o = align256(o + (size_t)T * 4);
+    l.slots = o;    o = align256(o + (size_t)T * 4);
+    l.offsets = o;  o = align256(o + (size_t)(E + 2) * 4);
+    l.total = o;
+    return l;
+}
+
+} // namespace
+
+size_t lora_moe_gather_workspace_bytes(int E, int T, const lora_route *rts)
+{
+    if (rts == nullptr || E < 1 || E > MAX_E || T < 0 || rts[0].magic != ROUTE_MAGIC ||
+        rts[0].kind != LORA_ROUTE_PROJ)
+        return 0;
+    return gather_ws(E, T, rts).total;
+}
+
+lora_status lora_moe_gather_apply(const void *x, int64_t x_stride, const void *const *W_e,
+                                  const int32_t *indices, int E, int T, int K, int N,
+                                  const int32_t *seq_slot, const lora_route *rts, const float *combine,
+                                  int top_k, void *y, int64_t y_stride, void *ws, size_t ws_bytes,
+                                  lora_stream_t stream)
+{
+    const char *who = "lora_moe_gather_apply";
+    if (E < 1 || E > MAX_E)
+        return fail(LORA_ERR_UNSUPPORTED, "%s: E %d must be in [1, %d]", who, E, MAX_E);
+    if (rts == nullptr || W_e == nullptr)
+        return fail(LORA_ERR_NULL, "%s: rts and W_e must be non-NULL", who);
+    for (int q = 0; q < E; ++q) {
+        lora_status s = check_route_kind(&rts[q], LORA_ROUTE_PROJ, who);
+        if (s != LORA_OK)
+            return s;
+        if (rts[q].n_in != K || rts[q].n_out != N)
+            return fail(LORA_ERR_SHAPE, "%s: route of expert %d is [n_out %d x n_in %d]; expected [%d x %d]",
+                        who, q, rts[q].n_out, rts[q].n_in, N, K);
+    }
+    if (T < 0)
+        return fail(LORA_ERR_SHAPE, "%s: T %d is negative", who, T);
+    if (T > LORA_GATHER_MAX_ROWS)
+        return fail(LORA_ERR_UNSUPPORTED, "%s: T %d exceeds %d slot-rows (group the rows by expert and use "
+                    "lora_moe_down_apply)", who, T, LORA_GATHER_MAX_ROWS);
+    if (combine != nullptr && (top_k < 1 || T % top_k != 0))
+        return fail(LORA_ERR_SHAPE, "%s: with combine weights top_k %d must be >= 1 and divide T %d", who,
+                    top_k, T);
+    if (T == 0)
+        return ok();
+    if (indices == nullptr)
+        return fail(LORA_ERR_NULL, "%s: indices is NULL", who);
+    lora_status s = check_io(who, x, x_stride, T, K, N, seq_slot, y, y_stride);
+    if (s != LORA_OK)
+        return s;
+    const GatherWs l = gather_ws(E, T, rts);
+    if (ws == nullptr)
+        return fail(LORA_ERR_NULL, "%s: workspace is NULL", who);
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+        return fail(LORA_ERR_ALIGN, "%s: workspace must be 256-byte aligned", who);
+    if (ws_bytes < l.total)
+        return fail(LORA_ERR_WORKSPACE, "%s: workspace has %zu bytes, needs %zu (%d slot-rows, %d experts)",
+                    who, ws_bytes, l.total, T, E);
+    DevInfo di;
+    if (!device_info(di))
+        return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    GatherParams g;
+    memset(&g, 0, sizeof g);
+    g.x = static_cast<const uint16_t *>(x);
+    g.x_stride = x_stride;
+    g.indices = indices;
+    g.seq_slot = seq_slot;
+    g.E = E;
+    g.T = T;
+    g.K = K;
+    g.N = N;
+    g.x_sorted = reinterpret_cast<uint16_t *>(b + l.x_sorted);
+    g.perm = reinterpret_cast<int32_t *>(b + l.perm);
+    g.inv = reinterpret_cast<int32_t *>(b + l.inv);
+    g.slots_sorted = reinterpret_cast<int32_t *>(b + l.slots);
+    g.offsets = reinterpret_cast<int32_t *>(b + l.offsets);
+    g.y_sorted = reinterpret_cast<const uint16_t *>(b + l.y_sorted);
+    g.combine = combine;
+    g.top_k = combine ? top_k : 1;
+    g.y = static_cast<uint16_t *>(y);
+    g.y_stride = y_stride;
+    g.status = static_cast<uint32_t *>(ws); // the grouped fold's status word
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_gather_sort(g, di.num_sms, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, who);
+    s = lora_moe_down_apply(g.x_sorted, K, W_e, g.offsets, E, T, K, N, g.slots_sorted, rts, b + l.y_sorted, N,
+                            ws, l.moe, stream);
+    if (s != LORA_OK)
+        return s;
+    e = launch_gather_combine(g, di.num_sms, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, who);
+    return ok();
+}
+
 lora_status lora_status_get(const void *ws, uint32_t *flags, lora_stream_t stream)
 {
     if (ws == nullptr || flags == nullptr)

@@ -184,6 +184,29 @@ constexpr int EMBED_LOCAL_BUCKETS = 64;
 bool embed_local_fits(int M, int ft, int R, int L);
 cudaError_t launch_embed(const EmbedParams &p, int num_sms, cudaStream_t st);
 
+// Decode-path MoE fold with per-slot-row expert indices (lora_gather.cu).
+struct GatherParams {
+    const uint16_t *x;
+    int64_t x_stride;
+    const int32_t *indices;  // [T] expert of each slot-row
+    const int32_t *seq_slot; // [T]
+    int E, T, K, N;
+    uint16_t *x_sorted;      // [T][K] rows in expert order (workspace)
+    int32_t *perm;           // [T] sorted position -> slot-row
+    int32_t *inv;            // [T] slot-row -> sorted position
+    int32_t *slots_sorted;   // [T]
+    int32_t *offsets;        // [E+2] expert starts in the sorted order; [E] = rows with an expert
+    const uint16_t *y_sorted; // [T][N] the grouped fold's output (workspace)
+    const float *combine;    // [T] weights, or nullptr
+    int top_k;
+    uint16_t *y;
+    int64_t y_stride;
+    uint32_t *status;
+};
+size_t gather_sort_smem(int T, int E);
+cudaError_t launch_gather_sort(const GatherParams &p, int num_sms, cudaStream_t st);
+cudaError_t launch_gather_combine(const GatherParams &p, int num_sms, cudaStream_t st);
+
 // act[i][n] = silu(y[i][n]) * y[i][I + n] (lora_act.cu).
 cudaError_t launch_silu_mul(const uint16_t *y, int64_t y_stride, int M, int I, uint16_t *act,
                             int64_t act_stride, int num_sms, cudaStream_t st);

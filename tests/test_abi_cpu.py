@@ -250,3 +250,24 @@ def test_gate_up_argument_checks():
     expect(rd.LORA_ERR_WORKSPACE, call(ws_bytes=need - 1))
     expect(rd.LORA_ERR_UNSUPPORTED, call(rt=fake_route(K=256, N=512, kind=rd.LORA_ROUTE_EMBED)))
     rd.lora_gate_up_apply(0, 256, 0, 0, 256, 256, 0, rt, 0, 256, 0, 0)  # M = 0: nothing
+
+
+def test_moe_gather_argument_checks():
+    rts = [fake_route(L=4, R=16, K=512, N=256) for _ in range(3)]
+    need = rd.lora_moe_gather_workspace_bytes(3, 100, rts)
+    assert need >= rd.lora_moe_workspace_bytes(3, 100, rts) + 100 * (512 + 256) * 2
+    args = dict(x=4096, x_stride=512, W=[8192] * 3, idx=4096, E=3, T=100, K=512, N=256, slots=4096, rts=rts,
+                comb=4096, top_k=2, y=4096, y_stride=256, ws=1 << 20, wsb=need)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lambda: rd.lora_moe_gather_apply(a["x"], a["x_stride"], a["W"], a["idx"], a["E"], a["T"], a["K"],
+                                                a["N"], a["slots"], a["rts"], a["comb"], a["top_k"], a["y"],
+                                                a["y_stride"], a["ws"], a["wsb"])
+
+    expect(rd.LORA_ERR_SHAPE, call(top_k=3), contains=("top_k 3", "T 100"))
+    expect(rd.LORA_ERR_UNSUPPORTED, call(T=rd.LORA_GATHER_MAX_ROWS + 2), contains=("8192",))
+    expect(rd.LORA_ERR_NULL, call(idx=0))
+    expect(rd.LORA_ERR_WORKSPACE, call(wsb=need - 1))
+    expect(rd.LORA_ERR_SHAPE, call(K=256), contains=("expert 0",))
+    expect(rd.LORA_ERR_UNSUPPORTED, call(E=17))

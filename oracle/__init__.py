@@ -82,6 +82,11 @@ def _load():
                 _u16p, ctypes.c_int64, ctypes.POINTER(_u16p), _i32p, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int, ctypes.POINTER(_u16p),
                 ctypes.POINTER(_u16p), _i32p, _f32p, _f32p, ctypes.c_int, _f32p]
+            lib.oracle_proj_stack.restype = None
+            lib.oracle_proj_stack.argtypes = [
+                _u16p, ctypes.c_int64, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                _i32p, ctypes.c_int, _i32p, ctypes.POINTER(_u16p), ctypes.POINTER(_u16p), _i32p,
+                _f32p, _i32p, ctypes.c_int, _i32p, ctypes.c_int, _f32p]
             lib.oracle_silu_mul.restype = None
             lib.oracle_silu_mul.argtypes = [_f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int64, _f32p]
             _lib = lib
@@ -163,6 +168,38 @@ def proj(x: np.ndarray, W: np.ndarray, seq_slot: np.ndarray, adapters: Sequence,
                         t.A, t.B, _p(t.rank, _i32p), _p(t.scale, _f32p),
                         _p(r, _i32p) if r is not None else None, nr,
                         _p(c, _i32p) if c is not None else None, nc, _p(y, _f32p))
+    return y
+
+
+def proj_stack(x: np.ndarray, W: np.ndarray, seq_slot: np.ndarray, stacks: Sequence,
+               rows=None, cols=None) -> np.ndarray:
+    """y = W x + sum_m s_m B_m (A_m x) per row over the members of the row's
+    slot, in order, fp32 (ferrox ``LoraStack::add_to``).
+
+    ``stacks[s]`` is a list of ``workloads.Adapter`` (empty or None: no
+    members); each member's scale is :func:`scale` of its own alpha, rank,
+    rule and adapter scale.
+    """
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    ss = np.ascontiguousarray(seq_slot, dtype=np.int32)
+    M, K = x.shape
+    N = W.shape[0]
+    assert W.shape[1] == K and ss.shape[0] == M
+    L = len(stacks)
+    members = []
+    off = np.zeros(L + 1, dtype=np.int32)
+    for s_, st in enumerate(stacks):
+        members += list(st or [])
+        off[s_ + 1] = len(members)
+    t = _Tables(members)
+    r, nr = _idx(rows, M)
+    c, nc = _idx(cols, N)
+    y = np.empty((nr, nc), dtype=np.float32)
+    _load().oracle_proj_stack(_p(x, _u16p), K, _p(W, _u16p), M, K, N, _p(ss, _i32p), L,
+                              _p(off, _i32p), t.A, t.B, _p(t.rank, _i32p), _p(t.scale, _f32p),
+                              _p(r, _i32p) if r is not None else None, nr,
+                              _p(c, _i32p) if c is not None else None, nc, _p(y, _f32p))
     return y
 
 
@@ -307,7 +344,8 @@ class _use_library:
         self.saved = _lib
         lib = ctypes.CDLL(self.path)
         for name in ("oracle_scale", "oracle_slot_sort", "oracle_proj", "oracle_moe",
-                     "oracle_moe_slot_sort", "oracle_embed", "oracle_silu_mul", "oracle_moe_gather"):
+                     "oracle_moe_slot_sort", "oracle_embed", "oracle_silu_mul", "oracle_moe_gather",
+                     "oracle_proj_stack"):
             src = getattr(self.saved, name)
             dst = getattr(lib, name)
             dst.restype = src.restype

@@ -170,6 +170,88 @@ void oracle_proj(const uint16_t *x, int64_t x_stride, const uint16_t *W, int M, 
 }
 
 /*
+ * Several adapters on one base matrix (ferrox-core `weight_matrix/lora.rs`,
+ * `LoraStack`: every adapter attached to a matrix is one term of the sum,
+ * applied in order by `LoraStack::add_to`):
+ *
+ *   y[i][n] = sum_k W[n][k] x[i][k] + sum_m s_m * sum_r B_m[n][r] * (A_m x_i)[r]
+ *
+ * where m runs over the members of row i's slot, member_off[s] ..
+ * member_off[s+1]-1, in order. A member whose scale is 0 is skipped before
+ * any arithmetic (the `add_to` early return), so a stack whose every scale is
+ * 0 -- or a slot with no members, or a row whose slot is negative or >= L --
+ * leaves the base product untouched, byte for byte.
+ *   A[m] [rank[m]][K], B[m] [N][rank[m]] bf16, scale[m] the member's
+ *   effective scale (oracle_scale); rows / cols / y as in oracle_proj.
+ * Each term is accumulated into the running fp32 sum in member order, as
+ * `add_to` adds each delta into `out` in turn.
+ */
+void oracle_proj_stack(const uint16_t *x, int64_t x_stride, const uint16_t *W, int M, int K, int N,
+                       const int32_t *seq_slot, int L, const int32_t *member_off,
+                       const uint16_t *const *A, const uint16_t *const *B, const int32_t *rank,
+                       const float *scale, const int32_t *rows, int n_rows, const int32_t *cols,
+                       int n_cols, float *y)
+{
+    if (rows == NULL)
+        n_rows = M;
+    if (cols == NULL)
+        n_cols = N;
+    if (n_rows <= 0 || n_cols <= 0)
+        return;
+    int n_members = member_off[L];
+    int rmax = 1;
+    for (int m = 0; m < n_members; m++)
+        if (rank[m] > rmax)
+            rmax = rank[m];
+
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int j = 0; j < n_rows; j++) {
+        int i = rows ? rows[j] : j;
+        float *xq = (float *)malloc(sizeof(float) * (size_t)(K > 0 ? K : 1));
+        float *h = (float *)malloc(sizeof(float) * (size_t)rmax);
+        for (int k = 0; k < K; k++)
+            xq[k] = widen(x[(int64_t)i * x_stride + k]);
+        int s = seq_slot[i];
+        int m0 = 0, m1 = 0;
+        if (s >= 0 && s < L) {
+            m0 = member_off[s];
+            m1 = member_off[s + 1];
+        }
+        for (int c = 0; c < n_cols; c++) {
+            int n = cols ? cols[c] : c;
+            const uint16_t *wn = W + (size_t)n * K;
+            float base = 0.0f;
+            for (int k = 0; k < K; k++)
+                base += widen(wn[k]) * xq[k];
+            y[(size_t)j * n_cols + c] = base;
+        }
+        for (int m = m0; m < m1; m++) {
+            if (scale[m] == 0.0f || A[m] == NULL || rank[m] <= 0)
+                continue;
+            /* h = A_m x (ferrox `project`) */
+            for (int r = 0; r < rank[m]; r++) {
+                const uint16_t *am = A[m] + (size_t)r * K;
+                float hv = 0.0f;
+                for (int k = 0; k < K; k++)
+                    hv += widen(am[k]) * xq[k];
+                h[r] = hv;
+            }
+            /* out[n] += s_m * (b_n . h) (ferrox `accumulate`) */
+            for (int c = 0; c < n_cols; c++) {
+                int n = cols ? cols[c] : c;
+                const uint16_t *bm = B[m] + (size_t)n * rank[m];
+                float dm = 0.0f;
+                for (int r = 0; r < rank[m]; r++)
+                    dm += widen(bm[r]) * h[r];
+                y[(size_t)j * n_cols + c] += scale[m] * dm;
+            }
+        }
+        free(xq);
+        free(h);
+    }
+}
+
+/*
  * Embedding row gather through the adapted matrix E + s*B*A (ferrox-core
  * `weight_matrix/lora.rs`, `LoraDelta::add_row_to`: the delta of ONE row r of
  * s*B*A is s * (b_r . A), which is what a token-embedding gather needs):

@@ -400,6 +400,68 @@ def check_moe_gather_is_the_grouped_fold():
     assert np.array_equal(y.view(np.uint32), (rows[1::wl.top_k] + 0.0).view(np.uint32))
 
 
+# --------------------------------------------------------------------------
+# several adapters on one matrix (ferrox-core weight_matrix/lora.rs, LoraStack)
+# --------------------------------------------------------------------------
+
+
+def small_stack(seed=61, M=11, K=24, N=16, L=4, R=16):
+    wl = workloads.stacked(seed=seed, M=M, K=K, N=N, L=L, R=R, ranks=(1, 3, 4), max_members=3,
+                           p_none=0.2, a_bound=0.3, zero_member_slot=1)
+    # one member under the square-root rule and one without alpha
+    st = wl.stacks[0]
+    st[0] = Adapter(st[0].A, st[0].B, st[0].rank, 8.0, True, st[0].adapter_scale)
+    if len(wl.stacks[2]) > 0:
+        m = wl.stacks[2][0]
+        wl.stacks[2][0] = Adapter(m.A, m.B, m.rank, 0.0, False, 0.75)
+    return wl
+
+
+def check_stack_brute_force(tol=1e-4):
+    """y = (W + sum_m s_m B_m A_m) x_i with the delta matrix materialised, fp64."""
+    for seed in (61, 62, 63):
+        wl = small_stack(seed=seed)
+        y = oracle.proj_stack(wl.x, wl.W, wl.seq_slot, wl.stacks)
+        W, x = _f64(wl.W), _f64(wl.x)
+        for i in range(wl.M):
+            s = int(wl.seq_slot[i])
+            Weff = W.copy()
+            if 0 <= s < wl.max_loras:
+                for m in wl.stacks[s]:
+                    sc = oracle.scale(m.alpha, m.rank, m.use_rslora, m.adapter_scale)
+                    Weff += np.float64(sc) * (_f64(m.B) @ _f64(m.A))
+            ref = Weff @ x[i]
+            assert np.abs(y[i] - ref).max() <= tol * (1.0 + np.abs(ref).max()), (seed, i)
+
+
+def check_stack_reductions():
+    """A stack of one adapter is that adapter, byte for byte; a member at scale
+    0 adds nothing (the stack without it, byte for byte); rows whose slot is
+    -1, past max_loras or empty, and stacks whose every scale is 0, are the
+    base product byte for byte (ferrox lora.rs module doc, 'Cost when absent')."""
+    wl = small_stack(seed=64)
+    ss = wl.seq_slot
+    one = [st[:1] for st in wl.stacks]
+    y1 = oracle.proj_stack(wl.x, wl.W, ss, one)
+    yp = oracle.proj(wl.x, wl.W, ss, [st[0] for st in wl.stacks])
+    assert np.array_equal(y1.view(np.uint32), yp.view(np.uint32))
+    y = oracle.proj_stack(wl.x, wl.W, ss, wl.stacks)
+    nz = [[m for m in st if m.adapter_scale != 0.0] for st in wl.stacks]
+    assert any(len(a) != len(b) for a, b in zip(nz, wl.stacks))
+    ynz = oracle.proj_stack(wl.x, wl.W, ss, nz)
+    assert np.array_equal(y.view(np.uint32), ynz.view(np.uint32))
+    base = oracle.proj(wl.x, wl.W, np.full(wl.M, -1, np.int32), [None] * wl.max_loras)
+    none = ss < 0
+    assert none.any() and (~none).any()
+    assert np.array_equal(y[none].view(np.uint32), base[none].view(np.uint32))
+    assert not np.array_equal(y[~none], base[~none])
+    zero = [[Adapter(m.A, m.B, m.rank, m.alpha, m.use_rslora, 0.0) for m in st] for st in wl.stacks]
+    for stacks, slots in ((zero, ss), ([[] for _ in wl.stacks], ss),
+                          (wl.stacks, np.full(wl.M, wl.max_loras + 2, np.int32))):
+        yz = oracle.proj_stack(wl.x, wl.W, slots, stacks)
+        assert np.array_equal(yz.view(np.uint32), base.view(np.uint32))
+
+
 ALL_CHECKS = [
     check_scale_examples,
     check_hand_example,
@@ -419,4 +481,6 @@ ALL_CHECKS = [
     check_gate_up_is_the_split_projections,
     check_moe_gather_brute_force,
     check_moe_gather_is_the_grouped_fold,
+    check_stack_brute_force,
+    check_stack_reductions,
 ]

@@ -49,6 +49,11 @@ MUTANTS = {
     "gather_expert_ignored": ("int e = indices[j];", "int e = indices[j] >= 0 ? 0 : -1;"),
     "gather_no_reset_per_token": ("if (j % top_k == 0)\n                for (int n = 0; n < N; n++)\n                    yt[n] = 0.0f;",
                                   "if (j == 0)\n                for (int n = 0; n < N; n++)\n                    yt[n] = 0.0f;"),
+    "stack_first_member_dropped": ("for (int m = m0; m < m1; m++) {", "for (int m = m0 + 1; m < m1; m++) {"),
+    "stack_first_scale_for_all": ("y[(size_t)j * n_cols + c] += scale[m] * dm;",
+                                  "y[(size_t)j * n_cols + c] += scale[m0] * dm;"),
+    "stack_h_from_the_first_member": ("const uint16_t *am = A[m] + (size_t)r * K;",
+                                      "const uint16_t *am = A[m0] + (size_t)(r % rank[m0]) * K;"),
     "h_uses_pool_row_of_next_slot": ("const uint16_t *arow = A[s] + (size_t)r * K;",
                                      "const uint16_t *arow = A[(s + 1) % L] ? A[(s + 1) % L] + (size_t)r * K : A[s] + (size_t)r * K;"),
 }

@@ -103,3 +103,11 @@ def test_moe_gather_brute_force_fp64():
 
 def test_moe_gather_is_the_grouped_fold():
     P.check_moe_gather_is_the_grouped_fold()
+
+
+def test_stack_brute_force_fp64():
+    P.check_stack_brute_force()
+
+
+def test_stack_reductions_are_exact():
+    P.check_stack_reductions()

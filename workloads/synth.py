@@ -382,6 +382,63 @@ def random_small(seed: int, M: int, K: int, N: int, L: int, R: int,
     return ProjWorkload(f"random{seed}", seed, M, K, N, L, R, W, x, seq_slot, ads)
 
 
+@dataclass
+class StackWorkload:
+    """A projection whose slots each hold a stack of adapters (several
+    adapters on one base matrix, all applied to the slot's rows)."""
+    name: str
+    seed: int
+    M: int
+    K: int
+    N: int
+    max_loras: int
+    max_rank: int
+    W: np.ndarray               # [N][K] bf16 bits
+    x: np.ndarray               # [M][K] bf16 bits
+    seq_slot: np.ndarray        # [M] int32, <0 = no adapter
+    stacks: List[List[Adapter]]  # per slot, its members in order (empty: no adapter)
+    note: str = ""
+
+
+def stacked(seed: int = 7, M: int = 64, K: int = 4096, N: int = 4096, L: int = 8, R: int = 64,
+            ranks=(8, 16, 32), max_members: int = 3, p_none: float = 0.1,
+            a_bound: float = 1.0 / 64, zero_member_slot: int = 1) -> StackWorkload:
+    """Base [N][K] ~ N(0, 1/K), M rows of x ~ N(0, 1), L slots each holding a
+    stack of 1..max_members adapters with ranks from ``ranks`` (A ~ U(+-a_bound),
+    B ~ N(0, 0.02), alpha = 2 rank, adapter scale from {0.5, 1}), the members'
+    ranks summing to at most R; slot ``zero_member_slot`` (if any) gets one more
+    member with adapter scale 0. Slots uniform over the L slots, round(p_none M)
+    rows set to -1.
+
+    Draw order: W, x, per slot (member count, then per member: rank, adapter
+    scale, A, B), slot per row, the -1 rows.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    W = _normal_bf16(rng, (N, K), 1.0 / K)
+    x = _normal_bf16(rng, (M, K), 1.0)
+    stacks: List[List[Adapter]] = []
+    for s in range(L):
+        n_m = int(rng.integers(1, max_members + 1))
+        members: List[Adapter] = []
+        used = 0
+        for _ in range(n_m):
+            r = int(rng.choice(np.array(ranks)))
+            sc = float(rng.choice(np.array([0.5, 1.0])))
+            if used + r > R:
+                break
+            members.append(_adapter(rng, K, N, r, a_bound, 0.02, alpha=2.0 * r, adapter_scale=sc))
+            used += r
+        if s == zero_member_slot and used + min(ranks) <= R:
+            members.append(_adapter(rng, K, N, int(min(ranks)), a_bound, 0.02, alpha=2.0 * min(ranks),
+                                    adapter_scale=0.0))
+        stacks.append(members)
+    seq_slot = rng.integers(0, L, size=M, dtype=np.int64).astype(np.int32)
+    seq_slot = _mark_no_adapter(rng, seq_slot, p_none)
+    return StackWorkload("stacked", seed, M, K, N, L, R, W, x, seq_slot, stacks,
+                         note="W~N(0,1/K) x~N(0,1); per slot 1-3 adapters r in {8,16,32} (sum <= R), "
+                              "A~U(+-1/64) B~N(0,0.02) alpha=2r, adapter scale {0.5,1}; one member at scale 0")
+
+
 def embed(seed: int = 5, M: int = 64, vocab: int = 32000, n_embd: int = 4096, L: int = 16,
           R: int = 64, ranks=None, p_none: float = 0.1) -> EmbedWorkload:
     """Token embedding [vocab][n_embd] ~ N(0, 0.02) gathered for M tokens drawn

@@ -110,7 +110,15 @@ enum {
  * factor_table[max_loras] f32 alpha factor (alpha/rank, alpha/sqrt(rank), or 1
  *             when alpha is 0), so that lora_set_scale can rebuild the scale.
  * rank_table  [max_loras] i32 true rank of each slot (0 = empty).
+ * comp_table  [max_loras][LORA_COMP_STRIDE] f32 per-rank factor of each slot:
+ *             the delta of slot s is sum_r B[:, r] * (scale_table[s] *
+ *             comp_table[s][r]) * (A x)[r]. 1 for every rank of a slot packed
+ *             with lora_pool_pack; a slot holding a stack of adapters
+ *             (lora_pool_pack_stack) carries each member's own scale on that
+ *             member's ranks.
  */
+#define LORA_COMP_STRIDE 256
+
 typedef struct lora_route {
     void *pool;
     const void **a_table;
@@ -118,6 +126,7 @@ typedef struct lora_route {
     float *scale_table;
     float *factor_table;
     int32_t *rank_table;
+    float *comp_table;
     int32_t n_in;      /* K */
     int32_t n_out;     /* N */
     int32_t max_rank;  /* R: the pool's padded rank */
@@ -132,7 +141,8 @@ typedef struct lora_route {
 size_t lora_pool_bytes(int max_loras, int max_rank, int n_in, int n_out);
 
 /* Bytes of the device tables of one route (a_table, b_table, scale_table,
- * factor_table, rank_table, each 256-byte aligned). 0 for max_loras <= 0. */
+ * factor_table, rank_table, comp_table, each 256-byte aligned). 0 for
+ * max_loras <= 0. */
 size_t lora_route_table_bytes(int max_loras);
 
 /*
@@ -169,6 +179,36 @@ lora_status lora_route_init(lora_route *rt, void *pool, size_t pool_bytes, void 
 lora_status lora_pool_pack(const lora_route *rt, int slot, const void *A, const void *B,
                            int rank, float alpha, int use_rslora, float adapter_scale,
                            lora_stream_t stream);
+
+/*
+ * Several adapters on one matrix, in one slot (ferrox-core `weight_matrix/
+ * lora.rs`, `LoraStack`: every adapter attached to a matrix is one term of
+ * the sum, y = W x + sum_m s_m B_m (A_m x)). The slot's rows get every
+ * member's delta.
+ *   n               members (0: the slot becomes empty)
+ *   A[m], B[m]      host arrays of n pointers: member m's [ranks[m]][n_in] and
+ *                   [n_out][ranks[m]] bf16 pair, host or device memory
+ *   ranks, alphas, use_rslora, adapter_scales   host arrays of n entries, each
+ *                   member's rank, alpha, rule and runtime scale, with the
+ *                   meaning they have in lora_pool_pack
+ * Member m's scale s_m = adapter_scales[m] * factor(alphas[m], ranks[m],
+ * use_rslora[m]). A member whose s_m is 0 is left out (the delta of a
+ * zero-scale adapter is skipped before any arithmetic); the others are laid
+ * out one after another along the slot's rank (A rows, B columns), their
+ * ranks summing to at most max_rank, and comp_table[slot] holds s_m on member
+ * m's ranks. scale_table[slot] = factor_table[slot] = 1, so lora_set_scale /
+ * lora_set_scales afterwards multiply the whole stack by the value given. A
+ * stack with no member left is an empty slot.
+ * Errors: embedding route (LORA_ERR_UNSUPPORTED); slot outside [0, max_loras);
+ * n < 0; NULL arrays with n > 0 or a NULL member pointer; a rank < 1; the
+ * kept members' ranks summing past max_rank (message names the sum and
+ * max_rank). Nothing is written on an error.
+ * Stream-ordered like lora_pool_pack.
+ */
+lora_status lora_pool_pack_stack(const lora_route *rt, int slot, int n, const void *const *A,
+                                 const void *const *B, const int32_t *ranks, const float *alphas,
+                                 const int32_t *use_rslora, const float *adapter_scales,
+                                 lora_stream_t stream);
 
 /* Empty `slot` (table entries NULL / 0): its rows get no delta afterwards. */
 lora_status lora_pool_unpack(const lora_route *rt, int slot, lora_stream_t stream);

@@ -43,6 +43,7 @@ LORA_PATH_TC = 2
 
 LORA_MAX_EXPERTS = 16
 LORA_STATIC_WS_BYTES = 8 << 20
+LORA_COMP_STRIDE = 256
 
 
 class LoraError(RuntimeError):
@@ -60,6 +61,7 @@ class lora_route(ctypes.Structure):
         ("scale_table", ctypes.c_void_p),
         ("factor_table", ctypes.c_void_p),
         ("rank_table", ctypes.c_void_p),
+        ("comp_table", ctypes.c_void_p),
         ("n_in", ctypes.c_int32),
         ("n_out", ctypes.c_int32),
         ("max_rank", ctypes.c_int32),
@@ -94,6 +96,8 @@ _SIGNATURES = {
     "lora_route_table_bytes": (_sz, [_i]),
     "lora_route_init": (_i, [_rtp, _vp, _sz, _vp, _sz, _i, _i, _i, _i, _vp]),
     "lora_pool_pack": (_i, [_rtp, _i, _vp, _vp, _i, _f, _i, _f, _vp]),
+    "lora_pool_pack_stack": (_i, [_rtp, _i, _i, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32p,
+                                  ctypes.POINTER(ctypes.c_float), _i32p, ctypes.POINTER(ctypes.c_float), _vp]),
     "lora_pool_unpack": (_i, [_rtp, _i, _vp]),
     "lora_set_scale": (_i, [_rtp, _i, _f, _vp]),
     "lora_set_scales": (_i, [_rtp, _i32p, ctypes.POINTER(ctypes.c_float), _i, _vp]),
@@ -190,6 +194,23 @@ def lora_pool_pack(rt: lora_route, slot: int, A, B, rank: int, alpha: float, use
     b = B.ctypes.data if hasattr(B, "ctypes") else _ptr(B)
     _check(lib().lora_pool_pack(ctypes.byref(rt), slot, a, b, rank, alpha, int(bool(use_rslora)),
                                 adapter_scale, _stream(stream)))
+
+
+def lora_pool_pack_stack(rt: lora_route, slot: int, As, Bs, ranks, alphas, use_rslora, adapter_scales,
+                         stream=None) -> None:
+    """Several adapters in one slot. As / Bs: lists of device pointers/tensors
+    or host numpy arrays (bf16 bits); the other arguments are lists of the
+    members' rank, alpha, rule and runtime scale."""
+    n = len(As)
+    keep = [ctypes.c_void_p(a.ctypes.data if hasattr(a, "ctypes") else _ptr(a)) for a in As]
+    keep_b = [ctypes.c_void_p(b.ctypes.data if hasattr(b, "ctypes") else _ptr(b)) for b in Bs]
+    pa = (ctypes.c_void_p * max(n, 1))(*keep)
+    pb = (ctypes.c_void_p * max(n, 1))(*keep_b)
+    rk = (ctypes.c_int32 * max(n, 1))(*[int(r) for r in ranks])
+    al = (ctypes.c_float * max(n, 1))(*[float(a) for a in alphas])
+    rs = (ctypes.c_int32 * max(n, 1))(*[int(bool(r)) for r in use_rslora])
+    sc = (ctypes.c_float * max(n, 1))(*[float(v) for v in adapter_scales])
+    _check(lib().lora_pool_pack_stack(ctypes.byref(rt), slot, n, pa, pb, rk, al, rs, sc, _stream(stream)))
 
 
 def lora_pool_unpack(rt: lora_route, slot: int, stream=None) -> None:

@@ -51,7 +51,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 size_t slot_bytes(int R, int K, int N) { return ((size_t)R * K + (size_t)N * R) * 2; }
 
 struct TableLayout {
-    size_t a, b, scale, factor, rank, total;
+    size_t a, b, scale, factor, rank, comp, total;
 };
 
 TableLayout table_layout(int L)
@@ -63,6 +63,7 @@ TableLayout table_layout(int L)
     t.scale = o;  o = align256(o + sizeof(float) * (size_t)L);
     t.factor = o; o = align256(o + sizeof(float) * (size_t)L);
     t.rank = o;   o = align256(o + sizeof(int32_t) * (size_t)L);
+    t.comp = o;   o = align256(o + sizeof(float) * LORA_COMP_STRIDE * (size_t)L);
     t.total = o;
     return t;
 }
@@ -247,6 +248,7 @@ lora_status route_setup(lora_route *rt, void *pool, size_t pool_bytes, void *tab
     rt->scale_table = reinterpret_cast<float *>(tb + tl.scale);
     rt->factor_table = reinterpret_cast<float *>(tb + tl.factor);
     rt->rank_table = reinterpret_cast<int32_t *>(tb + tl.rank);
+    rt->comp_table = reinterpret_cast<float *>(tb + tl.comp);
     rt->n_in = n_in;
     rt->n_out = n_out;
     rt->max_rank = max_rank;
@@ -334,6 +336,12 @@ lora_status pack_slot(const lora_route *rt, int slot, const void *A, const void 
         e = cudaMemcpy2DAsync(dB, (size_t)R * 2, B, (size_t)rank * 2, (size_t)rank * 2, (size_t)N,
                               cudaMemcpyDefault, st);
     const float factor = alpha_factor(alpha, rank, use_rslora);
+    if (e == cudaSuccess && !embed) {
+        CompRow ones;
+        for (int k = 0; k < LORA_COMP_STRIDE; ++k)
+            ones.v[k] = 1.0f; // s * 1 == s: the slot's delta is its scale times B (A x)
+        e = launch_comp_set(*rt, slot, ones, st);
+    }
     if (e == cudaSuccess)
         e = launch_table_set(*rt, slot, dA, dB, rank, factor, adapter_scale * factor, st);
     if (e != cudaSuccess)
@@ -366,6 +374,78 @@ lora_status lora_pool_pack(const lora_route *rt, int slot, const void *A, const 
                            float alpha, int use_rslora, float adapter_scale, lora_stream_t stream)
 {
     return pack_slot(rt, slot, A, B, rank, alpha, use_rslora, adapter_scale, stream, false);
+}
+
+lora_status lora_pool_pack_stack(const lora_route *rt, int slot, int n, const void *const *A,
+                                 const void *const *B, const int32_t *ranks, const float *alphas,
+                                 const int32_t *use_rslora, const float *adapter_scales,
+                                 lora_stream_t stream)
+{
+    const char *who = "lora_pool_pack_stack";
+    lora_status s = check_route_kind(rt, LORA_ROUTE_PROJ, who);
+    if (s != LORA_OK)
+        return s;
+    if (slot < 0 || slot >= rt->max_loras)
+        return fail(LORA_ERR_RANGE, "%s: slot %d is out of range: pool has %d slot(s)", who, slot,
+                    rt->max_loras);
+    if (n < 0)
+        return fail(LORA_ERR_SHAPE, "%s: n %d is negative", who, n);
+    if (n > 0 && (A == nullptr || B == nullptr || ranks == nullptr || alphas == nullptr ||
+                  use_rslora == nullptr || adapter_scales == nullptr))
+        return fail(LORA_ERR_NULL, "%s: the member arrays must be non-NULL when n > 0", who);
+    const int R = rt->max_rank, K = rt->n_in, N = rt->n_out;
+    // members kept (nonzero scale), their scales and rank offsets
+    CompRow comp;
+    for (int k = 0; k < LORA_COMP_STRIDE; ++k)
+        comp.v[k] = 0.0f;
+    int total = 0;
+    for (int m = 0; m < n; ++m) {
+        if (ranks[m] < 1)
+            return fail(LORA_ERR_SHAPE, "%s: member %d has rank %d (need >= 1)", who, m, ranks[m]);
+        if (A[m] == nullptr || B[m] == nullptr)
+            return fail(LORA_ERR_NULL, "%s: member %d has a NULL A or B", who, m);
+        const float sm = adapter_scales[m] * alpha_factor(alphas[m], ranks[m], use_rslora[m]);
+        if (sm == 0.0f)
+            continue;
+        if (total + ranks[m] > R) {
+            int sum = 0;
+            for (int q = 0; q < n; ++q)
+                if (adapter_scales[q] * alpha_factor(alphas[q], ranks[q], use_rslora[q]) != 0.0f)
+                    sum += ranks[q];
+            return fail(LORA_ERR_SHAPE,
+                        "%s: the members' ranks sum to %d, past max_rank %d of route [n_out %d x n_in %d]",
+                        who, sum, R, N, K);
+        }
+        for (int k = total; k < total + ranks[m]; ++k)
+            comp.v[k] = sm;
+        total += ranks[m];
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *base = static_cast<uint8_t *>(rt->pool) + (size_t)slot * slot_bytes(R, K, N);
+    uint16_t *dA = reinterpret_cast<uint16_t *>(base);
+    uint16_t *dB = reinterpret_cast<uint16_t *>(base + (size_t)R * K * 2);
+    // unpublish first, as lora_pool_pack does
+    cudaError_t e = launch_table_set(*rt, slot, nullptr, nullptr, 0, 0.0f, 0.0f, st);
+    if (e == cudaSuccess && total > 0)
+        e = cudaMemsetAsync(base, 0, slot_bytes(R, K, N), st);
+    int off = 0;
+    for (int m = 0; m < n && e == cudaSuccess && total > 0; ++m) {
+        const int r = ranks[m];
+        if (adapter_scales[m] * alpha_factor(alphas[m], r, use_rslora[m]) == 0.0f)
+            continue;
+        e = cudaMemcpyAsync(dA + (size_t)off * K, A[m], (size_t)r * K * 2, cudaMemcpyDefault, st);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(dB + off, (size_t)R * 2, B[m], (size_t)r * 2, (size_t)r * 2, (size_t)N,
+                                  cudaMemcpyDefault, st);
+        off += r;
+    }
+    if (e == cudaSuccess && total > 0)
+        e = launch_comp_set(*rt, slot, comp, st);
+    if (e == cudaSuccess && total > 0)
+        e = launch_table_set(*rt, slot, dA, dB, total, 1.0f, 1.0f, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e, who);
+    return ok();
 }
 
 lora_status lora_embed_pool_pack(const lora_route *rt, int slot, const void *rows, const void *cols,
@@ -508,6 +588,7 @@ Tables tables_of(const lora_route &rt)
     t.b_table = reinterpret_cast<const uint16_t *const *>(rt.b_table);
     t.scale_table = rt.scale_table;
     t.rank_table = rt.rank_table;
+    t.comp_table = rt.comp_table;
     return t;
 }
 

@@ -20,6 +20,7 @@ struct Tables {
     const uint16_t *const *b_table;
     const float *scale_table;
     const int32_t *rank_table;
+    const float *comp_table; // [L][LORA_COMP_STRIDE] per-rank factors
 };
 
 // What the expand needs for a row routed to slot s of table t. A row gets no
@@ -143,6 +144,11 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
 cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, const void *b,
                              int rank, float factor, float scale, cudaStream_t st);
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st);
+// The per-rank factors of one slot, passed by value.
+struct CompRow {
+    float v[LORA_COMP_STRIDE];
+};
+cudaError_t launch_comp_set(const lora_route &rt, int slot, const CompRow &row, cudaStream_t st);
 // A^T [n][R] of a device A [rank][n], into a zeroed slot.
 cudaError_t launch_transpose_pack(uint16_t *At, int R, const uint16_t *A, int rank, int n, cudaStream_t st);
 // Runtime scales of up to SCALE_CHUNK consecutive slots, passed by value.

@@ -327,6 +327,17 @@ cudaError_t launch_transpose_pack(uint16_t *At, int R, const uint16_t *A, int ra
     return cudaGetLastError();
 }
 
+__global__ void comp_set_kernel(float *comp_row, CompRow row)
+{
+    comp_row[threadIdx.x] = row.v[threadIdx.x];
+}
+
+cudaError_t launch_comp_set(const lora_route &rt, int slot, const CompRow &row, cudaStream_t st)
+{
+    comp_set_kernel<<<1, LORA_COMP_STRIDE, 0, st>>>(rt.comp_table + (size_t)slot * LORA_COMP_STRIDE, row);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st)
 {
     scale_set_kernel<<<1, 1, 0, st>>>(rt.scale_table, rt.factor_table, slot, adapter_scale);

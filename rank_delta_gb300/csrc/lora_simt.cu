@@ -3,9 +3,11 @@
 // One warp per output row n (grid-stride), rows of x taken 8 at a time: the
 // warp streams W[n, :] once per 8 rows with 16-byte loads, keeps 8 fp32
 // partial sums per lane and reduces them with shuffles. The expand-fold is in
-// the same pass: y = base + s * (B_s[n, :] . h_i), rounded once to bf16
+// the same pass: y = base + s * (B_s[n, :] . (c_s * h_i)), rounded once to bf16
 // (ferrox-core `weight_matrix/lora.rs`, `LoraDelta::accumulate`), with h_i
-// the rank-sized shrink of the row produced by shrink_kernel.
+// the rank-sized shrink of the row produced by shrink_kernel and c_s the
+// slot's per-rank factors (1 for a single adapter, each member's scale for a
+// stack of adapters).
 #include "lora_internal.cuh"
 #include "shrink.cuh"
 #include "vec.cuh"
@@ -58,10 +60,16 @@ __global__ void __launch_bounds__(256) simt_kernel(Params p)
                     const SlotInfo si = slot_info(tab, p.seq_slot[t], p.L);
                     if (si.on) {
                         const uint16_t *brow = si.b + (size_t)n * p.R;
+                        const float *cr = tab.comp_table + (size_t)p.seq_slot[t] * LORA_COMP_STRIDE;
                         float d = 0.0f;
                         for (int q = 0; q < si.rank; q += 8) {
                             float4 h0, h1;
                             h_sum8(p, t, q, h0, h1);
+                            // the rank's factor (1 unless the slot holds a stack of adapters)
+                            const float4 c0 = __ldg(reinterpret_cast<const float4 *>(cr + q));
+                            const float4 c1 = __ldg(reinterpret_cast<const float4 *>(cr + q + 4));
+                            h0.x *= c0.x; h0.y *= c0.y; h0.z *= c0.z; h0.w *= c0.w;
+                            h1.x *= c1.x; h1.y *= c1.y; h1.z *= c1.z; h1.w *= c1.w;
                             d = dot8_bf_f32(d, ld_nc_16(brow + q), h0, h1);
                         }
                         v = v + si.scale * d;

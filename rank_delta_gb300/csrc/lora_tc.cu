@@ -96,6 +96,7 @@ struct EpiAux {
     int32_t koff[MAX_TN];            // k offset of column j's slot in the expand, -1: no delta here
     float cscale[MAX_TN];            // scale of column j's slot
     int16_t crank[MAX_TN];           // rank of column j's slot
+    int16_t cslot[MAX_TN];           // column j's slot (per-rank factors)
     uint16_t soff[1024];             // per slot: padded rank if used (0 if not), then its k offset
     int8_t part_of[1024];            // per used slot: the K part that adds its delta
     int16_t entry_slot[MAX_TN];      // the expand's slots, ascending
@@ -521,17 +522,22 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
             continue;
         const int rk = aux->crank[j];
         const float s = aux->cscale[j];
+        const float *cr = p.tab[ti.e].comp_table + (size_t)aux->cslot[j] * LORA_COMP_STRIDE;
         // ranks r (multiples of 8, r < rank) of this slot that fall in the pass
         const int rlo = max(0, r0k - ko), rhi = min(rk, r0k + kt - ko);
         const float *hrow = p.ws.h + (size_t)(ti.r0 + j) * p.R;
         for (int r = rlo + 8 * sub; r < rhi; r += 32 * tpc) {
-            float4 a[4], b[4];
+            float4 a[4], b[4], ca[4], cb[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int rr = r + 8 * tpc * u;
                 a[u] = make_float4(0.f, 0.f, 0.f, 0.f);
                 b[u] = a[u];
+                ca[u] = a[u];
+                cb[u] = a[u];
                 if (rr < rhi) {
+                    ca[u] = __ldg(reinterpret_cast<const float4 *>(cr + rr));
+                    cb[u] = __ldg(reinterpret_cast<const float4 *>(cr + rr + 4));
 #pragma unroll
                     for (int kq = 0; kq < 4; ++kq) {
                         if (kq < p.kp) { // parts summed in part order
@@ -549,8 +555,11 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
                 const int rr = r + 8 * tpc * u;
                 if (rr >= rhi)
                     break;
-                const float v[8] = {a[u].x * s, a[u].y * s, a[u].z * s, a[u].w * s,
-                                    b[u].x * s, b[u].y * s, b[u].z * s, b[u].w * s};
+                // s * comp: the slot's scale times the rank's factor (1 unless the
+                // slot holds a stack of adapters)
+                const float v[8] = {a[u].x * (s * ca[u].x), a[u].y * (s * ca[u].y), a[u].z * (s * ca[u].z),
+                                    a[u].w * (s * ca[u].w), b[u].x * (s * cb[u].x), b[u].y * (s * cb[u].y),
+                                    b[u].z * (s * cb[u].z), b[u].w * (s * cb[u].w)};
                 uint32_t h8[8], l8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
@@ -636,6 +645,7 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
             aux->koff[j] = si.on ? sl : -1;
             aux->cscale[j] = si.scale;
             aux->crank[j] = (int16_t)si.rank;
+            aux->cslot[j] = (int16_t)(si.on ? sl : 0);
             if (si.on) {
                 aux->soff[sl] = (uint16_t)((si.rank + 15) & ~15); // same value from every writer
                 if (c.local_route) {

@@ -65,6 +65,13 @@ class DeviceRoute:
                           np.ascontiguousarray(adapter.B), adapter.rank, adapter.alpha,
                           adapter.use_rslora, adapter.adapter_scale, stream)
 
+    def pack_stack(self, slot: int, members, stream=None) -> None:
+        """Pack a list of ``workloads.Adapter`` into `slot` as one stack."""
+        rd.lora_pool_pack_stack(self.rt, slot, [np.ascontiguousarray(m.A) for m in members],
+                                [np.ascontiguousarray(m.B) for m in members], [m.rank for m in members],
+                                [m.alpha for m in members], [m.use_rslora for m in members],
+                                [m.adapter_scale for m in members], stream)
+
     def pack_all(self, adapters, stream=None) -> None:
         for s, ad in enumerate(adapters):
             if ad is not None:

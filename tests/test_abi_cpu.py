@@ -271,3 +271,20 @@ def test_moe_gather_argument_checks():
     expect(rd.LORA_ERR_WORKSPACE, call(wsb=need - 1))
     expect(rd.LORA_ERR_SHAPE, call(K=256), contains=("expert 0",))
     expect(rd.LORA_ERR_UNSUPPORTED, call(E=17))
+
+
+def test_pack_stack_refusals_name_the_problem():
+    rt = fake_route(L=4, R=16, K=64, N=32)
+    A = np.zeros((8, 64), np.uint16)
+    B = np.zeros((32, 8), np.uint16)
+    expect(rd.LORA_ERR_RANGE, rd.lora_pool_pack_stack, rt, 4, [A], [B], [8], [16.0], [0], [1.0],
+           contains=("slot 4", "4 slot"))
+    # three members of rank 8 at nonzero scale: 24 > max_rank 16
+    expect(rd.LORA_ERR_SHAPE, rd.lora_pool_pack_stack, rt, 0, [A, A, A], [B, B, B], [8, 8, 8],
+           [16.0] * 3, [0] * 3, [1.0] * 3, contains=("sum to 24", "max_rank 16"))
+    expect(rd.LORA_ERR_SHAPE, rd.lora_pool_pack_stack, rt, 0, [A], [B], [0], [16.0], [0], [1.0],
+           contains=("rank 0",))
+    expect(rd.LORA_ERR_NULL, rd.lora_pool_pack_stack, rt, 0, [A, 0], [B, B], [8, 8], [16.0] * 2,
+           [0] * 2, [1.0] * 2, contains=("member 1",))
+    emb = fake_route(kind=rd.LORA_ROUTE_EMBED)
+    expect(rd.LORA_ERR_UNSUPPORTED, rd.lora_pool_pack_stack, emb, 0, [A], [B], [8], [16.0], [0], [1.0])

@@ -52,9 +52,16 @@ DESCRIBE = {
                "8 adapters r=64 rsLoRA alpha=16 (B rows split the same way), act = silu(gate) * up",
     "gate_up_decode": "gated MLP input: 64 rows x fused W[4096x4096] bf16 = gate 2048 | up 2048, 16 adapters "
                       "r in {8,16,32,64} pool R=64, alpha=2r, 10% rows slot -1, act = silu(gate) * up",
+    "moe_gather": "decode MoE down with top-2 combine: 64 tokens x top-2 = 128 slot-rows in token order, "
+                  "8 experts W_e[4096x14336] bf16 named per slot-row, 4 adapters/expert r=16 alpha=32, "
+                  "combine = softmax of the top-2 logits",
+    "stack": "several adapters per slot: 64 rows x W[4096x4096] bf16, 8 slots each a stack of 1-3 adapters "
+             "r in {8,16,32} (ranks summing to <= pool R=64), alpha=2r, adapter scales {0.5,1}, one member "
+             "at scale 0, 10% rows slot -1",
 }
 BOUND = {"tiny": "hbm", "decode": "hbm", "qkv": "hbm", "prefill": "tensor", "moe": "hbm",
-         "embed": "hbm", "embed_prefill": "hbm", "gate_up": "tensor", "gate_up_decode": "hbm"}
+         "embed": "hbm", "embed_prefill": "hbm", "gate_up": "tensor", "gate_up_decode": "hbm",
+         "stack": "hbm", "moe_gather": "hbm"}
 GATE_UP = {"gate_up": "prefill", "gate_up_decode": "decode"}  # the projection workload each one reads
 EMBED_ROWS = {"embed": 64, "embed_prefill": 4096}
 # --small: the same kernels on fewer rows, for profiler captures only (never a bench line)
@@ -114,6 +121,49 @@ def embed_algorithmic(wl):
             touched.add(s)
     for s in touched:
         byts += wl.adapters[s].rank * n * 2
+    return float(byts), float(flops)
+
+
+def moe_gather_algorithmic(wl):
+    """W of every expert a slot-row names, x, y [tokens][N], indices, slots
+    and combine weights, plus each expert's touched adapters at true rank."""
+    T, K, N = wl.T, wl.K, wl.N
+    byts = T * K * 2 + (T // wl.top_k) * N * 2 + T * 4 * 3
+    flops = 2.0 * T * N * K
+    for e in range(wl.E):
+        rows = np.nonzero(wl.indices == e)[0]
+        if len(rows) == 0:
+            continue
+        byts += N * K * 2
+        touched = set()
+        for j in rows:
+            s = int(wl.seq_slot[j])
+            if 0 <= s < wl.max_loras and _scale_on(wl.adapters[e][s]):
+                flops += 2.0 * wl.adapters[e][s].rank * (K + N)
+                touched.add(s)
+        for s in touched:
+            r = wl.adapters[e][s].rank
+            byts += (r * K + N * r) * 2
+    return float(byts), float(flops)
+
+
+def stack_algorithmic(wl):
+    """W + x + y + seq_slot, plus A and B of every member (scale not 0, true
+    rank) of the slots the batch touches; flops 2MNK + per adapted row the
+    members' 2 r (K + N)."""
+    M, K, N = wl.M, wl.K, wl.N
+    byts = N * K * 2 + M * K * 2 + M * N * 2 + M * 4
+    flops = 2.0 * M * N * K
+    touched = set()
+    for i in range(M):
+        s = int(wl.seq_slot[i])
+        if 0 <= s < wl.max_loras:
+            ms = [m for m in wl.stacks[s] if m.adapter_scale != 0.0]
+            flops += sum(2.0 * m.rank * (K + N) for m in ms)
+            if ms:
+                touched.add(s)
+    for s in touched:
+        byts += sum((m.rank * K + N * m.rank) * 2 for m in wl.stacks[s] if m.adapter_scale != 0.0)
     return float(byts), float(flops)
 
 
@@ -317,6 +367,50 @@ class EmbedSet:
                             y.stride(0), self.ws, self.ws.numel(), stream)
 
 
+class MoeGatherSet:
+    """One buffer set of the decode MoE fold with the top-k combine."""
+
+    def __init__(self, wl, th, rd, torch):
+        self.x = th.to_device_bf16(wl.x)
+        self.W = [th.to_device_bf16(w) for w in wl.W]
+        self.idx = torch.from_numpy(wl.indices.astype(np.int32)).cuda()
+        self.slots = torch.from_numpy(wl.seq_slot.astype(np.int32)).cuda()
+        self.combine = torch.from_numpy(wl.combine.astype(np.float32)).cuda()
+        self.routes = []
+        for e in range(wl.E):
+            r = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.K, wl.N)
+            r.pack_all(wl.adapters[e])
+            self.routes.append(r)
+        self.rts = [r.rt for r in self.routes]
+        self.y = torch.empty((wl.T // wl.top_k, wl.N), dtype=torch.bfloat16, device="cuda")
+        self.ws = th.workspace(rd.lora_moe_gather_workspace_bytes(wl.E, wl.T, self.rts))
+        self.bytes = (sum(w.numel() for w in self.W) * 2 + sum(r.pool_bytes for r in self.routes)
+                      + self.x.numel() * 2 + self.y.numel() * 2)
+
+    def step(self, wl, rd, stream, x=None, slots=None, y=None):
+        x = self.x if x is None else x
+        slots = self.slots if slots is None else slots
+        y = self.y if y is None else y
+        rd.lora_moe_gather_apply(x, x.stride(0), self.W, self.idx, wl.E, wl.T, wl.K, wl.N, slots, self.rts,
+                                 self.combine, wl.top_k, y, y.stride(0), self.ws, self.ws.numel(), stream)
+
+
+class StackSet(ProjSet):
+    """A projection buffer set whose slots each hold a stack of adapters."""
+
+    def __init__(self, wl, th, rd, torch):
+        self.x = th.to_device_bf16(wl.x)
+        self.W = th.to_device_bf16(wl.W)
+        self.slots = torch.from_numpy(wl.seq_slot.astype(np.int32)).cuda()
+        self.route = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.K, wl.N)
+        for s, st in enumerate(wl.stacks):
+            self.route.pack_stack(s, st)
+        self.y = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
+        self.ws = th.workspace(rd.lora_proj_workspace_bytes(wl.M, self.route.rt))
+        self.bytes = (self.W.numel() * 2 + self.route.pool_bytes + self.x.numel() * 2 +
+                      self.y.numel() * 2)
+
+
 class GateUpSet(ProjSet):
     """A projection buffer set whose output is act [M][I]."""
 
@@ -363,6 +457,8 @@ TC_SHRINK_MIN_ROWS = 2048
 def launches_per_call(config, rows, kernel):
     if kernel == "embed_kernel":
         return LAUNCHES_EMBED
+    if config == "moe_gather":  # expert sort + row copy, the grouped fold, the combine
+        return LAUNCHES_TC + 2
     if config in GATE_UP: # the projection, then the activation kernel
         return launches_per_call(GATE_UP[config], rows, kernel) + 1
     if kernel == "simt_kernel":
@@ -376,6 +472,10 @@ def make_workload(config, small=False):
     import workloads
     if config in EMBED_ROWS:
         return workloads.embed(M=EMBED_ROWS[config])
+    if config == "stack":
+        return workloads.stacked()
+    if config == "moe_gather":
+        return workloads.moe_gather()
     if config in GATE_UP:
         base = GATE_UP[config]
         return workloads.make(base, **(SMALL.get(base, {}) if small else {}))
@@ -397,16 +497,25 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     wl = make_workload(args.config, args.small)
     is_moe = args.config == "moe"
+    slot_rows = args.config in ("moe", "moe_gather")
     is_embed = args.config in EMBED_ROWS
-    rows = wl.T if is_moe else wl.M
+    rows = wl.T if slot_rows else wl.M
     is_gate_up = args.config in GATE_UP
     if is_embed:
         algo_bytes, algo_flops = embed_algorithmic(wl)
+    elif args.config == "stack":
+        algo_bytes, algo_flops = stack_algorithmic(wl)
+    elif args.config == "moe_gather":
+        algo_bytes, algo_flops = moe_gather_algorithmic(wl)
     elif is_gate_up:
         algo_bytes, algo_flops = gate_up_algorithmic(wl)
     else:
         algo_bytes, algo_flops = moe_algorithmic(wl) if is_moe else proj_algorithmic(wl)
     Set = MoeSet if is_moe else (EmbedSet if is_embed else (GateUpSet if is_gate_up else ProjSet))
+    if args.config == "stack":
+        Set = StackSet
+    if args.config == "moe_gather":
+        Set = MoeGatherSet
     first = Set(wl, th, rd, torch)
     nsets = max(1, int(np.ceil(3 * L2_BYTES / first.bytes)))
     if is_embed:
@@ -500,7 +609,14 @@ def run_ours(args, rank, world, local_rank):
         peak, unit = hbm, "GB/s"
     else:
         achieved = algo_flops / avg_call_s / 1e12
-        peak, unit = tf_burst, "TFLOP/s"
+        # a contraction timed over a long back-to-back loop runs in the
+        # power-capped regime the sustained figure was measured in; a short
+        # one is compared with the burst figure
+        long_loop = elapsed_ms >= 100.0
+        peak, unit = (tf_sus if long_loop else tf_burst), "TFLOP/s"
+        peak_kind = (f"{peak_kind} sustained (timed region {elapsed_ms:.0f} ms of back-to-back calls; "
+                     f"{achieved / tf_burst:.3f} of the burst {tf_burst})" if long_loop else
+                     f"{peak_kind} burst")
     if is_embed:
         kernel = "embed_kernel"
     else:
@@ -539,8 +655,8 @@ def run_ours(args, rank, world, local_rank):
             "frac": achieved / peak, "traffic": traffic,
             "kernel": f"{kernel} (timed as the whole call: routing sort + {kernel}, graph replay)",
             "algorithmic_bytes_per_call": algo_bytes, "algorithmic_flops_per_call": algo_flops,
-            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" else
-                           "fallback",
+            "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind.startswith("measured") else
+                            f"{peak_kind} (MEASURED_PEAKS.json absent)"),
             "call_us": call_ms * 1e3,
         },
         "status_flags": status,
@@ -557,13 +673,19 @@ def oracle_rate(wl, config, budget_s=12.0, cap_s=30.0):
     import oracle
     oracle.build()
     is_moe = config == "moe"
-    rows_total = wl.T if is_moe else wl.M
+    rows_total = wl.T if config in ("moe", "moe_gather") else wl.M
     if config in EMBED_ROWS:
         def fn(w, rows):
             return oracle.embed(w.tokens[rows], w.E, w.seq_slot[rows], w.adapters)
     elif config in GATE_UP:
         def fn(w, rows):
             return oracle.gate_up(w.x, w.W, w.seq_slot, w.adapters, rows=rows)
+    elif config == "stack":
+        def fn(w, rows):
+            return oracle.proj_stack(w.x, w.W, w.seq_slot, w.stacks, rows=rows)
+    elif config == "moe_gather":
+        def fn(w, rows):  # the sampled slot-rows (the fp32 combine of pairs is left out)
+            return oracle.moe_gather(w.x[rows], w.W, w.indices[rows], w.seq_slot[rows], w.adapters)
     else:
         fn = oracle.workload_moe if is_moe else oracle.workload_proj
     # calibrate on a few rows, then size the sample to ~budget_s
@@ -605,7 +727,7 @@ def run_reference(args, rank, world):
                           cap_s=max(4.0, 90.0 / max(1, args.steps)))
         per.append(cpu["value"])
     value = float(np.median(per))
-    rows = wl.T if args.config == "moe" else wl.M
+    rows = wl.T if args.config in ("moe", "moe_gather") else wl.M
     cpu["value"] = value
     out = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,

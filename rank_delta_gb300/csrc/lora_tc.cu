@@ -72,11 +72,13 @@ constexpr int MAX_STAGES = 8;
 constexpr uint32_t W_CHUNK_BYTES = TC_BM * 64 * 2;
 constexpr uint32_t XB_BLOCK = TC_BM * 128; // 64 k of 128 B rows, 128 rows
 constexpr int LR_MAX_L = 64;               // slots a launch may have for local routing
+constexpr int TC_TGROUP = 8;               // token tiles per group of the grouped tile order
 
 struct TcCfg {
     int tn, kc, stages, csplit;
     int n_tiles;      // ceil(N / 128)
     int static_tiles; // total tiles when the host knows them, -1 when the prep kernel lists them
+    int tgroup;       // token tiles walked together per feature tile (L2 reuse of W), 1 = row-major
     int kchunks, kstages;
     int use3d;
     int xblk;         // 64-wide k blocks of one expand round (dedicated buffers, region 0)
@@ -153,7 +155,18 @@ __device__ __forceinline__ bool get_tile(const Params &p, const TcCfg &c, int ti
 {
     if (tile >= total)
         return false;
-    const int tt = tile / c.n_tiles, nt = tile % c.n_tiles;
+    int tt = tile / c.n_tiles, nt = tile % c.n_tiles;
+    if (c.static_tiles >= 0 && c.tgroup > 1) {
+        // grouped order: consecutive tiles cycle over tgroup token tiles for
+        // one feature tile, then move to the next feature tile, so the CTAs
+        // of one wave share each W tile among several token tiles in L2
+        const int ntt = c.static_tiles / c.n_tiles;
+        const int span = c.tgroup * c.n_tiles;
+        const int g = tile / span, within = tile - g * span;
+        const int gt = min(c.tgroup, ntt - g * c.tgroup);
+        tt = g * c.tgroup + within % gt;
+        nt = within / gt;
+    }
     ti.n0 = nt * TC_BM;
     if (c.static_tiles >= 0) {
         ti.e = 0;
@@ -1026,7 +1039,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // warm L2 with what the epilogue reads first: its first tile's slots
         // and the slot tables (one line of 32 entries per thread)
         const int et = threadIdx.x - (TC_THREADS - EPI_THREADS);
-        const int r0 = (blockIdx.x / c.csplit) / c.n_tiles * c.tn;
+        TileInfo t0;
+        const int r0 = get_tile(p, c, blockIdx.x / c.csplit, c.static_tiles, t0) ? t0.r0 : 0;
         if (et < c.tn && r0 + et < p.rows && (et & 31) == 0)
             prefetch_l2(p.seq_slot + r0 + et);
         for (int s = et * 32; s < p.L; s += EPI_THREADS * 32) {
@@ -1118,6 +1132,7 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
     c.xblk_b = (int)min(8u, (uint32_t)c.stages * c.stage_bytes / (XB_BLOCK + (uint32_t)c.hl * (uint32_t)c.tn * 128u));
     const int tt = (p.rows + c.tn - 1) / c.tn;
     c.static_tiles = dyn ? -1 : tt * c.n_tiles;
+    c.tgroup = (!dyn && tt > 1) ? (tt < TC_TGROUP ? tt : TC_TGROUP) : 1;
     return c;
 }
 

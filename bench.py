@@ -573,30 +573,72 @@ def run_ours(args, rank, world, local_rank):
     value = job_rate(rows, args.steps, world, elapsed_ms)
     status = rd.lora_status_get(sets[0].ws)
 
-    # end to end through the C ABI: pinned host x (tokens for the embedding) /
-    # seq_slot in, y out, every step
+    # end to end through the C ABI: every step copies its own inputs (pinned
+    # host x -- tokens for the embedding -- and seq_slot) to the device, makes
+    # the call, and reads its result back to pinned host memory. The copies of
+    # step i+1 and the read-back of step i run on their own streams beside the
+    # call of step i (buffer set i % nsets; events order each set's reuse), as
+    # a serving loop would overlap them.
+    # input/output buffers of the steps in flight: at least two, so that one
+    # step's copies can overlap another's call even with one weight set
+    nio = max(2, nsets)
     x_h = sets[0].x.cpu().pin_memory()
     s_h = sets[0].slots.cpu().pin_memory()
-    y_h = torch.empty(sets[0].y.shape, dtype=torch.bfloat16).pin_memory()
-    xs = [torch.empty_like(s.x) for s in sets]
-    ss = [torch.empty_like(s.slots) for s in sets]
-    for i in range(args.warmup):
-        k = i % nsets
-        xs[k].copy_(x_h, non_blocking=True)
-        ss[k].copy_(s_h, non_blocking=True)
-        sets[k].step(wl, rd, stream, x=xs[k], slots=ss[k])
-        y_h.copy_(sets[k].y, non_blocking=True)
+    y_hs = [torch.empty(sets[0].y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(nio)]
+    xs = [torch.empty_like(sets[0].x) for _ in range(nio)]
+    ss = [torch.empty_like(sets[0].slots) for _ in range(nio)]
+    ys = [torch.empty_like(sets[0].y) for _ in range(nio)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_ev = [torch.cuda.Event() for _ in range(nio)]
+    comp_ev = [torch.cuda.Event() for _ in range(nio)]
+    out_ev = [torch.cuda.Event() for _ in range(nio)]
+
+    def e2e_steps(n, main):
+        for i in range(n):
+            k, j = i % nsets, i % nio
+            with torch.cuda.stream(s_in):
+                if i >= nio:
+                    s_in.wait_event(comp_ev[j])  # step i - nio has read xs[j], ss[j]
+                xs[j].copy_(x_h, non_blocking=True)
+                ss[j].copy_(s_h, non_blocking=True)
+                in_ev[j].record(s_in)
+            main.wait_event(in_ev[j])
+            if i >= nio:
+                main.wait_event(out_ev[j])  # step i - nio's y is back on the host
+            sets[k].step(wl, rd, main, x=xs[j], slots=ss[j], y=ys[j])
+            comp_ev[j].record(main)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_ev[j])
+                y_hs[j].copy_(ys[j], non_blocking=True)
+                out_ev[j].record(s_out)
+
+    # eager warm-up, then the K steps as one CUDA graph (copy nodes from and to
+    # pinned host memory, the calls' kernels), replayed once untimed and once
+    # timed, so the host's enqueue rate does not set the number
+    with torch.cuda.stream(cap):
+        s_in.wait_stream(cap)
+        s_out.wait_stream(cap)
+        e2e_steps(args.warmup, cap)
+        cap.wait_stream(s_in)
+        cap.wait_stream(s_out)
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=cap):
+        main = torch.cuda.current_stream()
+        s_in.wait_stream(main)
+        s_out.wait_stream(main)
+        e2e_steps(args.steps, main)
+        main.wait_stream(s_in)
+        main.wait_stream(s_out)
+    with torch.cuda.stream(cap):
+        g2.replay()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        k = i % nsets
-        xs[k].copy_(x_h, non_blocking=True)
-        ss[k].copy_(s_h, non_blocking=True)
-        sets[k].step(wl, rd, stream, x=xs[k], slots=ss[k])
-        y_h.copy_(sets[k].y, non_blocking=True)
-    e1.record(stream)
+    with torch.cuda.stream(cap):
+        e0.record(cap)
+        g2.replay()
+        e1.record(cap)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
     e2e_value = job_rate(rows, args.steps, world, e2e_ms)
@@ -648,7 +690,10 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "rows/s",
                 "h2d_bytes_per_step": int(x_h.numel() * x_h.element_size() + s_h.numel() * 4),
-                "d2h_bytes_per_step": int(y_h.numel() * 2)},
+                "d2h_bytes_per_step": int(y_hs[0].numel() * 2),
+                "how": "one CUDA graph of the K steps: each step copies its own inputs from pinned host "
+                       "memory and reads its result back to pinned host memory, the copies on two streams "
+                       "beside the neighbouring calls"},
         "gpu_launches": launches_per_call(args.config, rows, kernel) * args.steps,
         "roofline": {
             "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,

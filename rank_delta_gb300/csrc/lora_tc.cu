@@ -33,12 +33,14 @@
 // k range exceeds the buffers, the expand runs in several rounds.
 //
 // Warp roles (256 threads):
-//   warps 0, 1   TMA producers of W (even / odd pipeline stages): 3D boxes
-//                [kc chunks][128 rows][64] so one copy brings kc K-slices;
-//   warp  2      allocates TMEM and issues the UMMAs from one elected thread;
-//   warp  3      TMA producer of x;
-//   warps 4..7   first run their share of the shrink work units (h = A_s x,
-//                shrink.cuh), then per item stage the expand operands and
+//   warp  0      TMA producer of W and x (3D boxes [kc chunks][128 rows][64],
+//                so one copy brings kc K-slices);
+//   warp  1      allocates TMEM and issues the UMMAs from one elected thread;
+//   warps 2, 3   one-tile launches: run this CTA's shrink work units (h = A_s x,
+//                shrink.cuh, two warps per unit) once the epilogue has sorted
+//                the rows, while the epilogue goes on;
+//   warps 4..7   (other launches: first run their share of the shrink units),
+//                then per item stage the expand operands and
 //                drain TMEM (warp w reads TMEM lanes 32(w-4)..+31), rounding
 //                once to bf16 (spark_model `layers/ops/lora_delta.rs`: the fold
 //                fused with the base product instead of a scaled-add pass over
@@ -188,11 +190,11 @@ __device__ __forceinline__ void flag_abort(const Params &p, Bars *bars)
 
 __device__ __forceinline__ bool aborted(Bars *bars) { return *(volatile int *)&bars->abort_flag != 0; }
 
-// TMA producer of W (par = 0 / 1: even / odd pipeline stages) or of x (par = -1).
+// TMA producer of the pipeline: for every stage, the W box and the x box of
+// its K chunks, both counted on the stage's full barrier.
 __device__ __forceinline__ void produce(const TmapSet &maps, const Params &p, const TcCfg &c, Bars *bars,
-                                        uint8_t *smem, int par)
+                                        uint8_t *smem)
 {
-    const bool is_x = par < 0;
     if (c.static_tiles < 0)
         grid_dependency_wait();
     const int total = item_total(p, c);
@@ -205,8 +207,6 @@ __device__ __forceinline__ void produce(const TmapSet &maps, const Params &p, co
         const int part = w % c.csplit;
         const int ks0 = part * c.kstages / c.csplit, ks1 = (part + 1) * c.kstages / c.csplit;
         for (int ks = ks0; ks < ks1; ++ks, ++g) {
-            if (!is_x && (g & 1) != par)
-                continue;
             const int slot = g % c.stages;
             const uint32_t ph = (uint32_t)(g / c.stages) & 1u;
             if (aborted(bars) || !mbar_wait(bars->empty + slot, ph ^ 1u)) {
@@ -214,19 +214,14 @@ __device__ __forceinline__ void produce(const TmapSet &maps, const Params &p, co
                 goto drain;
             }
             uint8_t *stage = smem + (size_t)slot * c.stage_bytes;
-            if (is_x) {
-                mbar_arrive_expect_tx(bars->full + slot, (uint32_t)c.kc * c.x_chunk);
-                uint8_t *dst = stage + (size_t)c.kc * W_CHUNK_BYTES;
-                if (c.use3d)
-                    tma_load_3d(dst, &maps.x, 0, ti.r0, ks * c.kc, bars->full + slot);
-                else
-                    tma_load_2d(dst, &maps.x, ks * 64, ti.r0, bars->full + slot);
+            mbar_arrive_expect_tx(bars->full + slot, (uint32_t)c.kc * (W_CHUNK_BYTES + c.x_chunk));
+            uint8_t *xdst = stage + (size_t)c.kc * W_CHUNK_BYTES;
+            if (c.use3d) {
+                tma_load_3d(stage, &maps.w[ti.e], 0, ti.n0, ks * c.kc, bars->full + slot);
+                tma_load_3d(xdst, &maps.x, 0, ti.r0, ks * c.kc, bars->full + slot);
             } else {
-                mbar_arrive_expect_tx(bars->full + slot, (uint32_t)c.kc * W_CHUNK_BYTES);
-                if (c.use3d)
-                    tma_load_3d(stage, &maps.w[ti.e], 0, ti.n0, ks * c.kc, bars->full + slot);
-                else
-                    tma_load_2d(stage, &maps.w[ti.e], ks * 64, ti.n0, bars->full + slot);
+                tma_load_2d(stage, &maps.w[ti.e], ks * 64, ti.n0, bars->full + slot);
+                tma_load_2d(xdst, &maps.x, ks * 64, ti.r0, bars->full + slot);
             }
             last_parity[slot] = (int)ph;
         }
@@ -410,6 +405,7 @@ __device__ __forceinline__ void split_hi_lo(float v, uint32_t &hi, uint32_t &lo)
 }
 
 constexpr int UNIT_BATCH = 64; // shrink units whose metadata is built at once
+constexpr int SHRINK_GROUP_THREADS = 64; // warps 2 and 3
 
 // This CTA's share of the shrink work units (h = A_s x, shrink.cuh): the
 // metadata of up to UNIT_BATCH units is built in parallel (one thread each:
@@ -591,6 +587,42 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
     }
 }
 
+// Shrink warps (warps 2 and 3) of one-tile launches: once the epilogue has
+// sorted the tile's rows by slot (named barrier 3), they run this CTA's
+// shrink units -- two warps per unit splitting its K part -- while the
+// epilogue assigns slots to K parts and stages the B rows; after the routing
+// kernel has finished (it clears the counters) each unit's bucket counter is
+// bumped. Named barrier 4 tells the epilogue the sort tables are free again.
+__device__ __forceinline__ void shrink_warps(const Params &p, const TcCfg &c, uint8_t *smem)
+{
+    const int st = threadIdx.x - 64; // 0..63
+    const EpiAux *aux = reinterpret_cast<const EpiAux *>(smem + c.aux_off);
+    float *red = reinterpret_cast<float *>(smem + c.red_off);
+    UnitMeta *um = reinterpret_cast<UnitMeta *>(smem + c.umeta_off);
+    named_bar_sync(3, SHRINK_GROUP_THREADS + EPI_THREADS);
+    const int tu = aux->lr_uoff[p.L];
+    const int mine = tu > (int)blockIdx.x ? (tu - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+    bool routed = false;
+    for (int k0 = 0; k0 < mine; k0 += UNIT_BATCH) {
+        const int nk = min(UNIT_BATCH, mine - k0);
+        if (st < nk)
+            um[st] = lr_unit_meta(p, aux, (int)blockIdx.x + (k0 + st) * (int)gridDim.x, 0);
+        named_bar_sync(2, SHRINK_GROUP_THREADS);
+        for (int k = 0; k < nk; ++k)
+            shrink_unit<2>(p, um[k], st >> 5, st & 31, red, 2);
+        __threadfence();
+        named_bar_sync(2, SHRINK_GROUP_THREADS);
+        if (!routed) {
+            grid_dependency_wait();
+            routed = true;
+        }
+        if (st < nk)
+            atomicAdd(p.ws.done + um[st].b, 1);
+        named_bar_sync(2, SHRINK_GROUP_THREADS); // um is rewritten by the next batch
+    }
+    named_bar_arrive(4, SHRINK_GROUP_THREADS + EPI_THREADS);
+}
+
 // Per item: which columns take their delta here (adapted rows whose slot the
 // rank-balanced assignment gives to this K part) and the k offset of each such
 // slot; stage the
@@ -631,7 +663,7 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         route_wait();
 
     const int total = item_total(p, c);
-    bool shrink_done = false;
+    bool shrink_done = false, grp_joined = false;
     int it = 0, xg[2] = {0, 0};
     TileInfo ti;
     for (int w = blockIdx.x; w < total && get_tile(p, c, w / c.csplit, total, ti); w += gridDim.x, ++it) {
@@ -642,6 +674,10 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         const Tables &tab = p.tab[ti.e];
         const int nmma = (ti.cnt + 15) & ~15;
 
+        if (c.local_route && it == 1) {
+            named_bar_sync(4, SHRINK_GROUP_THREADS + EPI_THREADS); // the shrink warps are done with lr_*
+            grp_joined = true;
+        }
         // (1) the columns whose delta this part adds, and the slots they use
         for (int q = et; q < p.L; q += EPI_THREADS)
             aux->soff[q] = 0;
@@ -672,9 +708,10 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         named_bar_sync(1, EPI_THREADS);
         if (c.local_route && !shrink_done) {
             // (1a) every row of the launch is in this tile: sort them by slot
-            // here (stable, so every CTA builds the same shrink work list) and
-            // run this CTA's units without waiting for the routing kernel; only
-            // the counter updates wait for it (it clears the counters).
+            // here (stable, so every CTA builds the same shrink work list); the
+            // shrink warps run this CTA's units from this sort without waiting
+            // for the routing kernel (only their counter updates wait for it:
+            // it clears the counters).
             int u_s = 0, c_s = 0;
             if (et < p.L) {
                 c_s = aux->lr_cnt[et];
@@ -712,24 +749,8 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
                                                 aux->lr_wcnt[2][et] + aux->lr_wcnt[3][et]);
                 named_bar_sync(1, EPI_THREADS);
             }
-            // this CTA's units, first of all the item's work (their loads
-            // should not queue behind the B copies)
-            const int mine = tu > (int)blockIdx.x ? (tu - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
-            for (int k0 = 0; k0 < mine; k0 += UNIT_BATCH) {
-                const int nk = min(UNIT_BATCH, mine - k0);
-                if (et < nk)
-                    um[et] = lr_unit_meta(p, aux, (int)blockIdx.x + (k0 + et) * (int)gridDim.x, ti.r0);
-                named_bar_sync(1, EPI_THREADS);
-                for (int k = 0; k < nk; ++k)
-                    shrink_unit(p, um[k], ew, et & 31, red, 1);
-                __threadfence();
-                named_bar_sync(1, EPI_THREADS);
-                if (!routed)
-                    route_wait();
-                if (et < nk)
-                    atomicAdd(p.ws.done + um[et].b, 1);
-                named_bar_sync(1, EPI_THREADS); // um is rewritten by the next batch
-            }
+            // the sort is done: the shrink warps run this CTA's units from here
+            named_bar_arrive(3, SHRINK_GROUP_THREADS + EPI_THREADS);
             shrink_done = true;
         }
         const int per = (p.L + EPI_THREADS - 1) / EPI_THREADS;
@@ -996,6 +1017,8 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
             route_wait();
         epi_shrink(p, unit_off, seg_off, red, um, et);
     }
+    if (c.local_route && !grp_joined && shrink_done)
+        named_bar_sync(4, SHRINK_GROUP_THREADS + EPI_THREADS);
 }
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -1013,7 +1036,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int i = 0; i < c.stages; ++i) {
-            mbar_init(bars->full + i, 2); // the W copy and the x copy of a stage
+            mbar_init(bars->full + i, 1); // one arrival; the W and x copies are counted in bytes
             mbar_init(bars->empty + i, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -1033,7 +1056,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         for (int e = 0; e < p.E; ++e)
             prefetch_tmap(&maps.w[e]);
     }
-    if (warp == 2)
+    if (warp == 1)
         tmem_alloc(&bars->tmem_base, c.tmem_cols);
     if (warp >= 4 && c.static_tiles >= 0) {
         // warm L2 with what the epilogue reads first: its first tile's slots
@@ -1055,22 +1078,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp < 2) {
+    if (warp == 0) {
         if (lane == 0)
-            produce(maps, p, c, bars, smem, warp);
-    } else if (warp == 3) {
-        if (lane == 0)
-            produce(maps, p, c, bars, smem, -1);
-    } else if (warp == 2) {
+            produce(maps, p, c, bars, smem);
+    } else if (warp == 1) {
         if (lane == 0)
             issue_mma(p, c, bars, smem, tmem);
+    } else if (warp < 4) {
+        if (c.local_route)
+            shrink_warps(p, c, smem);
     } else {
         epilogue(p, c, bars, smem, tmem);
         tc_fence_before();
         mbar_arrive(&bars->epi_done);
     }
     __syncwarp();
-    if (warp == 2) {
+    if (warp == 1) {
         // TMEM is freed only once the epilogue warps are done reading it
         mbar_wait(&bars->epi_done, 0);
         tc_fence_after();

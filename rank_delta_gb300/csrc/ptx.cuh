@@ -286,6 +286,12 @@ __device__ __forceinline__ void grid_dependency_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Arrive on named barrier `id` (of `count` threads) without waiting.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
 {

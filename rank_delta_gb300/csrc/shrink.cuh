@@ -2,7 +2,8 @@
 // `LoraDelta::project`), as work units over the routing sort.
 //
 // A unit is (bucket b, rank group of 8, up to 4 rows of that bucket, one of
-// kp parts of K): four warps splitting the K part, lanes taking 8-element
+// kp parts of K): a group of warps splitting the K part (four in the shrink
+// kernel and the epilogue, two in the projection kernel's shrink warps), lanes taking 8-element
 // (16-byte) vectors, each lane accumulating 8 ranks x 4 rows. A slot's A rows
 // are read once per 4 rows rather than once per row. Part q writes its
 // partial sums to h[q][row][r] (fp32); readers add the kp parts in part
@@ -110,12 +111,13 @@ __device__ __forceinline__ UnitMeta unit_meta(const Params &p, int u, const int3
     return m;
 }
 
-// Unit m, executed by SHRINK_WARPS warps (w = 0..3) of one group that shares
-// named barrier `bar_id` and the float scratch `red` [SHRINK_WARPS][32]: the
-// warps split the unit's K part in four, each lane accumulating 8 ranks x 4
-// rows over its 8-element K slices so every load of a pass is in flight at
-// once; lane sums are reduce-scattered, then the four warps' sums are added
-// (warp order) and written to h.
+// Unit m, executed by NW warps (w = 0..NW-1) of one group that shares named
+// barrier `bar_id` and the float scratch `red` [NW][32]: the warps split the
+// unit's K part NW ways, each lane accumulating 8 ranks x 4 rows over its
+// 8-element K slices so every load of a pass is in flight at once; lane sums
+// are reduce-scattered, then the warps' sums are added (warp order) and
+// written to h.
+template <int NW = SHRINK_WARPS>
 __device__ __forceinline__ void shrink_unit(const Params &p, const UnitMeta &m, int w, int lane,
                                             float *red, int bar_id)
 {
@@ -123,7 +125,7 @@ __device__ __forceinline__ void shrink_unit(const Params &p, const UnitMeta &m, 
     kpart_range(p.K, p.kp, m.kpart, kb, ke);
     // this warp's quarter of the K part, in whole 256-element steps
     const int steps = (ke - kb + 255) / 256;
-    const int s0 = kb + (steps * w / SHRINK_WARPS) * 256, s1 = min(ke, kb + (steps * (w + 1) / SHRINK_WARPS) * 256);
+    const int s0 = kb + (steps * w / NW) * 256, s1 = min(ke, kb + (steps * (w + 1) / NW) * 256);
     const uint16_t *arow[SHRINK_RG];
 #pragma unroll
     for (int r = 0; r < SHRINK_RG; ++r) {
@@ -157,17 +159,17 @@ __device__ __forceinline__ void shrink_unit(const Params &p, const UnitMeta &m, 
     }
     const float mine = warp_reduce_scatter32(acc, lane); // lane = rank * 4 + row
     red[w * 32 + lane] = mine;
-    named_bar_sync(bar_id, SHRINK_WARPS * 32);
+    named_bar_sync(bar_id, NW * 32);
     if (w == 0) {
         float t = red[lane];
 #pragma unroll
-        for (int q = 1; q < SHRINK_WARPS; ++q)
+        for (int q = 1; q < NW; ++q)
             t += red[q * 32 + lane];
         const int r = m.rg * SHRINK_RG + lane / 4, j = lane % 4;
         if (j < nr)
             hpart[(size_t)m.row[j] * p.R + r] = r < m.rank ? t : 0.0f;
     }
-    named_bar_sync(bar_id, SHRINK_WARPS * 32);
+    named_bar_sync(bar_id, NW * 32);
 }
 
 // h[row][r..r+8) summed over the kp parts (part order), for readers running

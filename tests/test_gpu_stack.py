@@ -143,3 +143,42 @@ def test_stack_large_batch_tensor_core_shrink():
     assert_close(y[rows], ref, "stack 2048 rows")
     none = wl.seq_slot < 0
     assert np.array_equal(y[none], run.base()[none])
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_stack_filling_the_pool_rank_with_odd_ranks(path):
+    """Members of ranks 3, 5 and 8 (16 = the pool rank) and 1 + 7 on another
+    slot: member boundaries off the 8-wide vectors, the pool rank used up."""
+    base = workloads.stacked(seed=9, M=40, K=512, N=384, L=3, R=16, zero_member_slot=-1)
+    rng = np.random.default_rng(1)
+
+    def member(r, sc):
+        A = workloads.f32_to_bf16(rng.uniform(-0.05, 0.05, (r, base.K)).astype(np.float32))
+        B = workloads.f32_to_bf16((rng.standard_normal((base.N, r)) * 0.1).astype(np.float32))
+        return workloads.Adapter(A, B, r, 2.0 * r, False, sc)
+
+    stacks = [[member(3, 1.0), member(5, 0.5), member(8, 1.0)], [member(1, 1.0), member(7, 0.5)],
+              [member(16, 1.0)]]
+    wl = workloads.StackWorkload("odd", 9, base.M, base.K, base.N, 3, 16, base.W, base.x, base.seq_slot, stacks)
+    run = StackRun(wl)
+    y = run.apply(path=path)
+    assert_close(y, oracle.proj_stack(wl.x, wl.W, wl.seq_slot, wl.stacks), "odd-rank stacks")
+
+
+def test_stack_replaces_a_single_adapter_in_place(stack64, stack64_ref):
+    """Packing a stack over a slot that held one adapter (and back) takes
+    effect for the applies enqueued after it."""
+    wl = stack64.wl
+    s0 = int(wl.seq_slot[wl.seq_slot >= 0][0])
+    rows = wl.seq_slot == s0
+    single = wl.stacks[s0][0]
+    try:
+        stack64.route.pack(s0, single)
+        y1 = stack64.apply(path=rd.LORA_PATH_TC)
+        one = [list(st) for st in wl.stacks]
+        one[s0] = [single]
+        assert_close(y1[rows], oracle.proj_stack(wl.x, wl.W, wl.seq_slot, one)[rows], "single in a stack slot")
+    finally:
+        stack64.route.pack_stack(s0, wl.stacks[s0])
+    y2 = stack64.apply(path=rd.LORA_PATH_TC)
+    assert_close(y2, stack64_ref, "stack packed again")

@@ -159,6 +159,24 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, u
     return r == CUDA_SUCCESS;
 }
 
+// Row-major bf16 [rows][inner] (row stride stride_elems) without swizzle,
+// for TMA stores of row-major boxes.
+bool make_map_plain(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows, uint64_t stride_elems,
+                    uint32_t box_inner, uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {stride_elems * 2};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 3D view [K/64 chunks][rows][64] of a K-major bf16 matrix (K a multiple of
 // 64): one box of box_chunks x box_rows x 64 brings several 64-wide K slices
 // of the same rows in one copy, each slice laid out as a 2D 128-byte-swizzled
@@ -658,6 +676,13 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
             if (!ok)
                 return fail(LORA_ERR_CUDA, "%s: encoding the W tensor map of expert %d failed", who, q);
         }
+        // y by TMA stores where its layout allows (16-byte aligned rows);
+        // otherwise the epilogue stores y element by element
+        p.ystore_ok = (!moe && aligned16(p.y) && p.y_stride % 8 == 0 &&
+                       make_map_plain(&maps.y, p.y, (uint64_t)p.N, (uint64_t)p.rows, (uint64_t)p.y_stride, 128,
+                                      (uint32_t)YSTORE_ROWS))
+                          ? 1
+                          : 0;
         e = launch_tc(p, maps, plan, st);
     }
     if (e != cudaSuccess)

@@ -77,6 +77,7 @@ struct Params {
     int ncnt; // split-K tile counters the prep kernel clears
     int no_units; // 1: h comes from the tensor-core shrink kernel (no shrink work units)
     int max_tiles; // token tiles the routing kernel may list (0: the workspace bound)
+    int ystore_ok; // 1: maps.y is encoded (y 16-byte aligned, y_stride a multiple of 8)
     const uint16_t *W[MAX_E];
     Tables tab[MAX_E];
     Ws ws;
@@ -120,7 +121,10 @@ inline WsLayout ws_layout(int rows, int nb, int R, int kp, size_t part_elems = 0
 struct TmapSet {
     CUtensorMap x;
     CUtensorMap w[MAX_E];
+    CUtensorMap y; // boxes of 128 features x YSTORE_ROWS rows of y, no swizzle (when ystore_ok)
 };
+// Rows of one TMA store of the tensor-core epilogue.
+constexpr int YSTORE_ROWS = 64;
 
 // Launchers (each defined next to its kernel). They return the launch error.
 cudaError_t launch_prep(const Params &p, cudaStream_t st);

@@ -88,6 +88,7 @@ struct TcCfg {
     int hl;           // XH planes: 1 (bf16) or 2 (hi + lo)
     int borrow;       // 1: no room for D' beside two accumulators; D' borrows the other one
     int local_route;  // 1: one token tile holds every row; each CTA sorts them itself for the shrink
+    int ystore;       // y boxes staged in the XH buffers: 0 = per-thread stores, else 1 or 2 buffers
     uint32_t x_chunk, stage_bytes;
     uint32_t xb_off, xh_off, aux_off, meta_off, red_off, umeta_off, bar_off, smem_bytes;
     uint32_t tmem_cols;
@@ -631,8 +632,8 @@ __device__ __forceinline__ void shrink_warps(const Params &p, const TcCfg &c, ui
 // them); then drain the accumulator (adding D' to those columns only), and
 // with csplit > 1 write the partial tile and, once every part is in, sum this
 // part's share of the columns in part order.
-__device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *bars, uint8_t *smem,
-                                         uint32_t tmem)
+__device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, const TcCfg &c, Bars *bars,
+                                         uint8_t *smem, uint32_t tmem)
 {
     const int et = threadIdx.x - (TC_THREADS - EPI_THREADS); // TMEM lane 0..127
     const int ew = et >> 5;
@@ -939,7 +940,29 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
             for (int j = 0; j < 16; ++j)
                 v[j] = (on16 >> j) & 1u ? __uint_as_float(rb[j]) + __uint_as_float(rdl[j])
                                         : __uint_as_float(rb[j]);
-            if (C == 1) {
+            if (C == 1 && c.ystore) {
+                // rows c0..c0+15 into the staging box (row-major [row][128
+                // features] bf16); a full box (or the tile's last rows) goes out
+                // as one TMA store, rows past the tensor clipped
+                const int sub = c0 % YSTORE_ROWS, bi = (c0 / YSTORE_ROWS) % c.ystore;
+                uint16_t *box = reinterpret_cast<uint16_t *>(XH) + (size_t)bi * YSTORE_ROWS * TC_BM;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    box[(sub + j) * TC_BM + et] = f32_to_bf16_bits(v[j]);
+                if (sub + 16 == YSTORE_ROWS || c0 + 16 >= ti.cnt) {
+                    fence_proxy_async_smem(); // generic-proxy writes, read by the TMA
+                    named_bar_sync(1, EPI_THREADS);
+                    if (et == 0) {
+                        tma_store_2d(&maps.y, box, ti.n0, ti.r0 + c0 - sub);
+                        bulk_commit();
+                        if (c.ystore == 1)
+                            bulk_wait_read<0>();
+                        else
+                            bulk_wait_read<1>(); // the other buffer is free again
+                    }
+                    named_bar_sync(1, EPI_THREADS);
+                }
+            } else if (C == 1) {
                 if (n < p.N) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
@@ -956,6 +979,8 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
         tc_fence_before();
         if (C > 1)
             __threadfence();
+        if (C == 1 && c.ystore && et == 0)
+            bulk_wait_read<0>(); // the XH buffers are staged again by the next item
         named_bar_sync(1, EPI_THREADS);
         if (et == 0) {
             mbar_arrive(bars->acc_empty + buf);
@@ -1019,6 +1044,8 @@ __device__ __forceinline__ void epilogue(const Params &p, const TcCfg &c, Bars *
     }
     if (c.local_route && !grp_joined && shrink_done)
         named_bar_sync(4, SHRINK_GROUP_THREADS + EPI_THREADS);
+    if (c.ystore && et == 0)
+        bulk_wait_all(); // the y stores have landed
 }
 
 __global__ void __launch_bounds__(TC_THREADS, 1)
@@ -1088,7 +1115,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (c.local_route)
             shrink_warps(p, c, smem);
     } else {
-        epilogue(p, c, bars, smem, tmem);
+        epilogue(maps, p, c, bars, smem, tmem);
         tc_fence_before();
         mbar_arrive(&bars->epi_done);
     }
@@ -1156,6 +1183,11 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
     const int tt = (p.rows + c.tn - 1) / c.tn;
     c.static_tiles = dyn ? -1 : tt * c.n_tiles;
     c.tgroup = (!dyn && tt > 1) ? (tt < TC_TGROUP ? tt : TC_TGROUP) : 1;
+    // y through TMA stores from the XH buffers (free while an item drains):
+    // one K part, tiles that end at the last row (static tiles), room for a box
+    const uint32_t xh_bytes = (uint32_t)c.hl * (uint32_t)c.xblk * (uint32_t)c.tn * 128u;
+    const uint32_t box_bytes = (uint32_t)YSTORE_ROWS * TC_BM * 2u;
+    c.ystore = (p.ystore_ok && !dyn && c.csplit == 1 && xh_bytes >= box_bytes) ? (xh_bytes >= 2 * box_bytes ? 2 : 1) : 0;
     return c;
 }
 

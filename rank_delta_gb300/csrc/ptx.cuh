@@ -172,6 +172,22 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
         : "memory");
 }
 
+// 2D tiled store of a shared-memory box to global memory (bulk group;
+// coordinates outside the tensor are not written).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(smem_u32(src))
+                 : "memory");
+}
+
+// Wait until at most N bulk groups of this thread still read shared memory.
+template <int N> __device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // 3D tiled load (c0 innermost); used with a [chunks][rows][64] view of a
 // K-major matrix so one copy brings several 64-wide K slices of the same rows.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int32_t c0, int32_t c1,

@@ -593,6 +593,7 @@ lora_status carve_ws(void *ws, size_t ws_bytes, int rows, int nb, int R, int kp,
     out.unit_off = reinterpret_cast<int32_t *>(b + l.unit_off);
     out.done = reinterpret_cast<int32_t *>(b + l.done);
     out.h = reinterpret_cast<float *>(b + l.h);
+    out.hs = reinterpret_cast<uint16_t *>(b + l.hs);
     out.tiles = reinterpret_cast<int32_t *>(b + l.tiles);
     out.part = reinterpret_cast<float *>(b + l.part);
     out.tile_cnt = reinterpret_cast<int32_t *>(b + l.tile_cnt);

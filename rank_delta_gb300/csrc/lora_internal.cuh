@@ -55,6 +55,7 @@ struct Ws {
     int32_t *unit_off;  // [nb + 1] first shrink unit of each bucket
     int32_t *done;      // [nb] finished shrink units per bucket
     float *h;           // [kp][rows][R] partial A_s x_i of every adapted row (fp32)
+    uint16_t *hs;       // [rows][R] bf16 of (s * comp[r]) * h, written by the tensor-core shrink
     int32_t *tiles;     // [1 + 3*max_tiles]: count, then (expert, first row, rows) per token tile
     float *part;        // [tiles][csplit][tn][128] split-K partial tiles (fp32)
     int32_t *tile_cnt;  // [tiles] split-K parts written so far (zeroed by prep)
@@ -84,7 +85,7 @@ struct Params {
 };
 
 struct WsLayout {
-    size_t status, perm, seg_off, unit_off, done, h, tiles, part, tile_cnt, total;
+    size_t status, perm, seg_off, unit_off, done, h, hs, tiles, part, tile_cnt, total;
 };
 
 // Upper bound on token tiles: each expert adds at most one partial tile.
@@ -110,6 +111,7 @@ inline WsLayout ws_layout(int rows, int nb, int R, int kp, size_t part_elems = 0
     l.unit_off = o; o = align256(o + sizeof(int32_t) * (size_t)(nb + 1));
     l.done = o;     o = align256(o + sizeof(int32_t) * (size_t)nb);
     l.h = o;        o = align256(o + sizeof(float) * (size_t)kp * (size_t)rows * (size_t)R);
+    l.hs = o;       o = align256(o + sizeof(uint16_t) * (size_t)rows * (size_t)R);
     l.tiles = o;    o = align256(o + sizeof(int32_t) * (1 + 3 * (size_t)max_token_tiles(rows, nb)));
     l.part = o;     o = align256(o + sizeof(float) * part_elems);
     l.tile_cnt = o; o = align256(o + sizeof(int32_t) * (size_t)ncnt);

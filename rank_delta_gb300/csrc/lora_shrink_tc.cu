@@ -242,6 +242,11 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
                 const int i = li - grp * G; // this row's slot block in the group, if any
                 const int rank = li >= 0 ? sh->slot_rank[li] : 0;
                 float *hrow = p.ws.h + (size_t)(r0 + t) * p.R;
+                // the expand's bf16 operand (s * comp[r]) * h, rounded as the
+                // projection kernel would round it from h
+                uint16_t *hsrow = p.ws.hs + (size_t)(r0 + t) * p.R;
+                const float sc = sl >= 0 ? p.tab[0].scale_table[sl] : 0.0f;
+                const float *crow = p.tab[0].comp_table + (size_t)(sl >= 0 ? sl : 0) * LORA_COMP_STRIDE;
                 const bool skip = __any_sync(0xffffffffu, stc_aborted(sh)); // warp-uniform: the loads are collective
                 for (int c0 = 0; c0 < N && !skip; c0 += 16) {
                     float v[16];
@@ -254,6 +259,19 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
                                 *reinterpret_cast<float4 *>(hrow + r + q) =
                                     make_float4(r + q + 0 < rank ? v[q + 0] : 0.0f, r + q + 1 < rank ? v[q + 1] : 0.0f,
                                                 r + q + 2 < rank ? v[q + 2] : 0.0f, r + q + 3 < rank ? v[q + 3] : 0.0f);
+#pragma unroll
+                        for (int q = 0; q < 16; q += 8)
+                            if (r + q < p.R) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int e = 0; e < 8; e += 2) {
+                                    const float a = r + q + e < rank ? v[q + e] : 0.0f;
+                                    const float b = r + q + e + 1 < rank ? v[q + e + 1] : 0.0f;
+                                    w[e / 2] = (uint32_t)f32_to_bf16_bits(a * (sc * crow[r + q + e])) |
+                                               ((uint32_t)f32_to_bf16_bits(b * (sc * crow[r + q + e + 1])) << 16);
+                                }
+                                *reinterpret_cast<uint4 *>(hsrow + r + q) = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
                     }
                 }
                 tc_fence_before();

@@ -535,6 +535,18 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
         const float *cr = p.tab[ti.e].comp_table + (size_t)aux->cslot[j] * LORA_COMP_STRIDE;
         // ranks r (multiples of 8, r < rank) of this slot that fall in the pass
         const int rlo = max(0, r0k - ko), rhi = min(rk, r0k + kt - ko);
+        if (c.hl == 1 && p.no_units) {
+            // the tensor-core shrink wrote this operand already rounded to
+            // bf16 (ws.hs, zero past the rank): copy it in 16-byte chunks
+            const uint16_t *hsrow = p.ws.hs + (size_t)(ti.r0 + j) * p.R;
+            for (int r = rlo + 8 * sub; r < rhi; r += 8 * tpc) {
+                const int k = ko + r - r0k, rg = k >= d.kr0 ? 1 : 0, kl = k - (rg ? d.kr0 : 0);
+                const int cq = kl >> 3;
+                cp_async_16(d.xh[rg] + (uint32_t)(cq >> 3) * xh_block + j * 128 + (((cq & 7) ^ (j & 7)) << 4),
+                            hsrow + r, 16u);
+            }
+            continue;
+        }
         const float *hrow = p.ws.h + (size_t)(ti.r0 + j) * p.R;
         for (int r = rlo + 8 * sub; r < rhi; r += 32 * tpc) {
             float4 a[4], b[4], ca[4], cb[4];

@@ -679,7 +679,7 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
         }
         // y by TMA stores where its layout allows (16-byte aligned rows);
         // otherwise the epilogue stores y element by element
-        p.ystore_ok = (!moe && aligned16(p.y) && p.y_stride % 8 == 0 &&
+        p.ystore_ok = (aligned16(p.y) && p.y_stride % 8 == 0 &&
                        make_map_plain(&maps.y, p.y, (uint64_t)p.N, (uint64_t)p.rows, (uint64_t)p.y_stride, 128,
                                       (uint32_t)YSTORE_ROWS))
                           ? 1

@@ -962,17 +962,27 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
                 for (int j = 0; j < 16; ++j)
                     box[(sub + j) * TC_BM + et] = f32_to_bf16_bits(v[j]);
                 if (sub + 16 == YSTORE_ROWS || c0 + 16 >= ti.cnt) {
-                    fence_proxy_async_smem(); // generic-proxy writes, read by the TMA
-                    named_bar_sync(1, EPI_THREADS);
-                    if (et == 0) {
-                        tma_store_2d(&maps.y, box, ti.n0, ti.r0 + c0 - sub);
-                        bulk_commit();
-                        if (c.ystore == 1)
-                            bulk_wait_read<0>();
-                        else
-                            bulk_wait_read<1>(); // the other buffer is free again
+                    const int brows = min(YSTORE_ROWS, ti.cnt - (c0 - sub));
+                    if (brows < YSTORE_ROWS && c.static_tiles < 0) {
+                        // a tile of an expert segment: the rows past it belong to
+                        // the next segment, so this last box goes out element-wise
+                        // (each thread its own feature column)
+                        if (n < p.N)
+                            for (int rr = 0; rr < brows; ++rr)
+                                p.y[(int64_t)(ti.r0 + c0 - sub + rr) * p.y_stride + n] = box[rr * TC_BM + et];
+                    } else {
+                        fence_proxy_async_smem(); // generic-proxy writes, read by the TMA
+                        named_bar_sync(1, EPI_THREADS);
+                        if (et == 0) {
+                            tma_store_2d(&maps.y, box, ti.n0, ti.r0 + c0 - sub);
+                            bulk_commit();
+                            if (c.ystore == 1)
+                                bulk_wait_read<0>();
+                            else
+                                bulk_wait_read<1>(); // the other buffer is free again
+                        }
+                        named_bar_sync(1, EPI_THREADS);
                     }
-                    named_bar_sync(1, EPI_THREADS);
                 }
             } else if (C == 1) {
                 if (n < p.N) {
@@ -1196,10 +1206,11 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
     c.static_tiles = dyn ? -1 : tt * c.n_tiles;
     c.tgroup = (!dyn && tt > 1) ? (tt < TC_TGROUP ? tt : TC_TGROUP) : 1;
     // y through TMA stores from the XH buffers (free while an item drains):
-    // one K part, tiles that end at the last row (static tiles), room for a box
+    // one K part and room for a box (expert tiles write a last partial box
+    // element-wise)
     const uint32_t xh_bytes = (uint32_t)c.hl * (uint32_t)c.xblk * (uint32_t)c.tn * 128u;
     const uint32_t box_bytes = (uint32_t)YSTORE_ROWS * TC_BM * 2u;
-    c.ystore = (p.ystore_ok && !dyn && c.csplit == 1 && xh_bytes >= box_bytes) ? (xh_bytes >= 2 * box_bytes ? 2 : 1) : 0;
+    c.ystore = (p.ystore_ok && c.csplit == 1 && xh_bytes >= box_bytes) ? (xh_bytes >= 2 * box_bytes ? 2 : 1) : 0;
     return c;
 }
 

@@ -6,12 +6,15 @@
 // bytes that bound these shapes -- streams through shared memory once.
 //
 // Work: items = (token tile, 128-feature tile, K part), spread over a grid
-// that never exceeds the SMs (every CTA resident). With csplit K parts, each
-// part writes its fp32 partial tile to the workspace (coalesced, L2-resident)
-// and bumps the tile's counter; once all parts are in, each part's CTA sums a
-// contiguous share of the columns in part order -- so every output element
-// is computed the same way whatever N is. Two TMEM accumulators let the
-// epilogue drain one item while the next accumulates.
+// that never exceeds the SMs (every CTA resident); several token tiles are
+// walked in groups of 8 per feature tile so a wave shares W tiles in L2.
+// With csplit K parts, each part writes its fp32 partial tile to the
+// workspace (coalesced, L2-resident) and bumps the tile's counter; once all
+// parts are in, each part's CTA sums a contiguous share of the columns in
+// part order -- so every output element is computed the same way whatever N
+// is. With one part, y leaves in 64-row bf16 boxes staged in the free XH
+// buffers and written by TMA stores. Two TMEM accumulators let the epilogue
+// drain one item while the next accumulates.
 //
 // The expand-fold runs on the tensor cores too. Each adapted slot of a tile
 // is owned by one K part (slots sorted by padded rank, largest first, dealt

@@ -506,24 +506,31 @@ __device__ __forceinline__ void stage_b(const Params &p, const EpiAux *aux, cons
 
 // XH rows 0..nmma-1 of the pass [r0k, r0k + kr0 + kr1): s_t * h_t in column
 // t's slot range (hi, and lo = the bf16 remainder when hl = 2), zero
-// elsewhere. First every chunk of the pass is zeroed; then each column's data
-// chunks are split over 128 / nmma threads, each issuing the loads of up to
-// four chunks (every K part of h) before converting any.
-__device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const EpiAux *aux, const XDst &d,
-                                        const TileInfo &ti, int nmma, int r0k, int et)
+// elsewhere (zero_xh has zeroed every chunk of the pass before). Each
+// column's data chunks are split over 128 / nmma threads, each issuing the
+// loads of up to four chunks (every K part of h) before converting any.
+// Zero the XH chunks of one staging region of the pass (rows 0..nmma-1,
+// every plane), before any of s * h is written: it needs nothing but the
+// region being free, so region 0 is zeroed while the shrink is still running.
+__device__ __forceinline__ void zero_xh(const TcCfg &c, const XDst &d, int rg, int nmma, int et)
 {
     const uint32_t xh_block = (uint32_t)c.tn * 128u;
-    const int nch0 = ((d.kr0 + 63) >> 6) * 8, nch = nch0 + ((d.kr1 + 63) >> 6) * 8;
+    const int nch = (((rg ? d.kr1 : d.kr0) + 63) >> 6) * 8;
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int idx = et; idx < nmma * nch; idx += EPI_THREADS) {
-        const int j = idx / nch, cq = idx - j * nch;
-        const int rg = cq >= nch0 ? 1 : 0, cl = cq - (rg ? nch0 : 0);
+        const int j = idx / nch, cl = idx - j * nch;
         uint8_t *dst = d.xh[rg] + (uint32_t)(cl >> 3) * xh_block + j * 128 + (((cl & 7) ^ (j & 7)) << 4);
         *reinterpret_cast<uint4 *>(dst) = z;
         if (c.hl == 2)
             *reinterpret_cast<uint4 *>(dst + d.plane[rg]) = z;
     }
-    named_bar_sync(1, EPI_THREADS);
+}
+
+__device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const EpiAux *aux, const XDst &d,
+                                        const TileInfo &ti, int nmma, int r0k, int et)
+{
+    const uint32_t xh_block = (uint32_t)c.tn * 128u;
+    named_bar_sync(1, EPI_THREADS); // the zeroed chunks (zero_xh, any thread) before the data
     const int kt = d.kr0 + d.kr1;
     const size_t part_stride = (size_t)p.rows * p.R;
     // tpc threads per column (a power of two), each taking every tpc-th chunk
@@ -877,8 +884,10 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
                     flag_abort(p, bars);
                 named_bar_sync(1, EPI_THREADS);
             }
-            if (d.kr0 > 0)
+            if (d.kr0 > 0) {
                 stage_b(p, aux, d, 0, d.kr0, nent, r0k, n, et);
+                zero_xh(c, d, 0, nmma, et);
+            }
             if (!shrink_done) {
                 if (!routed)
                     route_wait();
@@ -905,6 +914,7 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
                     flag_abort(p, bars);
                 named_bar_sync(1, EPI_THREADS);
                 stage_b(p, aux, d, d.kr0, d.kr0 + d.kr1, nent, r0k, n, et);
+                zero_xh(c, d, 1, nmma, et);
             }
             if (d.kr0 + d.kr1 > 0)
                 stage_h(p, c, aux, d, ti, nmma, r0k, et);

@@ -896,6 +896,13 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
             }
             if (!routed)
                 route_wait(); // the counters below are the routing kernel's
+            if (d.kr1 > 0) { // region 1: the stages are free once the base UMMAs are done
+                if (et == 0 && !mbar_wait(&bars->base_done, (uint32_t)it & 1u))
+                    flag_abort(p, bars);
+                named_bar_sync(1, EPI_THREADS);
+                stage_b(p, aux, d, d.kr0, d.kr0 + d.kr1, nent, r0k, n, et);
+                zero_xh(c, d, 1, nmma, et);
+            }
             if (pass == 0 && nent > 0) { // the shrink of the staged slots has finished
                 for (int e = et; e < nent; e += EPI_THREADS) {
                     const int b = ti.e * (p.L + 1) + aux->entry_slot[e] + 1;
@@ -908,13 +915,6 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
                     stop = true;
                     break;
                 }
-            }
-            if (d.kr1 > 0) { // region 1: the stages are free once the base UMMAs are done
-                if (et == 0 && !mbar_wait(&bars->base_done, (uint32_t)it & 1u))
-                    flag_abort(p, bars);
-                named_bar_sync(1, EPI_THREADS);
-                stage_b(p, aux, d, d.kr0, d.kr0 + d.kr1, nent, r0k, n, et);
-                zero_xh(c, d, 1, nmma, et);
             }
             if (d.kr0 + d.kr1 > 0)
                 stage_h(p, c, aux, d, ti, nmma, r0k, et);

@@ -1044,9 +1044,13 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
                 for (int jj = 0; jj < 8; ++jj)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        const int cc = min(col0 + 4 * jj, ce - 1), qq = min(q, C - 1); // clamped: in bounds
-                        acc[jj][q] = __ldcg(reinterpret_cast<const float4 *>(parts + qq * pstride +
-                                                                             (size_t)cc * EPI_THREADS) + quad);
+                        // only the parts and columns that exist are loaded
+                        const int cc = col0 + 4 * jj;
+                        acc[jj][q] = (q < C && cc < ce)
+                                         ? __ldcg(reinterpret_cast<const float4 *>(parts + q * pstride +
+                                                                                   (size_t)cc * EPI_THREADS) +
+                                                  quad)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
 #pragma unroll
                 for (int jj = 0; jj < 8; ++jj) {

@@ -118,43 +118,9 @@ template <int N> __device__ __forceinline__ void cp_async_wait_group()
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ------------------------------------------------------ bulk (untiled) copies
-// Add `bytes` to the transaction count of the barrier's current phase without
-// arriving (each thread that issues copies posts its own bytes).
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-// Contiguous global -> shared copy by the tensor memory accelerator; both
-// addresses 16-byte aligned, bytes a multiple of 16; completion counted on
-// `bar` in bytes.
-__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(smem_dst)),
-                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
-// Contiguous shared -> global copy (same alignment rules), tracked in this
-// thread's bulk groups.
-__device__ __forceinline__ void bulk_store(void *gdst, const void *smem_src, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-                 "r"(smem_u32(smem_src)), "r"(bytes)
-                 : "memory");
-}
-
+// ------------------------------------------------------------ bulk groups
+// Close this thread's current group of bulk (TMA) stores.
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// This thread's bulk stores have finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all()
-{
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 
 // This thread's bulk stores are complete (their writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -211,91 +177,7 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// ------------------------------------------------------- clusters / PDL
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %clusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t ncluster_x()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %nclusterid.x;" : "=r"(r));
-    return r;
-}
-
-// Shared-memory address of the same variable in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t local_smem, uint32_t rank)
-{
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem), "r"(rank));
-    return r;
-}
-
-// Arrive on an mbarrier of another CTA of the cluster, releasing this
-// thread's prior writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
-{
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar_addr, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar_addr), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait (acquire, cluster scope) for a barrier that other CTAs arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity)
-{
-    const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait_cluster(a, parity))
-        return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait_cluster(a, parity))
-            return true;
-        if ((i & 255u) == 0 && globaltimer_ns() - t0 > WAIT_NS)
-            return false;
-    }
-}
-
-__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t cluster_addr)
-{
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
-    return v;
-}
-
-// Whole-cluster barrier (every thread of every CTA in the cluster).
-__device__ __forceinline__ void cluster_sync_all()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_acq_rel_cluster()
-{
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-
+// ------------------------------------------------------------------ PDL
 // Programmatic dependent launch: wait for the preceding kernel's results.
 __device__ __forceinline__ void grid_dependency_wait()
 {

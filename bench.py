@@ -749,10 +749,22 @@ def oracle_rate(wl, config, budget_s=12.0, cap_s=30.0):
         el = time.perf_counter() - t
         if el >= min(budget_s, cap_s) or el + el / (done / n) > cap_s:
             break
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    omp = os.environ.get("OMP_NUM_THREADS")
-    threads = int(omp) if omp else cores
+    threads = oracle.max_threads()
+    # the same loops on one core, over a short sample of the same rows
+    oracle.set_threads(1)
+    try:
+        m = min(n, 2)
+        done1, t1 = 0, time.perf_counter()
+        while True:
+            fn(wl, rows=idx[:m])
+            done1 += m
+            el1 = time.perf_counter() - t1
+            if el1 >= min(3.0, budget_s / 4):
+                break
+    finally:
+        oracle.set_threads(threads)
     return {"value": done / el, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "single_core_value": done1 / el1,
             "sample": f"{n} of {rows_total} rows (all "
                       f"{wl.n_embd if config in EMBED_ROWS else (wl.N // 2 if config in GATE_UP else wl.N)} "
                       f"output columns each), "

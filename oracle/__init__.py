@@ -55,6 +55,10 @@ def _load():
         if _lib is None:
             build()
             lib = ctypes.CDLL(_SO)
+            lib.oracle_set_threads.restype = None
+            lib.oracle_set_threads.argtypes = [ctypes.c_int]
+            lib.oracle_max_threads.restype = ctypes.c_int
+            lib.oracle_max_threads.argtypes = []
             lib.oracle_scale.restype = ctypes.c_float
             lib.oracle_scale.argtypes = [ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_float]
             lib.oracle_slot_sort.restype = None
@@ -95,6 +99,15 @@ def _load():
 
 def _p(a: np.ndarray, t):
     return a.ctypes.data_as(t)
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's OpenMP loops (timing only; results do not depend on it)."""
+    _load().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
 
 
 def scale(alpha: float, rank: int, use_rslora: bool, adapter_scale: float) -> float:

@@ -31,6 +31,7 @@
  * byte identities, closed forms and worked examples under tests/golden/).
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -42,6 +43,16 @@ static float widen(uint16_t b)
     memcpy(&f, &u, sizeof f);
     return f;
 }
+
+/* Threads of the OpenMP loops below (timing only; the result does not
+ * depend on it: every output element is summed by one thread). */
+void oracle_set_threads(int n)
+{
+    if (n > 0)
+        omp_set_num_threads(n);
+}
+
+int oracle_max_threads(void) { return omp_get_max_threads(); }
 
 /* adapter_scale * (alpha / rank), or * (alpha / sqrt(rank)) under rsLoRA,
  * or adapter_scale alone when alpha is 0 ("absent").

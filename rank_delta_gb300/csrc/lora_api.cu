@@ -684,7 +684,7 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
                                       (uint32_t)YSTORE_ROWS))
                           ? 1
                           : 0;
-        e = launch_tc(p, maps, plan, st);
+        e = launch_tc(p, maps, plan, di.num_sms, st);
     }
     if (e != cudaSuccess)
         return cuda_fail(e, who);

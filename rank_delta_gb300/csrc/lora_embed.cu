@@ -842,14 +842,10 @@ bool embed_local_fits(int M, int ft, int R, int L)
 cudaError_t launch_embed(const EmbedParams &p, int num_sms, cudaStream_t st)
 {
     const EmbCfg c = make_embed_cfg(p.ft, p.R, p.L, p.local ? p.M : 0);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(embed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_LIMIT);
-        if (e != cudaSuccess)
-            return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> raised{0};
+    cudaError_t ea = raise_smem_limit(raised, embed_kernel, (int)SMEM_LIMIT);
+    if (ea != cudaSuccess)
+        return ea;
     // chunks at most: every non-empty bucket adds at most one partial chunk
     const long long nb = p.L + 1;
     const long long chunks = p.M / CH + (p.M < nb ? p.M : nb);

@@ -192,14 +192,10 @@ size_t gather_sort_smem(int T, int E) { return (size_t)((T + 3) & ~3) * 4 + (siz
 cudaError_t launch_gather_sort(const GatherParams &p, int num_sms, cudaStream_t st)
 {
     const size_t smem = gather_sort_smem(p.T, p.E);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(gather_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)gather_sort_smem(LORA_GATHER_MAX_ROWS, LORA_MAX_EXPERTS));
-        if (e != cudaSuccess)
-            return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> raised{0};
+    cudaError_t ea = raise_smem_limit(raised, gather_sort_kernel, (int)gather_sort_smem(LORA_GATHER_MAX_ROWS, LORA_MAX_EXPERTS));
+    if (ea != cudaSuccess)
+        return ea;
     int grid = p.T < 2 * num_sms ? p.T : 2 * num_sms;
     if (grid < 1)
         grid = 1;

@@ -1,5 +1,6 @@
 // Internal definitions shared by the host ABI (lora_api.cu) and the kernels.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -128,6 +129,27 @@ struct TmapSet {
 // Rows of one TMA store of the tensor-core epilogue.
 constexpr int YSTORE_ROWS = 64;
 
+// Raise a kernel's dynamic shared-memory limit on the current device. The
+// attribute belongs to the device's context, so a process driving several
+// GPUs raises it on each: `done` keeps one bit per device already raised.
+template <typename F>
+inline cudaError_t raise_smem_limit(std::atomic<uint64_t> &done, F *fn, int bytes)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= 64)
+        return cudaErrorInvalidDevice;
+    const uint64_t bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit)
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess)
+        done.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
 // Launchers (each defined next to its kernel). They return the launch error.
 cudaError_t launch_prep(const Params &p, cudaStream_t st);
 cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st);
@@ -146,7 +168,8 @@ struct TcPlan {
     int hl;   // planes of the staged s * h: 1 (bf16) or 2 (bf16 hi + lo)
 };
 TcPlan plan_tc(const Params &p, bool per_expert_tiles);
-cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, cudaStream_t st);
+cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, int num_sms,
+                      cudaStream_t st);
 cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, const void *b,
                              int rank, float factor, float scale, cudaStream_t st);
 cudaError_t launch_scale_set(const lora_route &rt, int slot, float adapter_scale, cudaStream_t st);

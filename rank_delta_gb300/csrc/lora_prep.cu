@@ -233,14 +233,10 @@ cudaError_t launch_prep(const Params &p, cudaStream_t st)
 {
     const int nb = p.E * (p.L + 1);
     const size_t smem = (size_t)nb * 16 + (size_t)32 * nb * 2;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)((size_t)MAX_BUCKETS * 16 + (size_t)32 * MAX_BUCKETS * 2));
-        if (e != cudaSuccess)
-            return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> raised{0};
+    cudaError_t ea = raise_smem_limit(raised, prep_kernel, (int)((size_t)MAX_BUCKETS * 16 + (size_t)32 * MAX_BUCKETS * 2));
+    if (ea != cudaSuccess)
+        return ea;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr.val.programmaticStreamSerializationAllowed = 1;

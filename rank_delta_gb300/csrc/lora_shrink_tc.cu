@@ -292,14 +292,10 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
 
 cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, int num_sms, cudaStream_t st)
 {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(shrink_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)STC_SMEM);
-        if (e != cudaSuccess)
-            return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> raised{0};
+    cudaError_t ea = raise_smem_limit(raised, shrink_tc_kernel, (int)STC_SMEM);
+    if (ea != cudaSuccess)
+        return ea;
     const int Rs = (p.R + 15) & ~15;
     const int ntiles = (p.rows + STC_M - 1) / STC_M;
     int grid = ntiles < num_sms ? ntiles : num_sms;

@@ -1294,35 +1294,20 @@ TcPlan plan_tc(const Params &p, bool dyn)
     return plan;
 }
 
-cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, cudaStream_t st)
+cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, int num_sms,
+                      cudaStream_t st)
 {
     const bool dyn = p.expert_offsets != nullptr;
     const TcCfg c = make_cfg(p, plan, dyn);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_LIMIT);
-        if (e != cudaSuccess)
-            return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> raised{0};
+    cudaError_t ea = raise_smem_limit(raised, tc_kernel, (int)SMEM_LIMIT);
+    if (ea != cudaSuccess)
+        return ea;
     if (c.smem_bytes > SMEM_LIMIT)
         return cudaErrorInvalidConfiguration;
     // One CTA per SM at most, so every CTA is resident (the in-launch waits
     // rely on it); never more CTAs than work items.
-    static int sms_cache[64];
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
-    if (sms_cache[dev] == 0) {
-        int sms = 0;
-        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess)
-            return e;
-        sms_cache[dev] = sms;
-    }
-    int grid = sms_cache[dev];
+    int grid = num_sms;
     if (c.static_tiles >= 0 && c.static_tiles * c.csplit < grid)
         grid = c.static_tiles * c.csplit;
     grid = grid / c.csplit * c.csplit;

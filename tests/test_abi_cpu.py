@@ -288,3 +288,16 @@ def test_pack_stack_refusals_name_the_problem():
            [0] * 2, [1.0] * 2, contains=("member 1",))
     emb = fake_route(kind=rd.LORA_ROUTE_EMBED)
     expect(rd.LORA_ERR_UNSUPPORTED, rd.lora_pool_pack_stack, emb, 0, [A], [B], [8], [16.0], [0], [1.0])
+
+
+def test_static_workspace_refuses_calls_that_outgrow_it():
+    rt = fake_route(L=16, R=64, K=4096, N=4096)
+    M = 20000
+    need = rd.lora_proj_workspace_bytes(M, rt)
+    assert need > rd.LORA_STATIC_WS_BYTES
+    msg = expect(rd.LORA_ERR_UNSUPPORTED, rd.lora_proj_apply_static_ws, 4096, 4096, 8192, M, 4096, 4096,
+                 4096, rt, 4096, 4096)
+    for part in (f"{M} rows", "max_rank 64", "16 slots", str(need), str(rd.LORA_STATIC_WS_BYTES)):
+        assert part in msg, (part, msg)
+    # the decode shapes fit the built-in array
+    assert rd.lora_proj_workspace_bytes(64, rt) <= rd.LORA_STATIC_WS_BYTES

@@ -643,6 +643,34 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
     e2e_value = job_rate(rows, args.steps, world, e2e_ms)
 
+    # per-call device times: one graph per buffer set holding a single call,
+    # each replay between two events on the launching stream, 100 replays
+    # after 3 untimed ones; the median and the minimum are reported beside the
+    # mean of the timed region (a failure here only drops these figures)
+    try:
+        one = []
+        for k in range(nsets):
+            g1 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g1, stream=cap):
+                sets[k].step(wl, rd, torch.cuda.current_stream())
+            one.append(g1)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(100)]
+        with torch.cuda.stream(cap):
+            for i in range(3):
+                one[i % nsets].replay()
+            for i, (a, b) in enumerate(evs):
+                a.record(cap)
+                one[i % nsets].replay()
+                b.record(cap)
+        torch.cuda.synchronize()
+        us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+        per_call = {"calls": len(us), "median_us": us[len(us) // 2], "min_us": us[0],
+                    "how": "one graph of a single call per buffer set, events around each replay "
+                           "(includes the graph's own launch gap, so above the mean of the K-step graph)"}
+    except Exception as ex:  # noqa: BLE001
+        per_call = {"error": f"{type(ex).__name__}: {ex}"[:200]}
+
     hbm, tf_burst, tf_sus, peak_kind = load_peaks()
     avg_call_s = call_ms / 1e3
     bound = BOUND[args.config]
@@ -703,6 +731,7 @@ def run_ours(args, rank, world, local_rank):
             "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind.startswith("measured") else
                             f"{peak_kind} (MEASURED_PEAKS.json absent)"),
             "call_us": call_ms * 1e3,
+            "per_call": per_call,
         },
         "status_flags": status,
     }

@@ -1,18 +1,26 @@
 #!/usr/bin/env python3
 """Benchmark of the multi-adapter LoRA projection on GB300.
 
-One step = one lora_proj_apply (or lora_moe_down_apply) call over one batch:
-the routing sort, the shrink, the base product and the fused expand-fold.
---config embed / embed_prefill time lora_embed_apply instead (the token
-embedding row gather with the adapted rows: routing sort + one launch).
-Default workload: the decode batch (64 rows, W [4096 x 4096] bf16, 16
-adapters of ranks {8,16,32,64} in a rank-64 pool, 10% rows without adapter).
+One step = one lora_proj_apply (or lora_moe_down_apply, ...) call over one
+batch: every kernel of the call (routing, shrink, base product, expand-fold).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+Default (--config suite): the headline is the prefill workload (8192 rows,
+W [14336 x 4096] bf16, 8 rank-64 rsLoRA adapters), the largest one; its
+timed region is exactly K steps, each a CUDA-graph replay of one call between
+its own pair of events, and value = rows / the median step time. Under
+"configs" the line carries prefill, decode, QKV and MoE (--extended: also the
+gated MLP input, the decode MoE gather, the stack and the embedding gather),
+each timed over max(K, 100) calls (median and min), beside the same calls
+with every slot -1 (the base product alone), an end-to-end rate through the
+C ABI with host copies, the roofline of the median call and the oracle on
+the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config suite|NAME] [--extended]
+                  [--impl ours|reference]
 
 N > 1 (under torchrun): every rank runs an independent replica on its own GPU
 (the projection shards by rows with no exchange); value = all ranks' rows /
-the slowest rank's time. Prints one JSON line on rank 0.
+the slowest rank's median step. Prints one JSON line on rank 0.
 """
 from __future__ import annotations
 
@@ -482,12 +490,248 @@ def make_workload(config, small=False):
     return workloads.make(config, **(SMALL.get(config, {}) if small else {}))
 
 
+SET_OF = {"moe": MoeSet, "stack": StackSet, "moe_gather": MoeGatherSet, "gate_up": GateUpSet,
+          "gate_up_decode": GateUpSet, "embed": EmbedSet, "embed_prefill": EmbedSet}
+# the configs of the default run: the headline (the largest workload, whose
+# contraction is tensor-bound) first, then the other workloads with targets
+SUITE = ["prefill", "decode", "qkv", "moe"]
+EXTENDED = ["gate_up", "gate_up_decode", "moe_gather", "stack", "embed", "embed_prefill"]
+MIN_CALLS = 100
+
+
+def algorithmic(config, wl):
+    if config in EMBED_ROWS:
+        return embed_algorithmic(wl)
+    if config == "stack":
+        return stack_algorithmic(wl)
+    if config == "moe_gather":
+        return moe_gather_algorithmic(wl)
+    if config in GATE_UP:
+        return gate_up_algorithmic(wl)
+    if config == "moe":
+        return moe_algorithmic(wl)
+    return proj_algorithmic(wl)
+
+
+def rows_of(config, wl):
+    return wl.T if config in ("moe", "moe_gather") else wl.M
+
+
+def config_dict(config, rows, world, small=False):
+    """The workload description both arms print (the same keys and values)."""
+    return {
+        "workload": DESCRIBE[config] + (" [--small profiling case, not the benchmark]"
+                                        if small and GATE_UP.get(config, config) in SMALL else ""),
+        "rows_per_step": rows,
+        "parallelism": f"replicas x{world} (rows shard, no collective)",
+        "l2": "buffer sets rotate so one pass over them touches >= 3x L2 (129 MB); inputs of prefill and "
+              "MoE exceed L2 on their own",
+        "timing": "each step its own CUDA-graph replay between two CUDA events on the launching stream; "
+                  "value = rows / median step time",
+    }
+
+
+def kernel_of(config, rows):
+    if config in EMBED_ROWS:
+        return "embed_kernel"
+    return "tc_kernel" if (config == "moe" or rows > 16) else "simt_kernel"
+
+
+def per_call_us(torch, graphs, n, stream, world=1, barrier=False):
+    """Device time of n single-call graph replays, each between its own pair
+    of events (3 untimed replays first); a barrier and a synchronize on both
+    sides of the timed replays."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    if barrier and world > 1:
+        torch.distributed.barrier()
+    with torch.cuda.stream(stream):
+        for i, (a, b) in enumerate(evs):
+            a.record(stream)
+            graphs[i % len(graphs)].replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    if barrier and world > 1:
+        torch.distributed.barrier()
+    return [a.elapsed_time(b) * 1e3 for a, b in evs]
+
+
+def summary(us):
+    s = sorted(us)
+    return {"calls": len(s), "median_us": s[len(s) // 2], "min_us": s[0],
+            "mean_us": sum(s) / len(s), "max_us": s[-1]}
+
+
+class Bench:
+    """Device buffers, graphs and timings of one workload."""
+
+    def __init__(self, config, args, world, small=False):
+        import torch
+        import rank_delta_gb300 as rd
+        from rank_delta_gb300 import torch_helpers as th
+        self.torch, self.rd, self.th = torch, rd, th
+        self.config, self.args, self.world, self.small = config, args, world, small
+        self.wl = make_workload(config, small)
+        self.rows = rows_of(config, self.wl)
+        self.algo_bytes, self.algo_flops = algorithmic(config, self.wl)
+        Set = SET_OF.get(config, ProjSet)
+        first = Set(self.wl, th, rd, torch)
+        self.nsets = max(1, int(np.ceil(3 * L2_BYTES / first.bytes)))
+        if config in EMBED_ROWS:
+            self.sets = [first] + [EmbedSet(self.wl, th, rd, torch, like=first) for _ in range(self.nsets - 1)]
+        else:
+            self.sets = [first] + [Set(self.wl, th, rd, torch) for _ in range(self.nsets - 1)]
+        self.set_bytes = first.bytes
+        self.stream = torch.cuda.Stream()
+        self.stream.wait_stream(torch.cuda.current_stream())
+        self.base_slots = [torch.full_like(s.slots, -1) for s in self.sets]
+
+    def graphs(self, base=False):
+        torch, wl, rd = self.torch, self.wl, self.rd
+        with torch.cuda.stream(self.stream):
+            for i in range(self.args.warmup):
+                k = i % self.nsets
+                self.sets[k].step(wl, rd, self.stream, slots=self.base_slots[k] if base else None)
+        torch.cuda.synchronize()
+        gs = []
+        for k in range(self.nsets):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.sets[k].step(wl, rd, torch.cuda.current_stream(),
+                                  slots=self.base_slots[k] if base else None)
+            gs.append(g)
+        return gs
+
+    def e2e(self, steps):
+        """Rows/s end to end through the C ABI: every step copies its own
+        inputs (pinned host x -- tokens for the embedding -- and seq_slot) to
+        the device, makes the call and reads its result back to pinned host
+        memory. The copies of step i+1 and the read-back of step i run on
+        their own streams beside the call of step i; the K steps are one CUDA
+        graph, replayed once untimed and once timed."""
+        torch, wl, rd, sets, nsets = self.torch, self.wl, self.rd, self.sets, self.nsets
+        cap = self.stream
+        nio = max(2, nsets)
+        x_h = sets[0].x.cpu().pin_memory()
+        s_h = sets[0].slots.cpu().pin_memory()
+        y_hs = [torch.empty(sets[0].y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(nio)]
+        xs = [torch.empty_like(sets[0].x) for _ in range(nio)]
+        ss = [torch.empty_like(sets[0].slots) for _ in range(nio)]
+        ys = [torch.empty_like(sets[0].y) for _ in range(nio)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        in_ev = [torch.cuda.Event() for _ in range(nio)]
+        comp_ev = [torch.cuda.Event() for _ in range(nio)]
+        out_ev = [torch.cuda.Event() for _ in range(nio)]
+
+        def run(n, main):
+            for i in range(n):
+                k, j = i % nsets, i % nio
+                with torch.cuda.stream(s_in):
+                    if i >= nio:
+                        s_in.wait_event(comp_ev[j])  # step i - nio has read xs[j], ss[j]
+                    xs[j].copy_(x_h, non_blocking=True)
+                    ss[j].copy_(s_h, non_blocking=True)
+                    in_ev[j].record(s_in)
+                main.wait_event(in_ev[j])
+                if i >= nio:
+                    main.wait_event(out_ev[j])  # step i - nio's y is back on the host
+                sets[k].step(wl, rd, main, x=xs[j], slots=ss[j], y=ys[j])
+                comp_ev[j].record(main)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(comp_ev[j])
+                    y_hs[j].copy_(ys[j], non_blocking=True)
+                    out_ev[j].record(s_out)
+
+        with torch.cuda.stream(cap):
+            s_in.wait_stream(cap)
+            s_out.wait_stream(cap)
+            run(self.args.warmup, cap)
+            cap.wait_stream(s_in)
+            cap.wait_stream(s_out)
+        torch.cuda.synchronize()
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=cap):
+            main = torch.cuda.current_stream()
+            s_in.wait_stream(main)
+            s_out.wait_stream(main)
+            run(steps, main)
+            main.wait_stream(s_in)
+            main.wait_stream(s_out)
+        with torch.cuda.stream(cap):
+            g2.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(cap):
+            e0.record(cap)
+            g2.replay()
+            e1.record(cap)
+        torch.cuda.synchronize()
+        ms = max_over_ranks(e0.elapsed_time(e1), self.world, "cuda")
+        return {"value": job_rate(self.rows, steps, self.world, ms), "unit": "rows/s",
+                "h2d_bytes_per_step": int(x_h.numel() * x_h.element_size() + s_h.numel() * 4),
+                "d2h_bytes_per_step": int(y_hs[0].numel() * 2),
+                "how": "one CUDA graph of the K steps: each step copies its own inputs from pinned host "
+                       "memory and reads its result back to pinned host memory, the copies on two streams "
+                       "beside the neighbouring calls"}
+
+    def roofline(self, call_us):
+        return roofline_of(self.config, self.rows, self.algo_bytes, self.algo_flops, call_us)
+
+
+def roofline_of(config, rows, algo_bytes, algo_flops, call_us):
+    """Achieved bytes (HBM-bound workloads) or flops (tensor-bound) per call
+    over the call time, against the measured peak: the HBM copy figure, or
+    the bf16 burst figure (one call is a sub-millisecond kernel timed alone)."""
+    hbm, tf_burst, _tf_sus, peak_kind = load_peaks()
+    bound = BOUND[config]
+    s = call_us / 1e6
+    if bound == "hbm":
+        achieved, peak, unit = algo_bytes / s / 1e9, hbm, "GB/s"
+    else:
+        achieved, peak, unit = algo_flops / s / 1e12, tf_burst, "TFLOP/s"
+    kernel = kernel_of(config, rows)
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": recorded_traffic(config, kernel),
+            "kernel": f"{kernel} (timed as the whole call, every launch of it)",
+            "algorithmic_bytes_per_call": algo_bytes, "algorithmic_flops_per_call": algo_flops,
+            "peak_source": (f"{peak_kind} {'HBM copy' if bound == 'hbm' else 'bf16 burst'} "
+                            f"({'MEASURED_PEAKS.json' if peak_kind == 'measured' else 'MEASURED_PEAKS.json absent'})"),
+            "call_us": call_us}
+
+
+def measure(b, want_cpu=True):
+    """One workload: per-call times of max(K, 100) calls (median, min), the
+    same calls with every slot -1 (base only), the end-to-end rate, the
+    roofline of the median call, and the oracle on the host cores."""
+    torch, args, world, config = b.torch, b.args, b.world, b.config
+    n = max(args.steps, MIN_CALLS)
+    full = summary(per_call_us(torch, b.graphs(), n, b.stream))
+    base = summary(per_call_us(torch, b.graphs(base=True), n, b.stream))
+    med = max_over_ranks(full["median_us"], world, "cuda")
+    ent = {
+        "value": b.rows * world / (med / 1e6), "unit": "rows/s", "ms_per_step": med / 1e3,
+        "per_call": full,
+        "base_only": dict(base, how="the same call with every slot -1 (no adapter applied)",
+                          delta_share=1.0 - base["median_us"] / full["median_us"]),
+        "roofline": b.roofline(med),
+        "e2e": b.e2e(args.steps),
+        "gpu_launches_per_call": launches_per_call(config, b.rows, kernel_of(config, b.rows)),
+        "status_flags": b.rd.lora_status_get(b.sets[0].ws),
+        "config": config_dict(config, b.rows, world, b.small),
+    }
+    if want_cpu:
+        ent["cpu_baseline"] = oracle_rate(b.wl, config, budget_s=8.0, cap_s=20.0)
+    return ent
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
-    import workloads
     import rank_delta_gb300 as rd
     from rank_delta_gb300 import build as rdbuild
-    from rank_delta_gb300 import torch_helpers as th
 
     if rank == 0:
         rdbuild.build()
@@ -495,247 +739,56 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     rd.lib()
     torch.cuda.set_device(local_rank)
-    wl = make_workload(args.config, args.small)
-    is_moe = args.config == "moe"
-    slot_rows = args.config in ("moe", "moe_gather")
-    is_embed = args.config in EMBED_ROWS
-    rows = wl.T if slot_rows else wl.M
-    is_gate_up = args.config in GATE_UP
-    if is_embed:
-        algo_bytes, algo_flops = embed_algorithmic(wl)
-    elif args.config == "stack":
-        algo_bytes, algo_flops = stack_algorithmic(wl)
-    elif args.config == "moe_gather":
-        algo_bytes, algo_flops = moe_gather_algorithmic(wl)
-    elif is_gate_up:
-        algo_bytes, algo_flops = gate_up_algorithmic(wl)
-    else:
-        algo_bytes, algo_flops = moe_algorithmic(wl) if is_moe else proj_algorithmic(wl)
-    Set = MoeSet if is_moe else (EmbedSet if is_embed else (GateUpSet if is_gate_up else ProjSet))
-    if args.config == "stack":
-        Set = StackSet
-    if args.config == "moe_gather":
-        Set = MoeGatherSet
-    first = Set(wl, th, rd, torch)
-    nsets = max(1, int(np.ceil(3 * L2_BYTES / first.bytes)))
-    if is_embed:
-        sets = [first] + [EmbedSet(wl, th, rd, torch, like=first) for _ in range(nsets - 1)]
-    else:
-        sets = [first] + [Set(wl, th, rd, torch) for _ in range(nsets - 1)]
-    stream = torch.cuda.current_stream()
-
-    # The timed region replays one CUDA graph holding the K steps (each step's
-    # kernels as graph nodes, buffer sets rotating), so the device time is the
-    # kernels' own and not the host's enqueue rate.
-    cap = torch.cuda.Stream()
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        for i in range(args.warmup):
-            sets[i % nsets].step(wl, rd, cap)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=cap):
-        for i in range(args.steps):
-            sets[i % nsets].step(wl, rd, torch.cuda.current_stream())
-    with torch.cuda.stream(cap):
-        graph.replay()  # one untimed replay: the graph's own first-launch costs
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    suite = args.config == "suite"
+    head = "prefill" if suite else args.config
+    rest = ([c for c in SUITE if c != head] + (EXTENDED if args.extended else [])) if suite else []
+    want_cpu = world == 1 and not args.no_cpu_baseline
 
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(cap):
-        t_start.record(cap)
-        graph.replay()
-        t_end.record(cap)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    # keep replaying ~1 s so the clock sampler sees the GPU under the same load
-    t_keep = time.time()
-    with torch.cuda.stream(cap):
-        while time.time() - t_keep < 1.0:
-            graph.replay()
-            torch.cuda.synchronize()
+    hb = Bench(head, args, world, args.small)
+    # the timed region: exactly K steps, each its own graph replay between events
+    us = per_call_us(torch, hb.graphs(), args.steps, hb.stream, world, barrier=True)
+    med = max_over_ranks(sorted(us)[len(us) // 2], world, "cuda")
+    head_ent = measure(hb, want_cpu)
+    del hb
+    torch.cuda.empty_cache()
+    configs = {head: head_ent}
+    for c in rest:
+        bc = Bench(c, args, world)
+        configs[c] = measure(bc, want_cpu)
+        del bc
+        torch.cuda.empty_cache()
     clk = clocks.stop()
-
-    elapsed_ms = t_start.elapsed_time(t_end)
-    call_ms = elapsed_ms / args.steps
-    elapsed_ms = max_over_ranks(elapsed_ms, world, "cuda")
-    ms_per_step = elapsed_ms / args.steps
-    value = job_rate(rows, args.steps, world, elapsed_ms)
-    status = rd.lora_status_get(sets[0].ws)
-
-    # end to end through the C ABI: every step copies its own inputs (pinned
-    # host x -- tokens for the embedding -- and seq_slot) to the device, makes
-    # the call, and reads its result back to pinned host memory. The copies of
-    # step i+1 and the read-back of step i run on their own streams beside the
-    # call of step i (buffer set i % nsets; events order each set's reuse), as
-    # a serving loop would overlap them.
-    # input/output buffers of the steps in flight: at least two, so that one
-    # step's copies can overlap another's call even with one weight set
-    nio = max(2, nsets)
-    x_h = sets[0].x.cpu().pin_memory()
-    s_h = sets[0].slots.cpu().pin_memory()
-    y_hs = [torch.empty(sets[0].y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(nio)]
-    xs = [torch.empty_like(sets[0].x) for _ in range(nio)]
-    ss = [torch.empty_like(sets[0].slots) for _ in range(nio)]
-    ys = [torch.empty_like(sets[0].y) for _ in range(nio)]
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    in_ev = [torch.cuda.Event() for _ in range(nio)]
-    comp_ev = [torch.cuda.Event() for _ in range(nio)]
-    out_ev = [torch.cuda.Event() for _ in range(nio)]
-
-    def e2e_steps(n, main):
-        for i in range(n):
-            k, j = i % nsets, i % nio
-            with torch.cuda.stream(s_in):
-                if i >= nio:
-                    s_in.wait_event(comp_ev[j])  # step i - nio has read xs[j], ss[j]
-                xs[j].copy_(x_h, non_blocking=True)
-                ss[j].copy_(s_h, non_blocking=True)
-                in_ev[j].record(s_in)
-            main.wait_event(in_ev[j])
-            if i >= nio:
-                main.wait_event(out_ev[j])  # step i - nio's y is back on the host
-            sets[k].step(wl, rd, main, x=xs[j], slots=ss[j], y=ys[j])
-            comp_ev[j].record(main)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(comp_ev[j])
-                y_hs[j].copy_(ys[j], non_blocking=True)
-                out_ev[j].record(s_out)
-
-    # eager warm-up, then the K steps as one CUDA graph (copy nodes from and to
-    # pinned host memory, the calls' kernels), replayed once untimed and once
-    # timed, so the host's enqueue rate does not set the number
-    with torch.cuda.stream(cap):
-        s_in.wait_stream(cap)
-        s_out.wait_stream(cap)
-        e2e_steps(args.warmup, cap)
-        cap.wait_stream(s_in)
-        cap.wait_stream(s_out)
-    torch.cuda.synchronize()
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2, stream=cap):
-        main = torch.cuda.current_stream()
-        s_in.wait_stream(main)
-        s_out.wait_stream(main)
-        e2e_steps(args.steps, main)
-        main.wait_stream(s_in)
-        main.wait_stream(s_out)
-    with torch.cuda.stream(cap):
-        g2.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(cap):
-        e0.record(cap)
-        g2.replay()
-        e1.record(cap)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, "cuda")
-    e2e_value = job_rate(rows, args.steps, world, e2e_ms)
-
-    # per-call device times: one graph per buffer set holding a single call,
-    # each replay between two events on the launching stream, 100 replays
-    # after 3 untimed ones; the median and the minimum are reported beside the
-    # mean of the timed region (a failure here only drops these figures)
-    try:
-        one = []
-        for k in range(nsets):
-            g1 = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g1, stream=cap):
-                sets[k].step(wl, rd, torch.cuda.current_stream())
-            one.append(g1)
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(100)]
-        with torch.cuda.stream(cap):
-            for i in range(3):
-                one[i % nsets].replay()
-            for i, (a, b) in enumerate(evs):
-                a.record(cap)
-                one[i % nsets].replay()
-                b.record(cap)
-        torch.cuda.synchronize()
-        us = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
-        per_call = {"calls": len(us), "median_us": us[len(us) // 2], "min_us": us[0],
-                    "how": "one graph of a single call per buffer set, events around each replay "
-                           "(includes the graph's own launch gap, so above the mean of the K-step graph)"}
-    except Exception as ex:  # noqa: BLE001
-        per_call = {"error": f"{type(ex).__name__}: {ex}"[:200]}
-
-    hbm, tf_burst, tf_sus, peak_kind = load_peaks()
-    avg_call_s = call_ms / 1e3
-    bound = BOUND[args.config]
-    if bound == "hbm":
-        achieved = algo_bytes / avg_call_s / 1e9
-        peak, unit = hbm, "GB/s"
-    else:
-        achieved = algo_flops / avg_call_s / 1e12
-        # a contraction timed over a long back-to-back loop runs in the
-        # power-capped regime the sustained figure was measured in; a short
-        # one is compared with the burst figure
-        long_loop = elapsed_ms >= 100.0
-        peak, unit = (tf_sus if long_loop else tf_burst), "TFLOP/s"
-        peak_kind = (f"{peak_kind} sustained (timed region {elapsed_ms:.0f} ms of back-to-back calls; "
-                     f"{achieved / tf_burst:.3f} of the burst {tf_burst})" if long_loop else
-                     f"{peak_kind} burst")
-    if is_embed:
-        kernel = "embed_kernel"
-    else:
-        kernel = "tc_kernel" if (is_moe or rows > 16) else "simt_kernel"
-    traffic = recorded_traffic(args.config, kernel)
+    rows = head_ent["config"]["rows_per_step"]
+    ra = head_ent["roofline"]
     out = {
         "metric": METRIC,
-        "value": value,
+        "value": rows * world / (med / 1e6),
         "unit": "rows/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
+        "ms_per_step": med / 1e3,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
-        "config": {
-            "workload": DESCRIBE[args.config] + (" [--small profiling case, not the benchmark]"
-                                                 if args.small and GATE_UP.get(args.config, args.config) in SMALL
-                                                 else ""),
-            "rows_per_step": rows,
-            "parallelism": f"replicas x{world} (rows shard, no collective)",
-            "l2": f"rotating {nsets} buffer sets of {first.bytes / 1e6:.1f} MB "
-                  f"{'touched per step ' if is_embed else ''}(>= 3x L2)",
-            "timing": "CUDA events around one replay of a graph of the K steps",
-        },
+        "config": head_ent["config"],
         "clocks": clk,
-        "e2e": {"value": e2e_value, "unit": "rows/s",
-                "h2d_bytes_per_step": int(x_h.numel() * x_h.element_size() + s_h.numel() * 4),
-                "d2h_bytes_per_step": int(y_hs[0].numel() * 2),
-                "how": "one CUDA graph of the K steps: each step copies its own inputs from pinned host "
-                       "memory and reads its result back to pinned host memory, the copies on two streams "
-                       "beside the neighbouring calls"},
-        "gpu_launches": launches_per_call(args.config, rows, kernel) * args.steps,
-        "roofline": {
-            "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-            "frac": achieved / peak, "traffic": traffic,
-            "kernel": f"{kernel} (timed as the whole call: routing sort + {kernel}, graph replay)",
-            "algorithmic_bytes_per_call": algo_bytes, "algorithmic_flops_per_call": algo_flops,
-            "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind.startswith("measured") else
-                            f"{peak_kind} (MEASURED_PEAKS.json absent)"),
-            "call_us": call_ms * 1e3,
-            "per_call": per_call,
-        },
-        "status_flags": status,
+        "e2e": head_ent["e2e"],
+        "gpu_launches": head_ent["gpu_launches_per_call"] * args.steps,
+        "roofline": dict(roofline_of(head, rows, ra["algorithmic_bytes_per_call"],
+                                     ra["algorithmic_flops_per_call"], med),
+                         per_call_timed_region=summary(us)),
+        "status_flags": head_ent["status_flags"],
+        "configs": configs,
     }
-    return out, wl
+    if want_cpu:
+        out["cpu_baseline"] = head_ent["cpu_baseline"]
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -801,30 +854,40 @@ def oracle_rate(wl, config, budget_s=12.0, cap_s=30.0):
 
 
 def run_reference(args, rank, world):
+    """The reference arm: the oracle (plain fp32 C loops) on the host cores,
+    on the headline workload -- each step a bounded sample of it -- plus one
+    bounded sample of every other workload of the run."""
     if rank != 0:
         return
-    wl = make_workload(args.config)
+    suite = args.config == "suite"
+    head = "prefill" if suite else args.config
+    rest = ([c for c in SUITE if c != head] + (EXTENDED if args.extended else [])) if suite else []
+    wl = make_workload(head, args.small)
+    rows = rows_of(head, wl)
     per = []
     cpu = None
-    for _ in range(args.warmup):
-        pass
-    for _ in range(max(1, args.steps)):
-        cpu = oracle_rate(wl, args.config, budget_s=max(2.0, 60.0 / max(1, args.steps)),
-                          cap_s=max(4.0, 90.0 / max(1, args.steps)))
+    steps = max(1, args.steps)
+    for _ in range(steps):
+        cpu = oracle_rate(wl, head, budget_s=max(1.5, 40.0 / steps), cap_s=max(3.0, 60.0 / steps))
         per.append(cpu["value"])
     value = float(np.median(per))
-    rows = wl.T if args.config in ("moe", "moe_gather") else wl.M
     cpu["value"] = value
+    configs = {head: {"value": value, "unit": "rows/s", "ms_per_step": rows / value * 1e3}}
+    for c in rest:
+        w = make_workload(c)
+        r = oracle_rate(w, c, budget_s=5.0, cap_s=10.0)
+        configs[c] = {"value": r["value"], "unit": "rows/s", "ms_per_step": rows_of(c, w) / r["value"] * 1e3,
+                      "cpu_baseline": r}
     out = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": rows / value * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded)",
-        "config": {"workload": DESCRIBE[args.config], "rows_per_step": rows,
-                   "note": "the reference is the CPU oracle (plain fp32 loops), no reference code "
-                           "exists to install"},
+        "data": "synthetic (seeded; shapes and distributions of the workload, no dataset)",
+        "config": config_dict(head, rows, world, args.small),
         "cpu_baseline": cpu,
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "configs": configs,
+        "note": "the reference is the CPU oracle (plain fp32 loops); no reference code exists to install",
     }
     print(json.dumps(out), flush=True)
 
@@ -832,9 +895,12 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="decode", choices=sorted(DESCRIBE))
+    ap.add_argument("--config", default="suite", choices=["suite"] + sorted(DESCRIBE),
+                    help="suite (default): prefill as the headline, decode, qkv and moe under 'configs'")
+    ap.add_argument("--extended", action="store_true",
+                    help="with the suite: also gate_up, gate_up_decode, moe_gather, stack, embed, embed_prefill")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--small", action="store_true",
@@ -852,10 +918,8 @@ def main():
         import torch
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
-    out, wl = run_ours(args, rank, world, local_rank)
+    out = run_ours(args, rank, world, local_rank)
     if rank == 0:
-        if world == 1 and not args.no_cpu_baseline:
-            out["cpu_baseline"] = oracle_rate(wl, args.config)
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch

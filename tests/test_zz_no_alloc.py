@@ -5,9 +5,12 @@ running). It takes no workspace and uses the scratch array built into the
 library instead.
 
 Checked here through the C ABI: two calls in a row, with different routing,
-each give what lora_proj_apply gives on the same inputs (within the parity
-tolerance), and a batch whose scratch need exceeds the built-in size is
-refused with a message naming both sizes. This file is collected last on
+each give the bytes lora_proj_apply gives on the same inputs (the same
+kernels with the same order of sums, so any difference would be a scratch
+region read wrongly or reused too early); a decode call followed by a
+2048-row prefill-shaped call (the tensor-core shrink layout of the scratch)
+gives the bytes of the workspace entry too; and a batch whose scratch need
+exceeds the built-in size is refused with a message naming both sizes. This file is collected last on
 purpose; it builds everything it uses, so it also passes on its own.
 """
 import numpy as np
@@ -18,7 +21,7 @@ import rank_delta_gb300 as rd
 import workloads
 from rank_delta_gb300 import build as rdbuild
 from rank_delta_gb300 import torch_helpers as th
-from tests.gpu_common import SENTINEL, ProjRun, assert_close
+from tests.gpu_common import SENTINEL, ProjRun
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +52,19 @@ def test_static_scratch_matches_workspace_entry_on_two_calls(name):
     for slots in (run.slots, torch.from_numpy(other).cuda()):
         want = run.apply(slots=slots)
         got = static_apply(run, slots)
-        assert_close(got, th.bf16_bits_to_f32(want), f"{name} static scratch")
+        assert np.array_equal(got, want), f"{name}: static scratch differs from the workspace entry"
+
+
+def test_static_scratch_decode_then_prefill_shaped_batch():
+    dec = ProjRun(workloads.make("decode"))
+    pre = ProjRun(workloads.make("prefill", seq_len=256))  # 2048 rows, 8 sequences
+    assert pre.wl.M == 2048
+    need = rd.lora_proj_workspace_bytes(pre.wl.M, pre.route.rt)
+    assert need <= rd.LORA_STATIC_WS_BYTES
+    for run in (dec, pre):
+        got = static_apply(run, run.slots)
+        want = run.apply()
+        assert np.array_equal(got, want), f"{run.wl.name}: static scratch differs from the workspace entry"
 
 
 def test_static_scratch_refuses_batches_beyond_its_size():

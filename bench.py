@@ -266,6 +266,7 @@ class ClockSampler:
 # the sources each timed kernel is compiled from (a recorded DRAM figure holds
 # while these are unchanged)
 KERNEL_SOURCES = {
+    "dec_kernel": ["lora_dec.cu", "ptx.cuh", "vec.cuh", "lora_internal.cuh"],
     "tc_kernel": ["lora_tc.cu", "shrink.cuh", "ptx.cuh", "vec.cuh", "lora_internal.cuh"],
     "simt_kernel": ["lora_simt.cu", "shrink.cuh", "vec.cuh", "lora_internal.cuh"],
     "embed_kernel": ["lora_embed.cu", "ptx.cuh", "lora_internal.cuh"],
@@ -313,7 +314,7 @@ class ProjSet:
         slots = self.slots if slots is None else slots
         y = self.y if y is None else y
         rd.lora_proj_apply(x, x.stride(0), self.W, wl.M, wl.K, wl.N, slots, self.route.rt, y,
-                           y.stride(0), self.ws, self.ws.numel(), stream)
+                           y.stride(0), self.ws, self.ws.numel(), stream, path=PROJ_PATH[0])
 
 
 class MoeSet:
@@ -454,12 +455,14 @@ def job_rate(rows: int, steps: int, world: int, elapsed_ms: float) -> float:
     return rows * steps * world / (elapsed_ms / 1e3)
 
 
-# kernels one call launches: the routing sort, then one fused tensor-core launch
-# (shrink + base + expand-fold), with a tensor-core shrink launch between the
-# two from 2048 projection rows; the CUDA-core path (<= 16 rows) runs the sort,
-# a shrink launch and the GEMV; the embedding gather runs the sort and one launch
-LAUNCHES_TC, LAUNCHES_SIMT, LAUNCHES_EMBED = 2, 3, 2
+# kernels one call launches: up to 256 rows, one kernel (routing, shrink,
+# base, expand-fold and the split-K sum); beyond, the routing sort, then one
+# fused tensor-core launch, with a tensor-core shrink launch between the two
+# from 2048 projection rows; the CUDA-core path (<= 16 rows) runs the sort, a
+# shrink launch and the GEMV; the embedding gather runs the sort and one launch
+LAUNCHES_DEC, LAUNCHES_TC, LAUNCHES_SIMT, LAUNCHES_EMBED = 1, 2, 3, 2
 TC_SHRINK_MIN_ROWS = 2048
+DEC_MAX_ROWS = 256
 
 
 def launches_per_call(config, rows, kernel):
@@ -467,6 +470,8 @@ def launches_per_call(config, rows, kernel):
         return LAUNCHES_EMBED
     if config == "moe_gather":  # expert sort + row copy, the grouped fold, the combine
         return LAUNCHES_TC + 2
+    if kernel == "dec_kernel":
+        return LAUNCHES_DEC
     if config in GATE_UP: # the projection, then the activation kernel
         return launches_per_call(GATE_UP[config], rows, kernel) + 1
     if kernel == "simt_kernel":
@@ -497,6 +502,8 @@ SET_OF = {"moe": MoeSet, "stack": StackSet, "moe_gather": MoeGatherSet, "gate_up
 SUITE = ["prefill", "decode", "qkv", "moe"]
 EXTENDED = ["gate_up", "gate_up_decode", "moe_gather", "stack", "embed", "embed_prefill"]
 MIN_CALLS = 100
+STEADY_CALLS = 10  # calls per steady-state graph (calls under a millisecond)
+PROJ_PATH = [0]    # lora_proj_apply path of the projection workloads (--path)
 
 
 def algorithmic(config, wl):
@@ -526,15 +533,21 @@ def config_dict(config, rows, world, small=False):
         "parallelism": f"replicas x{world} (rows shard, no collective)",
         "l2": "buffer sets rotate so one pass over them touches >= 3x L2 (129 MB); inputs of prefill and "
               "MoE exceed L2 on their own",
-        "timing": "each step its own CUDA-graph replay between two CUDA events on the launching stream; "
-                  "value = rows / median step time",
+        "timing": "configs: value = rows / median per-call time in steady state (100 replays of one CUDA "
+                  "graph of back-to-back calls, the buffer sets in turn, each replay between two CUDA events "
+                  "on the launching stream); the isolated single-call latency beside it. Headline: exactly "
+                  "K steps, each its own graph replay between events, value = rows / median step time",
     }
 
 
 def kernel_of(config, rows):
     if config in EMBED_ROWS:
         return "embed_kernel"
-    return "tc_kernel" if (config == "moe" or rows > 16) else "simt_kernel"
+    if config in ("moe", "moe_gather"):
+        return "tc_kernel"
+    if rows <= 16 and PROJ_PATH[0] == 0:
+        return "simt_kernel"
+    return "dec_kernel" if rows <= DEC_MAX_ROWS and PROJ_PATH[0] == 3 else "tc_kernel"
 
 
 def per_call_us(torch, graphs, n, stream, world=1, barrier=False):
@@ -557,6 +570,24 @@ def per_call_us(torch, graphs, n, stream, world=1, barrier=False):
     if barrier and world > 1:
         torch.distributed.barrier()
     return [a.elapsed_time(b) * 1e3 for a, b in evs]
+
+
+def steady_us(torch, graph, calls, samples, stream):
+    """Per-call device time in steady state: `samples` replays of one graph of
+    `calls` back-to-back calls, each replay between its own pair of events (3
+    untimed replays first); a sample is the replay's time / calls."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(samples)]
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            graph.replay()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) * 1e3 / calls for a, b in evs]
 
 
 def summary(us):
@@ -604,6 +635,17 @@ class Bench:
                                   slots=self.base_slots[k] if base else None)
             gs.append(g)
         return gs
+
+    def steady_graph(self, calls, base=False):
+        """One graph of `calls` back-to-back calls, the buffer sets in turn."""
+        torch, wl, rd = self.torch, self.wl, self.rd
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            for i in range(calls):
+                k = i % self.nsets
+                self.sets[k].step(wl, rd, torch.cuda.current_stream(),
+                                  slots=self.base_slots[k] if base else None)
+        return g
 
     def e2e(self, steps):
         """Rows/s end to end through the C ABI: every step copies its own
@@ -709,13 +751,21 @@ def measure(b, want_cpu=True):
     roofline of the median call, and the oracle on the host cores."""
     torch, args, world, config = b.torch, b.args, b.world, b.config
     n = max(args.steps, MIN_CALLS)
-    full = summary(per_call_us(torch, b.graphs(), n, b.stream))
-    base = summary(per_call_us(torch, b.graphs(base=True), n, b.stream))
+    iso = summary(per_call_us(torch, b.graphs(), n, b.stream))
+    calls = STEADY_CALLS if iso["median_us"] < 1000.0 else 1
+    full = summary(steady_us(torch, b.steady_graph(calls), calls, n, b.stream))
+    b.graphs(base=True)  # warm-up of the base-only calls
+    base = summary(steady_us(torch, b.steady_graph(calls, base=True), calls, n, b.stream))
     med = max_over_ranks(full["median_us"], world, "cuda")
     ent = {
         "value": b.rows * world / (med / 1e6), "unit": "rows/s", "ms_per_step": med / 1e3,
-        "per_call": full,
-        "base_only": dict(base, how="the same call with every slot -1 (no adapter applied)",
+        "per_call": dict(full, how=f"steady state: {n} replays of one CUDA graph of {calls} back-to-back "
+                                   f"calls (the buffer sets in turn), each replay between its own events; "
+                                   f"a sample is the replay time / {calls}"),
+        "per_call_isolated": dict(iso, how="each call its own single-call graph replay between its own "
+                                           "events: the latency of one call, the graph launch (about 5 us "
+                                           "on this GPU) included"),
+        "base_only": dict(base, how="steady state as per_call, every slot -1 (no adapter applied)",
                           delta_share=1.0 - base["median_us"] / full["median_us"]),
         "roofline": b.roofline(med),
         "e2e": b.e2e(args.steps),
@@ -903,11 +953,14 @@ def main():
                     help="with the suite: also gate_up, gate_up_decode, moe_gather, stack, embed, embed_prefill")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "tc", "tc_one"],
+                    help="lora_proj_apply path of the projection workloads (default: the library's choice)")
     ap.add_argument("--small", action="store_true",
                     help="profiling case: prefill 2048 rows, MoE 128 tokens (not the benchmarked workload)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    PROJ_PATH[0] = {"auto": 0, "tc": 2, "tc_one": 3}[args.path]
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

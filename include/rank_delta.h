@@ -90,7 +90,12 @@ enum {
 enum {
     LORA_PATH_AUTO = 0, /* by row count: CUDA-core GEMV for few rows, tensor cores otherwise */
     LORA_PATH_SIMT = 1, /* CUDA-core GEMV path (any row count; slow for many rows) */
-    LORA_PATH_TC = 2    /* tcgen05 tensor-core path */
+    LORA_PATH_TC = 2,   /* tcgen05 tensor-core path: a routing kernel, then the projection kernel
+                           (from 2048 rows a tensor-core shrink kernel before it) */
+    LORA_PATH_TC_ONE = 3 /* batches of up to 256 rows in one launch: routing, shrink, base, expand
+                            and the split-K sum in a single kernel (other shapes, or a device that
+                            cannot hold its grid, take LORA_PATH_TC). Measured slower than
+                            LORA_PATH_TC on the decode and fused-QKV shapes; kept for comparison */
 };
 
 /*
@@ -265,7 +270,9 @@ lora_status lora_select_victim_slot(const lora_slot_view *cache, int n, int32_t 
 /*
  * Workspace of lora_proj_apply for M rows on route `rt` (device scratch the
  * caller provides: the routing sort, the shrink work list, the rank-sized h of
- * every row, handoff counters and the status word). 256-byte aligned
+ * every row, handoff counters or the exchange flags of the one-launch kernel,
+ * and the status words). Its contents need no initialisation: every call
+ * tags what it waits on with an epoch kept in the workspace. 256-byte aligned
  * sections; the caller passes a buffer of at least this many bytes, 256-byte
  * aligned. Returns 0 if rt is NULL or not initialised.
  */
@@ -352,6 +359,16 @@ size_t lora_gate_up_workspace_bytes(int M, const lora_route *rt);
 lora_status lora_gate_up_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int I,
                                const int32_t *seq_slot, const lora_route *rt, void *act,
                                int64_t act_stride, void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/* lora_gate_up_apply with an explicit path of the projection (LORA_PATH_*).
+ * LORA_PATH_TC_ONE takes batches of 17..256 rows with K and I multiples of
+ * 64 through the one-launch kernel, whose split-K sum writes act directly
+ * (silu(g) * u of the bf16-rounded halves, rounded once: the same rule);
+ * every other case runs the projection on that path, then the act pass. */
+lora_status lora_gate_up_apply_ex(const void *x, int64_t x_stride, const void *W, int M, int K,
+                                  int I, const int32_t *seq_slot, const lora_route *rt, void *act,
+                                  int64_t act_stride, void *ws, size_t ws_bytes, int path,
+                                  lora_stream_t stream);
 
 /* Largest expert count lora_moe_down_apply takes in one call. */
 #define LORA_MAX_EXPERTS 16
@@ -485,8 +502,49 @@ lora_status lora_moe_gather_apply(const void *x, int64_t x_stride, const void *c
                                   lora_stream_t stream);
 
 /* Read the status word (LORA_FLAG_* bits) of the most recent call that used
- * workspace `ws`. Synchronises `stream` (diagnostic, not a hot-path call). */
+ * workspace `ws`. Synchronises `stream` (diagnostic, not a hot-path call).
+ * The first 16 bytes of a workspace hold the bits, the tag of the call that
+ * set them and an epoch that every call advances by one; the bits count when
+ * the tag is the last call's (epoch - 1), so a call that sets no bit needs no
+ * clearing pass and reads as 0. */
 lora_status lora_status_get(const void *ws, uint32_t *flags, lora_stream_t stream);
+
+/* Which kernels a projection call of M rows on `rt` takes on the current
+ * device (lora_proj_plan; the pages have no counterpart: a diagnostic). */
+enum {
+    LORA_PLAN_SIMT = 1,        /* <= 16 rows: CUDA-core GEMV (routing, shrink, GEMV launches) */
+    LORA_PLAN_TC = 2,          /* routing launch, then tensor-core launches */
+    LORA_PLAN_ONE_LAUNCH = 3   /* <= 256 rows: everything in one clustered tensor-core launch */
+};
+typedef struct lora_plan_info {
+    int32_t path;              /* LORA_PLAN_* */
+    int32_t kernels;           /* kernel launches of one call */
+    int32_t cluster_size;      /* one-launch kernel: CTAs per cluster (the K parts) */
+    int32_t clusters_needed;   /* one-launch kernel: clusters of the grid (feature tiles) */
+    int32_t clusters_resident; /* clusters of that size the device can hold at once */
+    int32_t smem_per_cta;      /* bytes of shared memory of one CTA of the one-launch kernel */
+} lora_plan_info;
+
+/*
+ * Fill `info` for a lora_proj_apply of M rows on projection route `rt`
+ * (gated = 1: lora_gate_up_apply with I = n_out / 2). The one-launch kernel
+ * needs its whole grid resident at once (its CTAs exchange h through the
+ * workspace); a shape whose clusters do not all fit takes LORA_PLAN_TC.
+ * Errors: NULL info, a route that is not a projection route, M < 0.
+ */
+lora_status lora_proj_plan(int M, const lora_route *rt, int gated, lora_plan_info *info);
+
+/*
+ * Test hook for the bounded device waits of the one-launch kernel of up to
+ * 256 rows (the pages have no counterpart). With wait_ns > 0, later calls
+ * give up their exchange wait after wait_ns nanoseconds instead of about a
+ * second, and wait for extra_flags flags that no CTA ever writes, so the
+ * wait runs out: the call then returns with LORA_FLAG_WAIT_TIMEOUT in its
+ * status word and y holding the base product without the delta. Nothing
+ * faults or hangs. wait_ns = 0 restores normal operation. Process-wide; for
+ * tests only.
+ */
+void lora_test_wait_hook(uint64_t wait_ns, int extra_flags);
 
 /*
  * Copy the routing sort of the most recent lora_proj_apply on `ws` to host

@@ -40,10 +40,27 @@ LORA_ROUTE_EMBED = 1
 LORA_PATH_AUTO = 0
 LORA_PATH_SIMT = 1
 LORA_PATH_TC = 2
+LORA_PATH_TC_ONE = 3
 
 LORA_MAX_EXPERTS = 16
 LORA_STATIC_WS_BYTES = 8 << 20
 LORA_COMP_STRIDE = 256
+
+
+LORA_PLAN_SIMT = 1
+LORA_PLAN_TC = 2
+LORA_PLAN_ONE_LAUNCH = 3
+
+
+class lora_plan_info(ctypes.Structure):
+    _fields_ = [
+        ("path", ctypes.c_int32),
+        ("kernels", ctypes.c_int32),
+        ("cluster_size", ctypes.c_int32),
+        ("clusters_needed", ctypes.c_int32),
+        ("clusters_resident", ctypes.c_int32),
+        ("smem_per_cta", ctypes.c_int32),
+    ]
 
 
 class LoraError(RuntimeError):
@@ -109,6 +126,7 @@ _SIGNATURES = {
     "lora_proj_apply_static_ws": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp]),
     "lora_gate_up_workspace_bytes": (_sz, [_i, _rtp]),
     "lora_gate_up_apply": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
+    "lora_gate_up_apply_ex": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _i, _vp]),
     "lora_moe_workspace_bytes": (_sz, [_i, _i, _rtp]),
     "lora_moe_gather_workspace_bytes": (_sz, [_i, _i, _rtp]),
     "lora_moe_gather_apply": (_i, [_vp, _i64, ctypes.POINTER(_vp), _vp, _i, _i, _i, _i, _vp, _rtp,
@@ -120,6 +138,8 @@ _SIGNATURES = {
     "lora_embed_workspace_bytes": (_sz, [_i, _rtp]),
     "lora_embed_apply": (_i, [_vp, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_status_get": (_i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
+    "lora_test_wait_hook": (None, [ctypes.c_uint64, _i]),
+    "lora_proj_plan": (_i, [_i, _rtp, _i, ctypes.POINTER(lora_plan_info)]),
     "lora_proj_routing": (_i, [_vp, _i, _i, _i32p, _i32p, _vp]),
     "lora_last_error": (ctypes.c_char_p, []),
     "lora_build_seq_slot": (_i, [_i32p, _i, _i, _i, _i32p]),
@@ -272,10 +292,16 @@ def lora_gate_up_workspace_bytes(M: int, rt: lora_route) -> int:
 
 
 def lora_gate_up_apply(x, x_stride: int, W, M: int, K: int, I: int, seq_slot, rt: lora_route, act,
-                       act_stride: int, ws, ws_bytes: int, stream=None) -> None:
-    _check(lib().lora_gate_up_apply(_ptr(x), x_stride, _ptr(W), M, K, I, _ptr(seq_slot),
-                                    ctypes.byref(rt), _ptr(act), act_stride, _ptr(ws), ws_bytes,
-                                    _stream(stream)))
+                       act_stride: int, ws, ws_bytes: int, stream=None, path: int = LORA_PATH_AUTO) -> None:
+    if path == LORA_PATH_AUTO:
+        code = lib().lora_gate_up_apply(_ptr(x), x_stride, _ptr(W), M, K, I, _ptr(seq_slot),
+                                        ctypes.byref(rt), _ptr(act), act_stride, _ptr(ws), ws_bytes,
+                                        _stream(stream))
+    else:
+        code = lib().lora_gate_up_apply_ex(_ptr(x), x_stride, _ptr(W), M, K, I, _ptr(seq_slot),
+                                           ctypes.byref(rt), _ptr(act), act_stride, _ptr(ws), ws_bytes,
+                                           path, _stream(stream))
+    _check(code)
 
 
 def lora_moe_workspace_bytes(E: int, T: int, rts) -> int:
@@ -338,6 +364,20 @@ def lora_status_get(ws, stream=None) -> int:
     out = ctypes.c_uint32(0)
     _check(lib().lora_status_get(_ptr(ws), ctypes.byref(out), _stream(stream)))
     return int(out.value)
+
+
+def lora_proj_plan(M: int, rt, gated: bool = False) -> dict:
+    """Which kernels a projection call of M rows on route `rt` takes on the
+    current device (path, launches, cluster shape and residency)."""
+    info = lora_plan_info()
+    _check(lib().lora_proj_plan(int(M), ctypes.byref(rt), int(bool(gated)), ctypes.byref(info)))
+    return {f: int(getattr(info, f)) for f, _ in lora_plan_info._fields_}
+
+
+def lora_test_wait_hook(wait_ns: int, extra_flags: int) -> None:
+    """Test hook: bounded device waits give up after wait_ns and wait for
+    extra_flags flags nothing writes (0, 0 restores normal operation)."""
+    lib().lora_test_wait_hook(int(wait_ns), int(extra_flags))
 
 
 def lora_proj_routing(ws, M: int, max_loras: int, stream=None):

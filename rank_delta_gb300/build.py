@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "librank_delta.so")
 SOURCES = ["lora_api.cu", "lora_prep.cu", "lora_simt.cu", "lora_tc.cu", "lora_shrink_tc.cu", "lora_embed.cu", "lora_act.cu", "lora_gather.cu",
-           "lora_static_ws.cu"]
+           "lora_static_ws.cu", "lora_dec.cu"]
 HEADERS = ["lora_internal.cuh", "ptx.cuh", "shrink.cuh", "vec.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")

@@ -197,6 +197,90 @@ bool make_map_3d(CUtensorMap *m, const void *base, uint64_t K, uint64_t rows, ui
     return r == CUDA_SUCCESS;
 }
 
+// The fused [gate | up] weight W [2I][K] (K a multiple of 64) as a 4D view
+// [K/64 chunks][2 halves][I rows][64]: one box of kc x 2 x 64 x 64 brings, per
+// 64-wide K slice, gate rows f..f+63 then up rows I+f..I+f+63 -- 128 rows in
+// the layout of a plain 128-row box.
+bool make_map_gated(CUtensorMap *m, const void *W, uint64_t K, uint64_t I, uint32_t box_chunks)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[4] = {64, I, 2, K / 64};
+    cuuint64_t strides[3] = {K * 2, I * K * 2, 128};
+    cuuint32_t box[4] = {64, 64, 2, box_chunks};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(W), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The A rows of every slot of a projection pool as a 3D bf16 view
+// [L slots][R rank rows][K] (slot stride = the pool's bytes per slot), boxes
+// of 8 rank rows x 64 k with the 128-byte swizzle: the shrink operand layout.
+bool make_map_pool_a(CUtensorMap *m, const void *pool, uint64_t K, uint64_t R, uint64_t L, uint64_t slot_bytes)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {K, R, L};
+    cuuint64_t strides[2] = {K * 2, slot_bytes};
+    cuuint32_t box[3] = {64, 8, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// The same pool (R a multiple of 8, K of 64) as a 5D view [L slots][K/64
+// chunks][R/8 groups][8 rows][64 k]: one box of 2^lg groups x nch chunks of
+// one slot lands chunk by chunk, each chunk's groups 1 KB apart, as the
+// shrink reads its A rows.
+bool make_map_pool_a5(CUtensorMap *m, const void *pool, uint64_t K, uint64_t R, uint64_t L, uint64_t slot_bytes,
+                      uint32_t groups, uint32_t nch)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[5] = {64, 8, R / 8, K / 64, L};
+    cuuint64_t strides[4] = {K * 2, K * 16, 128, slot_bytes};
+    cuuint32_t box[5] = {64, 8, groups, nch, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(pool), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Workspace of the one-launch kernel of up to 256 rows: the status words (and
+// the h arrival counter, in the same 256-byte block) and the routing export
+// where the general layout has them, then the partial h of every CTA and,
+// for the workspace sum, the K parts' tile flags and tiles.
+struct DecWs {
+    size_t perm, seg_off, hpart, pflags, gpart, core, total;
+};
+
+// `core` bytes serve the cluster-sum mode; `total` adds the K parts' fp32
+// tiles of the workspace-sum mode.
+DecWs dec_ws_layout(int M, int K, int N, int L, int R, int gated)
+{
+    DecWs l;
+    const size_t nf = (size_t)dec_flag_count(M, K, N, gated);
+    size_t o = 256;
+    l.perm = o;    o = align256(o + sizeof(int32_t) * (size_t)M);
+    l.seg_off = o; o = align256(o + sizeof(int32_t) * (size_t)(L + 2));
+    l.hpart = o;   o = align256(o + sizeof(float) * dec_hpart_floats(M, K, N, L, R, gated));
+    l.pflags = o;  o = align256(o + sizeof(unsigned long long) * nf);
+    l.core = o;
+    l.gpart = o;   o = align256(o + sizeof(float) * nf * (size_t)M * 128);
+    l.total = o;
+    return l;
+}
+
+constexpr int DEC_MAX_ROWS = 256;
+
 } // namespace
 
 namespace rd {
@@ -691,6 +775,87 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
     return ok();
 }
 
+// One-launch path of up to 256 rows (routing, shrink, base, expand and the
+// split-K sum in one kernel). `taken` stays false when the shape, the
+// workspace or the device does not suit it; the caller then takes the
+// general path.
+lora_status run_dec(const Params &p, const void *rt_pool, void *ws, size_t ws_bytes, int gated, int I,
+                    cudaStream_t st, const char *who, bool &taken)
+{
+    taken = false;
+    if (p.rows > DEC_MAX_ROWS || p.E != 1)
+        return LORA_OK;
+    // the gated weight view takes whole 64-row halves of each tile
+    if (gated && (p.K % 64 != 0 || I % 64 != 0))
+        return LORA_OK;
+    const int kc = dec_plan_kc(p.rows, p.K, p.N, p.L, p.R, gated, I);
+    if (kc == 0)
+        return LORA_OK;
+    const DecWs l = dec_ws_layout(p.rows, p.K, p.N, p.L, p.R, gated);
+    if (ws_bytes < l.core)
+        return LORA_OK;
+    DevInfo di;
+    if (!device_info(di))
+        return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
+    DecLaunch d;
+    memset(&d, 0, sizeof d);
+    const int tn = tc_token_tile(p.rows);
+    const bool use3d = p.K % 64 == 0;
+    bool okm = use3d ? make_map_3d(&d.maps.x, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride,
+                                   (uint32_t)tn, (uint32_t)kc)
+                     : make_map(&d.maps.x, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64,
+                                (uint32_t)tn);
+    if (okm)
+        okm = gated ? make_map_gated(&d.maps.w[0], p.W[0], (uint64_t)p.K, (uint64_t)I, (uint32_t)kc)
+                    : (use3d ? make_map_3d(&d.maps.w[0], p.W[0], (uint64_t)p.K, (uint64_t)p.N, (uint64_t)p.K, 128,
+                                           (uint32_t)kc)
+                             : make_map(&d.maps.w[0], p.W[0], (uint64_t)p.K, (uint64_t)p.N, (uint64_t)p.K, 64, 128));
+    if (!okm)
+        return fail(LORA_ERR_CUDA, "%s: encoding the tensor maps failed", who);
+    d.pool = rt_pool;
+    d.slot_bytes = slot_bytes(p.R, p.K, p.N);
+    if (!make_map_pool_a(&d.amap, rt_pool, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.L, (uint64_t)d.slot_bytes))
+        return fail(LORA_ERR_CUDA, "%s: encoding the A-row tensor map failed", who);
+    // one-copy A rows: boxes of 1..16 groups over the largest K part
+    d.gb_mask = 0;
+    if (use3d && p.R % 8 == 0) {
+        const int kch = p.K / 64, C = tc_csplit(p.rows, p.K, false);
+        const uint32_t nchb = (uint32_t)((kch + C - 1) / C);
+        for (int lg = 0; lg <= 4 && (8 << lg) <= p.R && nchb <= 256; ++lg)
+            if (make_map_pool_a5(&d.amap5[lg], rt_pool, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.L,
+                                 (uint64_t)d.slot_bytes, 1u << lg, nchb))
+                d.gb_mask |= 1 << lg;
+    }
+    uint8_t *b = static_cast<uint8_t *>(ws);
+    d.x = p.x;
+    d.x_stride = p.x_stride;
+    d.y = p.y;
+    d.y_stride = p.y_stride;
+    d.seq_slot = p.seq_slot;
+    d.M = p.rows;
+    d.K = p.K;
+    d.N = p.N;
+    d.L = p.L;
+    d.R = p.R;
+    d.gated = gated;
+    d.I = I;
+    d.yvec = ((reinterpret_cast<uintptr_t>(p.y) & 7u) == 0 && p.y_stride % 4 == 0) ? 1 : 0;
+    d.tab = p.tab[0];
+    d.status = reinterpret_cast<uint32_t *>(b);
+    d.perm = reinterpret_cast<int32_t *>(b + l.perm);
+    d.seg_off = reinterpret_cast<int32_t *>(b + l.seg_off);
+    d.hpart = reinterpret_cast<float *>(b + l.hpart);
+    d.pflags = reinterpret_cast<unsigned long long *>(b + l.pflags);
+    d.gpart = ws_bytes >= l.total ? reinterpret_cast<float *>(b + l.gpart) : nullptr;
+    cudaError_t e = launch_dec(d, di.num_sms, st);
+    if (e == cudaErrorNotSupported)
+        return LORA_OK;
+    taken = true;
+    if (e != cudaSuccess)
+        return cuda_fail(e, who);
+    return ok();
+}
+
 lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int N,
                        const int32_t *seq_slot, const lora_route *rt, void *y, int64_t y_stride,
                        void *ws, size_t ws_bytes, int path, lora_stream_t stream)
@@ -701,7 +866,7 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
         return s;
     if (M < 0)
         return fail(LORA_ERR_SHAPE, "%s: M %d is negative", who, M);
-    if (path < LORA_PATH_AUTO || path > LORA_PATH_TC)
+    if (path < LORA_PATH_AUTO || path > LORA_PATH_TC_ONE)
         return fail(LORA_ERR_RANGE, "%s: path %d is not one of LORA_PATH_*", who, path);
     if (K != rt->n_in || N != rt->n_out)
         return fail(LORA_ERR_SHAPE,
@@ -739,6 +904,19 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
     if (path == LORA_PATH_AUTO)
         path = M <= SIMT_MAX_ROWS ? LORA_PATH_SIMT : LORA_PATH_TC;
     p.tn = tc_token_tile(M);
+    // the workspace must hold what lora_proj_workspace_bytes asks for, whichever path runs
+    if (M > 0 && M <= DEC_MAX_ROWS) {
+        const size_t need = dec_ws_layout(M, K, N, p.L, p.R, 0).total;
+        if (ws_bytes < need)
+            return fail(LORA_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", who, ws_bytes, need);
+    }
+    if (path == LORA_PATH_TC_ONE) {
+        bool taken = false;
+        s = run_dec(p, rt->pool, ws, ws_bytes, 0, 0, reinterpret_cast<cudaStream_t>(stream), who, taken);
+        if (taken || s != LORA_OK)
+            return s;
+        path = LORA_PATH_TC;
+    }
     if (path == LORA_PATH_TC && M >= TC_SHRINK_MIN_ROWS) {
         p.kp = 1; // the tensor-core shrink writes h over the whole K
         p.no_units = 1;
@@ -757,8 +935,12 @@ size_t lora_proj_workspace_bytes(int M, const lora_route *rt)
     size_t part_elems = 0;
     int ncnt = 0;
     split_scratch(M, rt->n_in, rt->n_out, part_elems, ncnt);
-    return ws_layout(M, rt->max_loras + 1, rt->max_rank, shrink_kparts(rt->n_in), part_elems, ncnt)
-        .total;
+    size_t need = ws_layout(M, rt->max_loras + 1, rt->max_rank, shrink_kparts(rt->n_in), part_elems, ncnt).total;
+    if (M <= DEC_MAX_ROWS) {
+        const size_t d = dec_ws_layout(M, rt->n_in, rt->n_out, rt->max_loras, rt->max_rank, 0).total;
+        need = d > need ? d : need;
+    }
+    return need;
 }
 
 lora_status lora_proj_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int N,
@@ -789,6 +971,14 @@ lora_status lora_gate_up_apply(const void *x, int64_t x_stride, const void *W, i
                                const int32_t *seq_slot, const lora_route *rt, void *act, int64_t act_stride,
                                void *ws, size_t ws_bytes, lora_stream_t stream)
 {
+    return lora_gate_up_apply_ex(x, x_stride, W, M, K, I, seq_slot, rt, act, act_stride, ws, ws_bytes,
+                                 LORA_PATH_AUTO, stream);
+}
+
+lora_status lora_gate_up_apply_ex(const void *x, int64_t x_stride, const void *W, int M, int K, int I,
+                                  const int32_t *seq_slot, const lora_route *rt, void *act, int64_t act_stride,
+                                  void *ws, size_t ws_bytes, int path, lora_stream_t stream)
+{
     const char *who = "lora_gate_up_apply";
     lora_status s = check_route_kind(rt, LORA_ROUTE_PROJ, who);
     if (s != LORA_OK)
@@ -818,9 +1008,39 @@ lora_status lora_gate_up_apply(const void *x, int64_t x_stride, const void *W, i
     if (!device_info(di))
         return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
     const size_t proj_ws = align256(lora_proj_workspace_bytes(M, rt));
+    if (path < LORA_PATH_AUTO || path > LORA_PATH_TC_ONE)
+        return fail(LORA_ERR_RANGE, "%s: path %d is not one of LORA_PATH_*", who, path);
+    if (path == LORA_PATH_TC_ONE && M > SIMT_MAX_ROWS && M <= DEC_MAX_ROWS) {
+        // one launch: the sum of the K parts rounds both halves and writes act
+        if (W == nullptr || x == nullptr || seq_slot == nullptr)
+            return fail(LORA_ERR_NULL, "%s: x, W and seq_slot must be non-NULL", who);
+        if (!aligned16(W))
+            return fail(LORA_ERR_ALIGN, "%s: W must be 16-byte aligned", who);
+        if ((s = check_io(who, x, x_stride, M, K, I, seq_slot, act, act_stride)) != LORA_OK)
+            return s;
+        Params p;
+        memset(&p, 0, sizeof p);
+        p.x = static_cast<const uint16_t *>(x);
+        p.x_stride = x_stride;
+        p.y = static_cast<uint16_t *>(act);
+        p.y_stride = act_stride;
+        p.seq_slot = seq_slot;
+        p.E = 1;
+        p.rows = M;
+        p.K = K;
+        p.N = 2 * I;
+        p.L = rt->max_loras;
+        p.R = rt->max_rank;
+        p.W[0] = static_cast<const uint16_t *>(W);
+        p.tab[0] = tables_of(*rt);
+        bool taken = false;
+        s = run_dec(p, rt->pool, ws, proj_ws, 1, I, reinterpret_cast<cudaStream_t>(stream), who, taken);
+        if (taken || s != LORA_OK)
+            return s;
+    }
     uint16_t *gu = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + proj_ws);
     s = proj_apply(x, x_stride, W, M, K, 2 * I, seq_slot, rt, gu, 2 * (int64_t)I, ws, proj_ws,
-                   LORA_PATH_AUTO, stream);
+                   path == LORA_PATH_TC_ONE ? LORA_PATH_TC : path, stream);
     if (s != LORA_OK)
         return s;
     cudaError_t e = launch_silu_mul(gu, 2 * (int64_t)I, M, I, static_cast<uint16_t *>(act), act_stride,
@@ -1096,16 +1316,63 @@ lora_status lora_moe_gather_apply(const void *x, int64_t x_stride, const void *c
     return ok();
 }
 
+lora_status lora_proj_plan(int M, const lora_route *rt, int gated, lora_plan_info *info)
+{
+    const char *who = "lora_proj_plan";
+    if (info == nullptr)
+        return fail(LORA_ERR_NULL, "%s: info is NULL", who);
+    memset(info, 0, sizeof *info);
+    lora_status s = check_route_kind(rt, LORA_ROUTE_PROJ, who);
+    if (s != LORA_OK)
+        return s;
+    if (M < 0)
+        return fail(LORA_ERR_SHAPE, "%s: M %d is negative", who, M);
+    if (gated && rt->n_out % 2 != 0)
+        return fail(LORA_ERR_SHAPE, "%s: a gated plan needs an even n_out (%d)", who, rt->n_out);
+    if (M == 0)
+        return ok();
+    DevInfo di;
+    if (!device_info(di))
+        return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
+    const int K = rt->n_in, N = rt->n_out, I = gated ? N / 2 : 0;
+    if (M <= SIMT_MAX_ROWS) {
+        info->path = LORA_PLAN_SIMT;
+        info->kernels = gated ? 4 : 3;
+        return ok();
+    }
+    uint32_t smem = 0;
+    const bool one = M <= DEC_MAX_ROWS && (!gated || (K % 64 == 0 && I % 64 == 0)) &&
+                     dec_plan_info(M, K, N, rt->max_loras, rt->max_rank, gated, I, di.num_sms,
+                                   &info->clusters_needed, &info->clusters_resident, &info->cluster_size,
+                                   &smem) == 1;
+    info->smem_per_cta = (int)smem;
+    if (one) {
+        info->path = LORA_PLAN_ONE_LAUNCH;
+        info->kernels = 1;
+    } else {
+        info->path = LORA_PLAN_TC;
+        info->kernels = (M >= TC_SHRINK_MIN_ROWS ? 3 : 2) + (gated ? 1 : 0);
+    }
+    return ok();
+}
+
+void lora_test_wait_hook(uint64_t wait_ns, int extra_flags)
+{
+    dec_test_hook(wait_ns, extra_flags < 0 ? 0 : extra_flags);
+}
+
 lora_status lora_status_get(const void *ws, uint32_t *flags, lora_stream_t stream)
 {
     if (ws == nullptr || flags == nullptr)
         return fail(LORA_ERR_NULL, "lora_status_get: ws and flags must be non-NULL");
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaMemcpyAsync(flags, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+    uint32_t w[3] = {0, 0, 0}; // flags, tag of the call that set them, epoch
+    cudaError_t e = cudaMemcpyAsync(w, ws, sizeof w, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(st);
     if (e != cudaSuccess)
         return cuda_fail(e, "lora_status_get");
+    *flags = w[1] == status_tag(w[2] - 1u) ? w[0] : 0u;
     return ok();
 }
 

@@ -615,7 +615,7 @@ __device__ void local_route(const EmbedParams &p, int *seg, uint16_t *cnt, int *
         atomicOr(sflags, fl);
     __syncthreads();
     if (blockIdx.x == 0 && tid == 0)
-        *p.ws.status = *sflags;
+        status_begin(p.ws.status, *sflags);
 }
 
 } // namespace

@@ -89,6 +89,23 @@ struct WsLayout {
     size_t status, perm, seg_off, unit_off, done, h, hs, tiles, part, tile_cnt, total;
 };
 
+// Status words at the start of a workspace: [0] LORA_FLAG_* bits, [1] the
+// tag of the call that set them, [2] the epoch, which every call advances by
+// one. The tag of the call with epoch e is status_tag(e), so the bits belong
+// to the last call when [1] == status_tag([2] - 1); whatever else a fresh
+// workspace holds there (zeros, leftover integers) does not pass for a tag.
+__host__ __device__ inline uint32_t status_tag(uint32_t e) { return e ^ 0x6A09E667u; }
+
+// One thread of a call's first kernel opens the call's status this way.
+__device__ __forceinline__ void status_begin(uint32_t *st, uint32_t flags)
+{
+    volatile uint32_t *v = st;
+    const uint32_t e = v[2];
+    v[0] = flags;
+    v[1] = status_tag(e);
+    v[2] = e + 1;
+}
+
 // Upper bound on token tiles: each expert adds at most one partial tile.
 __host__ __device__ inline int max_token_tiles(int rows, int E) { return rows / 16 + E + 1; }
 
@@ -245,6 +262,46 @@ cudaError_t launch_gather_combine(const GatherParams &p, int num_sms, cudaStream
 // act[i][n] = silu(y[i][n]) * y[i][I + n] (lora_act.cu).
 cudaError_t launch_silu_mul(const uint16_t *y, int64_t y_stride, int M, int I, uint16_t *act,
                             int64_t act_stride, int num_sms, cudaStream_t st);
+
+// One-launch projection of up to 256 rows (lora_dec.cu): the routing, the
+// tensor-core shrink inside the base K loop, the h exchange through the
+// workspace, the expand and the split-K sum over a thread-block cluster.
+struct DecLaunch {
+    TmapSet maps;            // x: boxes [kc][tn][64] (3D) or [tn][64]; W: [kc][128][64], or the gated 4D view
+    const uint16_t *x;
+    int64_t x_stride;
+    uint16_t *y;             // y [M][N], or act [M][I] when gated
+    int64_t y_stride;
+    const int32_t *seq_slot;
+    int M, K, N, L, R;
+    int gated, I;            // gated: W is [gate I | up I] and y receives act = silu(g) * u
+    int yvec;                // y / act 8-byte aligned with y_stride a multiple of 4
+    Tables tab;
+    uint32_t *status;        // [0] flags, [1] tag, [2] epoch, u64 [8] h arrival counter (workspace)
+    int32_t *perm, *seg_off; // routing export
+    float *hpart;            // dec_hpart_floats(...) floats
+    float *gpart;            // dec_flag_count(...) * M * 128 floats, or null (the workspace sum then cannot run)
+    unsigned long long *pflags; // dec_flag_count(...) words
+    CUtensorMap amap;        // the pool's A rows: [L slots][R rank rows][K], boxes of 8 rows x 64 k
+    CUtensorMap amap5[5];    // the same, boxes of 2^lg 8-row groups over a whole K part (bit lg of gb_mask: encoded)
+    int gb_mask;
+    const void *pool;        // the route's pool and its bytes per slot (where the A rows of slot s lie)
+    size_t slot_bytes;
+};
+// K chunks per pipeline stage the kernel would take (0: the shape does not fit it).
+int dec_plan_kc(int M, int K, int N, int L, int R, int gated, int I);
+size_t dec_hpart_floats(int M, int K, int N, int L, int R, int gated);
+// 1 when a call of this shape takes the one-launch kernel on the current
+// device: the clusters it needs, how many can be resident at once, their
+// size (the K parts) and the shared memory of one CTA.
+int dec_plan_info(int M, int K, int N, int L, int R, int gated, int I, int num_sms, int *clusters_needed,
+                  int *clusters_resident, int *cluster_size, uint32_t *smem);
+int dec_flag_count(int M, int K, int N, int gated);
+// cudaErrorNotSupported: the shape or the device does not take this kernel.
+cudaError_t launch_dec(const DecLaunch &d, int num_sms, cudaStream_t st);
+// Test hook: the exchange wait gives up after wait_ns and waits for
+// extra_flags flags that no CTA writes (0, 0: normal operation).
+void dec_test_hook(uint64_t wait_ns, int extra_flags);
 
 // Record `msg` as the thread's last error and return `code` (lora_api.cu).
 lora_status api_fail(lora_status code, const char *msg);

@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
         for (int e = 0; e < p.E; ++e)
             etiles[e + 1] += etiles[e];
         p.ws.tiles[0] = min(etiles[p.E], cap);
-        *p.ws.status = flags;
+        status_begin(p.ws.status, flags);
     }
     __syncthreads();
     if (tid < p.E) {

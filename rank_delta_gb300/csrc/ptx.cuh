@@ -102,6 +102,13 @@ __device__ __forceinline__ void cp_async_wait_all()
 
 // Arrive on `bar` once every cp.async this thread issued so far has landed
 // (the arrival is counted in the barrier's expected count: no increment).
+// The barrier waits for this thread's earlier cp.async as well (its pending
+// count rises by one now and falls when they complete: no arrival of its own).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar)
 {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -121,6 +128,19 @@ template <int N> __device__ __forceinline__ void cp_async_wait_group()
 // ------------------------------------------------------------ bulk groups
 // Close this thread's current group of bulk (TMA) stores.
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// 1D bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from shared to global memory, in this thread's current bulk group.
+__device__ __forceinline__ void bulk_store_1d(void *gdst, const void *ssrc, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Order this thread's async-proxy global writes (bulk copies it has waited
+// for) before its later generic-proxy operations, such as a release.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // This thread's bulk stores are complete (their writes performed).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

@@ -37,17 +37,22 @@ def qkv():
     return ProjRun(workloads.make("qkv"))
 
 
-def test_qkv_matches_oracle_on_every_row(qkv):
-    y = qkv.apply()
+PATHS = [rd.LORA_PATH_AUTO, rd.LORA_PATH_TC_ONE]
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_qkv_matches_oracle_on_every_row(qkv, path):
+    y = qkv.apply(path=path)
     assert qkv.last_status == 0
     assert_all_rows(y, oracle.workload_proj(qkv.wl), "qkv")
 
 
-def test_qkv_fused_equals_three_split_calls(qkv):
+@pytest.mark.parametrize("path", PATHS)
+def test_qkv_fused_equals_three_split_calls(qkv, path):
     """One A per adapter, B rows split q/k/v: the fused call's bytes equal the
     stacked split calls' bytes (frink lora_attach.rs module doc)."""
     wl = qkv.wl
-    fused = qkv.apply()
+    fused = qkv.apply(path=path)
     parts = []
     row0 = 0
     for n in wl.splits:
@@ -56,15 +61,16 @@ def test_qkv_fused_equals_three_split_calls(qkv):
             np.ascontiguousarray(wl.W[row0:row0 + n]), wl.x, wl.seq_slot,
             [workloads.Adapter(a.A, np.ascontiguousarray(a.B[row0:row0 + n]), a.rank, a.alpha,
                                a.use_rslora, a.adapter_scale) for a in wl.adapters])
-        parts.append(ProjRun(sub).apply())
+        parts.append(ProjRun(sub).apply(path=path))
         row0 += n
     assert np.array_equal(fused, np.concatenate(parts, axis=1))
 
 
-def test_qkv_no_delta_rows_are_base_bytes(qkv):
+@pytest.mark.parametrize("path", PATHS)
+def test_qkv_no_delta_rows_are_base_bytes(qkv, path):
     wl = qkv.wl
-    y = qkv.apply()
-    base = qkv.apply(slots=torch.full_like(qkv.slots, -1))
+    y = qkv.apply(path=path)
+    base = qkv.apply(slots=torch.full_like(qkv.slots, -1), path=path)
     scales = np.array([oracle.scale(a.alpha, a.rank, a.use_rslora, a.adapter_scale)
                        for a in wl.adapters])
     none = (wl.seq_slot < 0) | (scales[np.maximum(wl.seq_slot, 0)] == 0.0)

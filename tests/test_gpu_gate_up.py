@@ -42,13 +42,13 @@ class GateUpRun:
         self.route.pack_all(wl.adapters)
         self.ws = th.workspace(rd.lora_gate_up_workspace_bytes(wl.M, self.route.rt))
 
-    def apply(self, slots=None, act_stride=None):
+    def apply(self, slots=None, act_stride=None, path=rd.LORA_PATH_AUTO):
         wl, I = self.wl, self.I
         st = I if act_stride is None else act_stride
         act = torch.full((wl.M, st), SENTINEL, dtype=torch.int16, device="cuda")
         rd.lora_gate_up_apply(self.x, self.x.stride(0), self.W, wl.M, wl.K, I,
                               self.slots if slots is None else slots, self.route.rt, act, st, self.ws,
-                              self.ws.numel())
+                              self.ws.numel(), path=path)
         torch.cuda.synchronize()
         self.last_status = rd.lora_status_get(self.ws)
         return th.to_numpy_bf16(act.view(torch.bfloat16)[:, :I])
@@ -85,21 +85,25 @@ def _no_delta_rows(wl):
     (9, 64, 24, 3, 16),     # CUDA-core path, I a multiple of 8
     (37, 128, 100, 4, 8),   # tensor-core path, I not a multiple of 8 (scalar activation)
     (300, 256, 136, 5, 32), # several token tiles
+    (48, 128, 64, 4, 16),   # K and I multiples of 64: the one-launch kernel's fused act
 ])
-def test_gate_up_matches_oracle(M, K, I, L, R):
+@pytest.mark.parametrize("path", [rd.LORA_PATH_AUTO, rd.LORA_PATH_TC_ONE])
+def test_gate_up_matches_oracle(M, K, I, L, R, path):
     wl = workloads.random_small(40 + M, M=M, K=K, N=2 * I, L=L, R=R)
     run = GateUpRun(wl)
-    act = run.apply()
+    act = run.apply(path=path)
     assert run.last_status == 0
     assert_close_act(act, oracle.proj(wl.x, wl.W, wl.seq_slot, wl.adapters), I, f"gate_up {M}x{K}x{I}")
 
 
-def test_gate_up_decode_shapes_and_no_delta_rows():
+@pytest.mark.parametrize("path", [rd.LORA_PATH_AUTO, rd.LORA_PATH_TC_ONE])
+def test_gate_up_decode_shapes_and_no_delta_rows(path):
     wl = workloads.make("decode")  # W [4096][4096] read as gate 2048 | up 2048
     run = GateUpRun(wl)
-    act = run.apply()
+    act = run.apply(path=path)
+    assert run.last_status == 0
     assert_close_act(act, oracle.proj(wl.x, wl.W, wl.seq_slot, wl.adapters), run.I, "gate_up decode")
-    base = run.apply(slots=torch.full_like(run.slots, -1))
+    base = run.apply(slots=torch.full_like(run.slots, -1), path=path)
     rows = _no_delta_rows(wl)
     assert rows
     assert np.array_equal(act[rows], base[rows])
@@ -114,8 +118,10 @@ def test_gate_up_prefill_shapes_sampled():
     assert_close_act(act[rows], ref, run.I, "gate_up prefill (sampled rows)")
 
 
-def test_gate_up_strided_output():
+@pytest.mark.parametrize("path", [rd.LORA_PATH_AUTO, rd.LORA_PATH_TC_ONE])
+def test_gate_up_strided_output(path):
     wl = workloads.random_small(77, M=20, K=64, N=2 * 40, L=2, R=8)
     run = GateUpRun(wl)
-    a = run.apply(act_stride=48)
+    a = run.apply(act_stride=48, path=path)
+    assert run.last_status == 0
     assert_close_act(a, oracle.proj(wl.x, wl.W, wl.seq_slot, wl.adapters), 40, "gate_up strided")

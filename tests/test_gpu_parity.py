@@ -18,7 +18,7 @@ from tests.gpu_common import ProjRun, assert_close
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [rd.LORA_PATH_SIMT, rd.LORA_PATH_TC]
+PATHS = [rd.LORA_PATH_SIMT, rd.LORA_PATH_TC, rd.LORA_PATH_TC_ONE]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -305,7 +305,7 @@ class ProjSet:
         self.route = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.K, wl.N)
         self.route.pack_all(wl.adapters)
         self.y = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
-        self.ws = th.workspace(rd.lora_proj_workspace_bytes(wl.M, self.route.rt))
+        self.ws = th.workspace(rd.lora_proj_workspace_bytes(wl.M, self.route.rt, PROJ_PATH[0]))
         self.bytes = (self.W.numel() * 2 + self.route.pool_bytes + self.x.numel() * 2 +
                       self.y.numel() * 2)
 
@@ -415,7 +415,7 @@ class StackSet(ProjSet):
         for s, st in enumerate(wl.stacks):
             self.route.pack_stack(s, st)
         self.y = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device="cuda")
-        self.ws = th.workspace(rd.lora_proj_workspace_bytes(wl.M, self.route.rt))
+        self.ws = th.workspace(rd.lora_proj_workspace_bytes(wl.M, self.route.rt, PROJ_PATH[0]))
         self.bytes = (self.W.numel() * 2 + self.route.pool_bytes + self.x.numel() * 2 +
                       self.y.numel() * 2)
 

@@ -270,13 +270,20 @@ lora_status lora_select_victim_slot(const lora_slot_view *cache, int n, int32_t 
 /*
  * Workspace of lora_proj_apply for M rows on route `rt` (device scratch the
  * caller provides: the routing sort, the shrink work list, the rank-sized h of
- * every row, handoff counters or the exchange flags of the one-launch kernel,
- * and the status words). Its contents need no initialisation: every call
- * tags what it waits on with an epoch kept in the workspace. 256-byte aligned
- * sections; the caller passes a buffer of at least this many bytes, 256-byte
- * aligned. Returns 0 if rt is NULL or not initialised.
+ * every row, split-K partial tiles and handoff counters, and the status
+ * words). Its contents need no initialisation: every call tags what it waits
+ * on with an epoch kept in the workspace. 256-byte aligned sections; the
+ * caller passes a buffer of at least this many bytes, 256-byte aligned.
+ * Returns 0 if rt is NULL or not initialised.
  */
 size_t lora_proj_workspace_bytes(int M, const lora_route *rt);
+
+/* The workspace a call on an explicit path needs (LORA_PATH_*): for
+ * LORA_PATH_TC_ONE and up to 256 rows, the larger of the general workspace
+ * and the one-launch kernel's (its h exchange, and the K parts' fp32 tiles
+ * for the cooperative launch); otherwise lora_proj_workspace_bytes. With less,
+ * LORA_PATH_TC_ONE calls take LORA_PATH_TC. */
+size_t lora_proj_workspace_bytes_ex(int M, const lora_route *rt, int path);
 
 /*
  * y[i, :] = W x_i + s * B_s (A_s x_i), s = seq_slot[i], for i in [0, M)
@@ -326,7 +333,13 @@ lora_status lora_proj_apply_ex(const void *x, int64_t x_stride, const void *W, i
  * the workspace: the kernels use a fixed LORA_STATIC_WS_BYTES array compiled
  * into the library instead, and nothing is allocated. Calls whose workspace
  * need (lora_proj_workspace_bytes(M, rt)) exceeds LORA_STATIC_WS_BYTES are
- * refused with LORA_ERR_UNSUPPORTED and a message giving both sizes.
+ * refused with LORA_ERR_UNSUPPORTED and a message giving both sizes. The need
+ * is the split-K partial tiles of up to 256 rows (K parts x 128 features x
+ * rows x 4 bytes per 128 features) or the rank-sized h of larger batches: the
+ * tiny, decode (64 x 4096 x 4096, 16 slots, rank 64: 5.2 MB) and prefill
+ * (8192 x 4096 x 14336: 5.3 MB) shapes fit; fused QKV at 256 rows (6144
+ * outputs: 18.9 MB) and decode rows on 14336 outputs (64 rows: 14.7 MB) do
+ * not -- they need a caller workspace.
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture. All calls
  * on a device share the array: calls that can overlap on the GPU race, so
@@ -356,6 +369,9 @@ lora_status lora_proj_apply_static_ws(const void *x, int64_t x_stride, const voi
  * of lora_proj_apply, a route whose n_out is not 2I, act_stride < I.
  */
 size_t lora_gate_up_workspace_bytes(int M, const lora_route *rt);
+/* The workspace of lora_gate_up_apply_ex on `path` (the projection's part
+ * sized by lora_proj_workspace_bytes_ex). */
+size_t lora_gate_up_workspace_bytes_ex(int M, const lora_route *rt, int path);
 lora_status lora_gate_up_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int I,
                                const int32_t *seq_slot, const lora_route *rt, void *act,
                                int64_t act_stride, void *ws, size_t ws_bytes, lora_stream_t stream);

@@ -120,11 +120,13 @@ _SIGNATURES = {
     "lora_set_scales": (_i, [_rtp, _i32p, ctypes.POINTER(ctypes.c_float), _i, _vp]),
     "lora_select_victim_slot": (_i, [ctypes.POINTER(lora_slot_view), _i, _i32p]),
     "lora_proj_workspace_bytes": (_sz, [_i, _rtp]),
+    "lora_proj_workspace_bytes_ex": (_sz, [_i, _rtp, _i]),
     "lora_proj_apply": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_proj_apply_ex": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _i,
                                 _vp]),
     "lora_proj_apply_static_ws": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp]),
     "lora_gate_up_workspace_bytes": (_sz, [_i, _rtp]),
+    "lora_gate_up_workspace_bytes_ex": (_sz, [_i, _rtp, _i]),
     "lora_gate_up_apply": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_gate_up_apply_ex": (_i, [_vp, _i64, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _i, _vp]),
     "lora_moe_workspace_bytes": (_sz, [_i, _i, _rtp]),
@@ -262,8 +264,10 @@ def lora_select_victim_slot(cache) -> int:
     return int(out.value)
 
 
-def lora_proj_workspace_bytes(M: int, rt: lora_route) -> int:
-    return int(lib().lora_proj_workspace_bytes(M, ctypes.byref(rt)))
+def lora_proj_workspace_bytes(M: int, rt: lora_route, path: int = LORA_PATH_AUTO) -> int:
+    if path == LORA_PATH_AUTO:
+        return int(lib().lora_proj_workspace_bytes(M, ctypes.byref(rt)))
+    return int(lib().lora_proj_workspace_bytes_ex(M, ctypes.byref(rt), path))
 
 
 def lora_proj_apply(x, x_stride: int, W, M: int, K: int, N: int, seq_slot, rt: lora_route, y,
@@ -287,8 +291,10 @@ def lora_proj_apply_static_ws(x, x_stride: int, W, M: int, K: int, N: int, seq_s
                                            ctypes.byref(rt), _ptr(y), y_stride, _stream(stream)))
 
 
-def lora_gate_up_workspace_bytes(M: int, rt: lora_route) -> int:
-    return int(lib().lora_gate_up_workspace_bytes(M, ctypes.byref(rt)))
+def lora_gate_up_workspace_bytes(M: int, rt: lora_route, path: int = LORA_PATH_AUTO) -> int:
+    if path == LORA_PATH_AUTO:
+        return int(lib().lora_gate_up_workspace_bytes(M, ctypes.byref(rt)))
+    return int(lib().lora_gate_up_workspace_bytes_ex(M, ctypes.byref(rt), path))
 
 
 def lora_gate_up_apply(x, x_stride: int, W, M: int, K: int, I: int, seq_slot, rt: lora_route, act,

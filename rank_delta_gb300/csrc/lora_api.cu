@@ -904,12 +904,6 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
     if (path == LORA_PATH_AUTO)
         path = M <= SIMT_MAX_ROWS ? LORA_PATH_SIMT : LORA_PATH_TC;
     p.tn = tc_token_tile(M);
-    // the workspace must hold what lora_proj_workspace_bytes asks for, whichever path runs
-    if (M > 0 && M <= DEC_MAX_ROWS) {
-        const size_t need = dec_ws_layout(M, K, N, p.L, p.R, 0).total;
-        if (ws_bytes < need)
-            return fail(LORA_ERR_WORKSPACE, "%s: workspace of %zu bytes, %zu needed", who, ws_bytes, need);
-    }
     if (path == LORA_PATH_TC_ONE) {
         bool taken = false;
         s = run_dec(p, rt->pool, ws, ws_bytes, 0, 0, reinterpret_cast<cudaStream_t>(stream), who, taken);
@@ -935,8 +929,13 @@ size_t lora_proj_workspace_bytes(int M, const lora_route *rt)
     size_t part_elems = 0;
     int ncnt = 0;
     split_scratch(M, rt->n_in, rt->n_out, part_elems, ncnt);
-    size_t need = ws_layout(M, rt->max_loras + 1, rt->max_rank, shrink_kparts(rt->n_in), part_elems, ncnt).total;
-    if (M <= DEC_MAX_ROWS) {
+    return ws_layout(M, rt->max_loras + 1, rt->max_rank, shrink_kparts(rt->n_in), part_elems, ncnt).total;
+}
+
+size_t lora_proj_workspace_bytes_ex(int M, const lora_route *rt, int path)
+{
+    size_t need = lora_proj_workspace_bytes(M, rt);
+    if (need > 0 && path == LORA_PATH_TC_ONE && M <= DEC_MAX_ROWS) {
         const size_t d = dec_ws_layout(M, rt->n_in, rt->n_out, rt->max_loras, rt->max_rank, 0).total;
         need = d > need ? d : need;
     }
@@ -965,6 +964,14 @@ size_t lora_gate_up_workspace_bytes(int M, const lora_route *rt)
         return 0;
     // the projection's workspace, then its [M][2I] bf16 output
     return align256(lora_proj_workspace_bytes(M, rt)) + align256((size_t)M * (size_t)rt->n_out * 2);
+}
+
+size_t lora_gate_up_workspace_bytes_ex(int M, const lora_route *rt, int path)
+{
+    const size_t base = lora_gate_up_workspace_bytes(M, rt);
+    if (base == 0)
+        return 0;
+    return align256(lora_proj_workspace_bytes_ex(M, rt, path)) + align256((size_t)M * (size_t)rt->n_out * 2);
 }
 
 lora_status lora_gate_up_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int I,
@@ -1004,12 +1011,16 @@ lora_status lora_gate_up_apply_ex(const void *x, int64_t x_stride, const void *W
     if (ws_bytes < need)
         return fail(LORA_ERR_WORKSPACE, "%s: workspace has %zu bytes, needs %zu (%d rows, 2I = %d)", who,
                     ws_bytes, need, M, 2 * I);
+    if (path < LORA_PATH_AUTO || path > LORA_PATH_TC_ONE)
+        return fail(LORA_ERR_RANGE, "%s: path %d is not one of LORA_PATH_*", who, path);
+    // the one-launch kernel needs its own workspace ahead of the act scratch;
+    // with less, the call takes the tensor-core path
+    if (path == LORA_PATH_TC_ONE && ws_bytes < lora_gate_up_workspace_bytes_ex(M, rt, path))
+        path = LORA_PATH_TC;
     DevInfo di;
     if (!device_info(di))
         return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
-    const size_t proj_ws = align256(lora_proj_workspace_bytes(M, rt));
-    if (path < LORA_PATH_AUTO || path > LORA_PATH_TC_ONE)
-        return fail(LORA_ERR_RANGE, "%s: path %d is not one of LORA_PATH_*", who, path);
+    const size_t proj_ws = align256(lora_proj_workspace_bytes_ex(M, rt, path));
     if (path == LORA_PATH_TC_ONE && M > SIMT_MAX_ROWS && M <= DEC_MAX_ROWS) {
         // one launch: the sum of the K parts rounds both halves and writes act
         if (W == nullptr || x == nullptr || seq_slot == nullptr)

@@ -43,10 +43,11 @@ class ProjRun:
         self.slots = torch.from_numpy(np.ascontiguousarray(wl.seq_slot, np.int32)).to(device)
         self.route = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.K, wl.N, device)
         self.route.pack_all(wl.adapters)
-        self.ws = th.workspace(rd.lora_proj_workspace_bytes(wl.M, self.route.rt), device)
+        # sized for every path (the one-launch kernel's workspace is the larger)
+        self.ws = th.workspace(rd.lora_proj_workspace_bytes(wl.M, self.route.rt, rd.LORA_PATH_TC_ONE), device)
         self.device = device
 
-    def apply(self, slots=None, path=rd.LORA_PATH_AUTO, x=None, rows=None):
+    def apply(self, slots=None, path=rd.LORA_PATH_AUTO, x=None, rows=None, ws_bytes=None):
         wl = self.wl
         x = self.x if x is None else x
         M = x.shape[0]
@@ -54,9 +55,10 @@ class ProjRun:
         y = torch.full((M, wl.N), 0, dtype=torch.int16, device=self.device)
         y.fill_(SENTINEL)
         y = y.view(torch.bfloat16)
-        ws = self.ws if M <= wl.M else th.workspace(rd.lora_proj_workspace_bytes(M, self.route.rt))
+        ws = self.ws if M <= wl.M else th.workspace(rd.lora_proj_workspace_bytes(M, self.route.rt,
+                                                                                   rd.LORA_PATH_TC_ONE))
         rd.lora_proj_apply(x, x.stride(0), self.W, M, wl.K, wl.N, s, self.route.rt, y, y.stride(0),
-                           ws, ws.numel(), None, path)
+                           ws, ws.numel() if ws_bytes is None else ws_bytes, None, path)
         torch.cuda.synchronize()
         self.last_status = rd.lora_status_get(ws)
         return th.to_numpy_bf16(y)

@@ -290,6 +290,23 @@ def test_pack_stack_refusals_name_the_problem():
     expect(rd.LORA_ERR_UNSUPPORTED, rd.lora_pool_pack_stack, emb, 0, [A], [B], [8], [16.0], [0], [1.0])
 
 
+def test_workspace_sizes_by_path():
+    """The one-launch path sizes its own exchange workspace for up to 256 rows;
+    every other path, and larger batches, the general one."""
+    rt = fake_route(L=32, R=16, K=4096, N=6144)
+    for M in (17, 64, 256):
+        base = rd.lora_proj_workspace_bytes(M, rt)
+        one = rd.lora_proj_workspace_bytes(M, rt, rd.LORA_PATH_TC_ONE)
+        assert one >= base > 0
+        assert rd.lora_proj_workspace_bytes(M, rt, rd.LORA_PATH_TC) == base
+        assert rd.lora_proj_workspace_bytes(M, rt, rd.LORA_PATH_SIMT) == base
+        gu = rd.lora_gate_up_workspace_bytes(M, rt)
+        assert rd.lora_gate_up_workspace_bytes(M, rt, rd.LORA_PATH_TC_ONE) - gu == (one + 255) // 256 * 256 - (base + 255) // 256 * 256
+    # fused QKV at 256 rows: the cooperative launch's K-part tiles make it larger
+    assert rd.lora_proj_workspace_bytes(256, rt, rd.LORA_PATH_TC_ONE) > rd.lora_proj_workspace_bytes(256, rt)
+    assert rd.lora_proj_workspace_bytes(300, rt, rd.LORA_PATH_TC_ONE) == rd.lora_proj_workspace_bytes(300, rt)
+
+
 def test_static_workspace_refuses_calls_that_outgrow_it():
     rt = fake_route(L=16, R=64, K=4096, N=4096)
     M = 20000

@@ -78,6 +78,17 @@ def test_qkv_no_delta_rows_are_base_bytes(qkv, path):
     assert np.array_equal(y[none], base[none])
 
 
+def test_one_launch_path_with_the_default_workspace_is_the_tensor_core_path(qkv):
+    """LORA_PATH_TC_ONE given only the default path's workspace runs the
+    tensor-core path instead: the same bytes as LORA_PATH_TC."""
+    need = rd.lora_proj_workspace_bytes(qkv.wl.M, qkv.route.rt)
+    assert need < rd.lora_proj_workspace_bytes(qkv.wl.M, qkv.route.rt, rd.LORA_PATH_TC_ONE)
+    y_tc = qkv.apply(path=rd.LORA_PATH_TC)
+    y_one = qkv.apply(path=rd.LORA_PATH_TC_ONE, ws_bytes=need)
+    assert qkv.last_status == 0
+    assert np.array_equal(y_one, y_tc)
+
+
 @pytest.fixture(scope="module")
 def prefill():
     run = ProjRun(workloads.make("prefill"))

@@ -40,7 +40,7 @@ class GateUpRun:
         self.slots = torch.from_numpy(np.ascontiguousarray(wl.seq_slot, np.int32)).cuda()
         self.route = th.DeviceRoute(wl.max_loras, wl.max_rank, wl.K, wl.N)
         self.route.pack_all(wl.adapters)
-        self.ws = th.workspace(rd.lora_gate_up_workspace_bytes(wl.M, self.route.rt))
+        self.ws = th.workspace(rd.lora_gate_up_workspace_bytes(wl.M, self.route.rt, rd.LORA_PATH_TC_ONE))
 
     def apply(self, slots=None, act_stride=None, path=rd.LORA_PATH_AUTO):
         wl, I = self.wl, self.I

@@ -753,7 +753,9 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
                 return cuda_fail(e, who);
         }
         for (int q = 0; q < p.E; ++q) {
-            if (plan.use3d)
+            if (p.gated)
+                ok = make_map_gated(&maps.w[q], p.W[q], (uint64_t)p.K, (uint64_t)p.I, (uint32_t)plan.kc);
+            else if (plan.use3d)
                 ok = make_map_3d(&maps.w[q], p.W[q], (uint64_t)p.K, (uint64_t)p.N, (uint64_t)p.K, 128,
                                  (uint32_t)plan.kc);
             else
@@ -763,11 +765,19 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
         }
         // y by TMA stores where its layout allows (16-byte aligned rows);
         // otherwise the epilogue stores y element by element
-        p.ystore_ok = (aligned16(p.y) && p.y_stride % 8 == 0 &&
-                       make_map_plain(&maps.y, p.y, (uint64_t)p.N, (uint64_t)p.rows, (uint64_t)p.y_stride, 128,
-                                      (uint32_t)YSTORE_ROWS))
-                          ? 1
-                          : 0;
+        if (p.gated) // act [rows][I], boxes of 64 act features x 64 rows
+            p.ystore_ok = make_map_plain(&maps.y, p.y, (uint64_t)p.I, (uint64_t)p.rows, (uint64_t)p.y_stride, 64,
+                                         (uint32_t)YSTORE_ROWS)
+                              ? 1
+                              : 0;
+        else
+            p.ystore_ok = (aligned16(p.y) && p.y_stride % 8 == 0 &&
+                           make_map_plain(&maps.y, p.y, (uint64_t)p.N, (uint64_t)p.rows, (uint64_t)p.y_stride,
+                                          128, (uint32_t)YSTORE_ROWS))
+                              ? 1
+                              : 0;
+        if (p.gated && !p.ystore_ok)
+            return fail(LORA_ERR_CUDA, "%s: encoding the act tensor map failed", who);
         e = launch_tc(p, maps, plan, di.num_sms, st);
     }
     if (e != cudaSuccess)
@@ -856,9 +866,12 @@ lora_status run_dec(const Params &p, const void *rt_pool, void *ws, size_t ws_by
     return ok();
 }
 
+// gated_I > 0: W is the fused [gate I | up I] (N = 2I) and y receives act
+// [M][gated_I] from the tensor-core kernel's drain (the caller has checked
+// that the shape takes it: tc_gated_ok).
 lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, int K, int N,
                        const int32_t *seq_slot, const lora_route *rt, void *y, int64_t y_stride,
-                       void *ws, size_t ws_bytes, int path, lora_stream_t stream)
+                       void *ws, size_t ws_bytes, int path, lora_stream_t stream, int gated_I = 0)
 {
     const char *who = "lora_proj_apply";
     lora_status s = check_route_kind(rt, LORA_ROUTE_PROJ, who);
@@ -878,7 +891,7 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
         return fail(LORA_ERR_NULL, "%s: W is NULL", who);
     if (!aligned16(W))
         return fail(LORA_ERR_ALIGN, "%s: W must be 16-byte aligned", who);
-    if ((s = check_io(who, x, x_stride, M, K, N, seq_slot, y, y_stride)) != LORA_OK)
+    if ((s = check_io(who, x, x_stride, M, K, gated_I > 0 ? gated_I : N, seq_slot, y, y_stride)) != LORA_OK)
         return s;
     Params p;
     memset(&p, 0, sizeof p);
@@ -886,6 +899,8 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
     p.x_stride = x_stride;
     p.y = static_cast<uint16_t *>(y);
     p.y_stride = y_stride;
+    p.gated = gated_I > 0 ? 1 : 0;
+    p.I = gated_I;
     p.seq_slot = seq_slot;
     p.expert_offsets = nullptr;
     p.E = 1;
@@ -1048,6 +1063,24 @@ lora_status lora_gate_up_apply_ex(const void *x, int64_t x_stride, const void *W
         s = run_dec(p, rt->pool, ws, proj_ws, 1, I, reinterpret_cast<cudaStream_t>(stream), who, taken);
         if (taken || s != LORA_OK)
             return s;
+    }
+    // several token tiles (one K part): the tensor-core kernel reads W as 64
+    // gate + 64 up rows per tile and writes act from its drain
+    if (path != LORA_PATH_SIMT && M > DEC_MAX_ROWS && aligned16(act) && act_stride % 8 == 0) {
+        Params q;
+        memset(&q, 0, sizeof q);
+        q.rows = M;
+        q.K = K;
+        q.N = 2 * I;
+        q.I = I;
+        q.gated = 1;
+        q.E = 1;
+        q.L = rt->max_loras;
+        q.R = rt->max_rank;
+        q.tn = tc_token_tile(M);
+        if (tc_gated_ok(q))
+            return proj_apply(x, x_stride, W, M, K, 2 * I, seq_slot, rt, act, act_stride, ws, proj_ws,
+                              LORA_PATH_TC, stream, I);
     }
     uint16_t *gu = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + proj_ws);
     s = proj_apply(x, x_stride, W, M, K, 2 * I, seq_slot, rt, gu, 2 * (int64_t)I, ws, proj_ws,

@@ -80,6 +80,8 @@ struct Params {
     int no_units; // 1: h comes from the tensor-core shrink kernel (no shrink work units)
     int max_tiles; // token tiles the routing kernel may list (0: the workspace bound)
     int ystore_ok; // 1: maps.y is encoded (y 16-byte aligned, y_stride a multiple of 8)
+    int gated, I;  // 1: W is the fused [gate I | up I] (N = 2I) read as tiles of 64 gate + 64 up rows,
+                   // and y receives act = silu(g) * u, [rows][I] (one K part, TMA stores only)
     const uint16_t *W[MAX_E];
     Tables tab[MAX_E];
     Ws ws;
@@ -299,6 +301,9 @@ int dec_plan_info(int M, int K, int N, int L, int R, int gated, int I, int num_s
 int dec_flag_count(int M, int K, int N, int gated);
 // cudaErrorNotSupported: the shape or the device does not take this kernel.
 cudaError_t launch_dec(const DecLaunch &d, int num_sms, cudaStream_t st);
+// 1 when the tensor-core kernel can take this gated call (W the fused
+// [gate | up], act written from its drain): see launch_tc.
+bool tc_gated_ok(const Params &p);
 // Test hook: the exchange wait gives up after wait_ns and waits for
 // extra_flags flags that no CTA writes (0, 0: normal operation).
 void dec_test_hook(uint64_t wait_ns, int extra_flags);

@@ -220,7 +220,11 @@ __device__ __forceinline__ void produce(const TmapSet &maps, const Params &p, co
             uint8_t *stage = smem + (size_t)slot * c.stage_bytes;
             mbar_arrive_expect_tx(bars->full + slot, (uint32_t)c.kc * (W_CHUNK_BYTES + c.x_chunk));
             uint8_t *xdst = stage + (size_t)c.kc * W_CHUNK_BYTES;
-            if (c.use3d) {
+            if (p.gated) {
+                // [chunks][2 halves][I rows][64]: gate rows n0/2.. then up rows I + n0/2..
+                tma_load_4d(stage, &maps.w[0], 0, ti.n0 >> 1, 0, ks * c.kc, bars->full + slot);
+                tma_load_3d(xdst, &maps.x, 0, ti.r0, ks * c.kc, bars->full + slot);
+            } else if (c.use3d) {
                 tma_load_3d(stage, &maps.w[ti.e], 0, ti.n0, ks * c.kc, bars->full + slot);
                 tma_load_3d(xdst, &maps.x, 0, ti.r0, ks * c.kc, bars->full + slot);
             } else {
@@ -693,7 +697,9 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
         const int tile = w / c.csplit, part = w % c.csplit;
         const int buf = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
-        const int n = ti.n0 + et;
+        // this thread's row of W and B: feature n0 + et, or for the gated view
+        // gate row n0/2 + et (et < 64) and up row I + n0/2 + et - 64
+        const int n = p.gated ? (et < 64 ? (ti.n0 >> 1) + et : p.I + (ti.n0 >> 1) + et - 64) : ti.n0 + et;
         const Tables &tab = p.tab[ti.e];
         const int nmma = (ti.cnt + 15) & ~15;
 
@@ -965,7 +971,40 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
             for (int j = 0; j < 16; ++j)
                 v[j] = (on16 >> j) & 1u ? __uint_as_float(rb[j]) + __uint_as_float(rdl[j])
                                         : __uint_as_float(rb[j]);
-            if (C == 1 && c.ystore) {
+            if (p.gated) {
+                // act = silu(g) * u of the bf16-rounded halves, rounded once: each
+                // thread's 16 values (gate or up of one feature) go through shared
+                // memory [16 rows][128] to the thread forming them; thread et then
+                // forms feature et % 64 for rows 8 (et / 64).. +7 into the staging
+                // box [row][64 act] bf16, and a full box goes out as one TMA store
+                const int sub = c0 % YSTORE_ROWS, bi = (c0 / YSTORE_ROWS) % c.ystore;
+                uint16_t *box = reinterpret_cast<uint16_t *>(XH) + (size_t)bi * YSTORE_ROWS * 64;
+                uint16_t *xs = reinterpret_cast<uint16_t *>(XH) + (size_t)c.ystore * YSTORE_ROWS * 64;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    xs[j * EPI_THREADS + et] = f32_to_bf16_bits(v[j]);
+                named_bar_sync(1, EPI_THREADS);
+                const int fe = et & 63, j0 = (et >> 6) * 8;
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = j0 + jj;
+                    const float g = bf_lo(xs[j * EPI_THREADS + fe]), u = bf_lo(xs[j * EPI_THREADS + 64 + fe]);
+                    box[(sub + j) * 64 + fe] = f32_to_bf16_bits(g / (1.0f + expf(-g)) * u);
+                }
+                if (sub + 16 == YSTORE_ROWS || c0 + 16 >= ti.cnt) {
+                    fence_proxy_async_smem(); // generic-proxy writes, read by the TMA
+                    named_bar_sync(1, EPI_THREADS);
+                    if (et == 0) {
+                        tma_store_2d(&maps.y, box, ti.n0 >> 1, ti.r0 + c0 - sub);
+                        bulk_commit();
+                        if (c.ystore == 1)
+                            bulk_wait_read<0>();
+                        else
+                            bulk_wait_read<1>(); // the other buffer is free again
+                    }
+                }
+                named_bar_sync(1, EPI_THREADS); // xs is written again by the next rows
+            } else if (C == 1 && c.ystore) {
                 // rows c0..c0+15 into the staging box (row-major [row][128
                 // features] bf16); a full box (or the tile's last rows) goes out
                 // as one TMA store, rows past the tensor clipped
@@ -1292,6 +1331,22 @@ TcPlan plan_tc(const Params &p, bool dyn)
         plan.hl = 1;
     }
     return plan;
+}
+
+// The gated view (act written from the drain) needs one K part, 64-wide K
+// chunks and the TMA-store drain: the plan of these rows must give them.
+bool tc_gated_ok(const Params &p)
+{
+    if (p.expert_offsets != nullptr || p.K % 64 != 0 || p.I % 64 != 0 || p.N != 2 * p.I)
+        return false;
+    Params q = p;
+    q.ystore_ok = 1;
+    const TcPlan plan = plan_tc(q, false);
+    const TcCfg c = make_cfg(q, plan, false);
+    const uint32_t xh_bytes = (uint32_t)c.hl * (uint32_t)c.xblk * (uint32_t)c.tn * 128u;
+    // act boxes [64 rows][64] bf16, then the [16][128] bf16 exchange rows
+    return plan.use3d && c.csplit == 1 && c.ystore > 0 && c.smem_bytes <= SMEM_LIMIT &&
+           xh_bytes >= (uint32_t)c.ystore * YSTORE_ROWS * 64u * 2u + 16u * EPI_THREADS * 2u;
 }
 
 cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, int num_sms,

@@ -86,6 +86,8 @@ def _no_delta_rows(wl):
     (37, 128, 100, 4, 8),   # tensor-core path, I not a multiple of 8 (scalar activation)
     (300, 256, 136, 5, 32), # several token tiles
     (48, 128, 64, 4, 16),   # K and I multiples of 64: the one-launch kernel's fused act
+    (300, 256, 128, 5, 32), # several token tiles, K and I multiples of 64: act from the tensor-core drain
+    (700, 192, 64, 6, 16),  # three token tiles, a partial last one
 ])
 @pytest.mark.parametrize("path", [rd.LORA_PATH_AUTO, rd.LORA_PATH_TC_ONE])
 def test_gate_up_matches_oracle(M, K, I, L, R, path):
@@ -109,13 +111,21 @@ def test_gate_up_decode_shapes_and_no_delta_rows(path):
     assert np.array_equal(act[rows], base[rows])
 
 
-def test_gate_up_prefill_shapes_sampled():
+def test_gate_up_prefill_shapes_every_token_tile():
+    """act from the tensor-core drain (W read as 64 gate + 64 up rows per
+    tile): one row of every 256-row token tile at a different offset in each,
+    and every row of one whole tile."""
     wl = workloads.make("prefill")  # W [14336][4096]: gate 7168 | up 7168, 8192 rows
     run = GateUpRun(wl)
     act = run.apply()
-    rows = np.arange(3, wl.M, 509).astype(np.int32)
+    assert run.last_status == 0
+    tiles = wl.M // 256
+    one = [t * 256 + (37 * t + 11) % 256 for t in range(tiles)]
+    whole = list(range(5 * 256, 6 * 256))
+    rows = np.array(sorted(set(one) | set(whole)), dtype=np.int32)
     ref = oracle.proj(wl.x, wl.W, wl.seq_slot, wl.adapters, rows=rows)
-    assert_close_act(act[rows], ref, run.I, "gate_up prefill (sampled rows)")
+    assert_close_act(act[rows], ref, run.I,
+                     f"gate_up prefill ({len(rows)} rows: one per token tile and all of tile 5)")
 
 
 @pytest.mark.parametrize("path", [rd.LORA_PATH_AUTO, rd.LORA_PATH_TC_ONE])

@@ -542,13 +542,17 @@ typedef struct lora_plan_info {
 } lora_plan_info;
 
 /*
- * Fill `info` for a lora_proj_apply of M rows on projection route `rt`
- * (gated = 1: lora_gate_up_apply with I = n_out / 2). The one-launch kernel
- * needs its whole grid resident at once (its CTAs exchange h through the
- * workspace); a shape whose clusters do not all fit takes LORA_PLAN_TC.
- * Errors: NULL info, a route that is not a projection route, M < 0.
+ * Fill `info` for a lora_proj_apply_ex of M rows on projection route `rt`
+ * and `path` (LORA_PATH_*; gated = 1: lora_gate_up_apply_ex with I = n_out /
+ * 2). The one-launch kernel (LORA_PATH_TC_ONE only) needs its whole grid
+ * resident at once (its CTAs exchange h through the workspace); a shape whose
+ * clusters do not all fit, or that needs more CTAs than the device has SMs,
+ * takes LORA_PLAN_TC. Calls whose shapes take different plans (a fused q/k/v
+ * call on one, its split calls on the other) are not byte-identical to each
+ * other. Errors: NULL info, a route that is not a projection route, M < 0, a
+ * path out of range.
  */
-lora_status lora_proj_plan(int M, const lora_route *rt, int gated, lora_plan_info *info);
+lora_status lora_proj_plan(int M, const lora_route *rt, int gated, int path, lora_plan_info *info);
 
 /*
  * Test hook for the bounded device waits of the one-launch kernel of up to

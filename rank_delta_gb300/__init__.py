@@ -141,7 +141,7 @@ _SIGNATURES = {
     "lora_embed_apply": (_i, [_vp, _vp, _i, _i, _i, _vp, _rtp, _vp, _i64, _vp, _sz, _vp]),
     "lora_status_get": (_i, [_vp, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "lora_test_wait_hook": (None, [ctypes.c_uint64, _i]),
-    "lora_proj_plan": (_i, [_i, _rtp, _i, ctypes.POINTER(lora_plan_info)]),
+    "lora_proj_plan": (_i, [_i, _rtp, _i, _i, ctypes.POINTER(lora_plan_info)]),
     "lora_proj_routing": (_i, [_vp, _i, _i, _i32p, _i32p, _vp]),
     "lora_last_error": (ctypes.c_char_p, []),
     "lora_build_seq_slot": (_i, [_i32p, _i, _i, _i, _i32p]),
@@ -372,11 +372,11 @@ def lora_status_get(ws, stream=None) -> int:
     return int(out.value)
 
 
-def lora_proj_plan(M: int, rt, gated: bool = False) -> dict:
-    """Which kernels a projection call of M rows on route `rt` takes on the
-    current device (path, launches, cluster shape and residency)."""
+def lora_proj_plan(M: int, rt, gated: bool = False, path: int = LORA_PATH_AUTO) -> dict:
+    """Which kernels a projection call of M rows on route `rt` and `path`
+    takes on the current device (plan, launches, cluster shape and residency)."""
     info = lora_plan_info()
-    _check(lib().lora_proj_plan(int(M), ctypes.byref(rt), int(bool(gated)), ctypes.byref(info)))
+    _check(lib().lora_proj_plan(int(M), ctypes.byref(rt), int(bool(gated)), int(path), ctypes.byref(info)))
     return {f: int(getattr(info, f)) for f, _ in lora_plan_info._fields_}
 
 

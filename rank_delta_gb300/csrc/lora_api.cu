@@ -234,6 +234,23 @@ bool make_map_pool_a(CUtensorMap *m, const void *pool, uint64_t K, uint64_t R, u
     return r == CUDA_SUCCESS;
 }
 
+// The same pool in boxes of `rows` rank rows (from row 0) x 64 k of one slot.
+bool make_map_pool_rows(CUtensorMap *m, const void *pool, uint64_t K, uint64_t R, uint64_t L, uint64_t slot_bytes,
+                        uint32_t rows)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {K, R, L};
+    cuuint64_t strides[2] = {K * 2, slot_bytes};
+    cuuint32_t box[3] = {64, rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // The same pool (R a multiple of 8, K of 64) as a 5D view [L slots][K/64
 // chunks][R/8 groups][8 rows][64 k]: one box of 2^lg groups x nch chunks of
 // one slot lands chunk by chunk, each chunk's groups 1 KB apart, as the
@@ -748,7 +765,13 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
             CUtensorMap xm;
             if (!make_map(&xm, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64, 128))
                 return fail(LORA_ERR_CUDA, "%s: encoding the x tensor map of the shrink failed", who);
-            e = launch_shrink_tc(p, xm, di.num_sms, st);
+            // the pool's A rows by TMA (one box of R rows per slot and chunk) when
+            // R is a multiple of 16 (the kernel's rows per slot)
+            CUtensorMap am;
+            const bool a_ok = p.pool != nullptr && p.R % 16 == 0 && p.R <= 256 &&
+                              make_map_pool_rows(&am, p.pool, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.L,
+                                                 (uint64_t)p.slot_bytes, (uint32_t)p.R);
+            e = launch_shrink_tc(p, xm, a_ok ? &am : nullptr, di.num_sms, st);
             if (e != cudaSuccess)
                 return cuda_fail(e, who);
         }
@@ -901,6 +924,8 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
     p.y_stride = y_stride;
     p.gated = gated_I > 0 ? 1 : 0;
     p.I = gated_I;
+    p.pool = rt->pool;
+    p.slot_bytes = slot_bytes(rt->max_rank, rt->n_in, rt->n_out);
     p.seq_slot = seq_slot;
     p.expert_offsets = nullptr;
     p.E = 1;
@@ -1360,7 +1385,7 @@ lora_status lora_moe_gather_apply(const void *x, int64_t x_stride, const void *c
     return ok();
 }
 
-lora_status lora_proj_plan(int M, const lora_route *rt, int gated, lora_plan_info *info)
+lora_status lora_proj_plan(int M, const lora_route *rt, int gated, int path, lora_plan_info *info)
 {
     const char *who = "lora_proj_plan";
     if (info == nullptr)
@@ -1373,19 +1398,38 @@ lora_status lora_proj_plan(int M, const lora_route *rt, int gated, lora_plan_inf
         return fail(LORA_ERR_SHAPE, "%s: M %d is negative", who, M);
     if (gated && rt->n_out % 2 != 0)
         return fail(LORA_ERR_SHAPE, "%s: a gated plan needs an even n_out (%d)", who, rt->n_out);
+    if (path < LORA_PATH_AUTO || path > LORA_PATH_TC_ONE)
+        return fail(LORA_ERR_RANGE, "%s: path %d is not one of LORA_PATH_*", who, path);
     if (M == 0)
         return ok();
     DevInfo di;
     if (!device_info(di))
         return fail(LORA_ERR_CUDA, "%s: no CUDA device", who);
     const int K = rt->n_in, N = rt->n_out, I = gated ? N / 2 : 0;
-    if (M <= SIMT_MAX_ROWS) {
+    if (path == LORA_PATH_SIMT || (path == LORA_PATH_AUTO && M <= SIMT_MAX_ROWS)) {
         info->path = LORA_PLAN_SIMT;
         info->kernels = gated ? 4 : 3;
         return ok();
     }
+    // the gated call of several token tiles writes act from the tensor-core drain
+    bool fused_act = false;
+    if (gated && M > DEC_MAX_ROWS) {
+        Params q;
+        memset(&q, 0, sizeof q);
+        q.rows = M;
+        q.K = K;
+        q.N = N;
+        q.I = I;
+        q.gated = 1;
+        q.E = 1;
+        q.L = rt->max_loras;
+        q.R = rt->max_rank;
+        q.tn = tc_token_tile(M);
+        fused_act = tc_gated_ok(q);
+    }
     uint32_t smem = 0;
-    const bool one = M <= DEC_MAX_ROWS && (!gated || (K % 64 == 0 && I % 64 == 0)) &&
+    const bool one = path == LORA_PATH_TC_ONE && M <= DEC_MAX_ROWS && (!gated || M > SIMT_MAX_ROWS) &&
+                     (!gated || (K % 64 == 0 && I % 64 == 0)) &&
                      dec_plan_info(M, K, N, rt->max_loras, rt->max_rank, gated, I, di.num_sms,
                                    &info->clusters_needed, &info->clusters_resident, &info->cluster_size,
                                    &smem) == 1;
@@ -1395,7 +1439,7 @@ lora_status lora_proj_plan(int M, const lora_route *rt, int gated, lora_plan_inf
         info->kernels = 1;
     } else {
         info->path = LORA_PLAN_TC;
-        info->kernels = (M >= TC_SHRINK_MIN_ROWS ? 3 : 2) + (gated ? 1 : 0);
+        info->kernels = (M >= TC_SHRINK_MIN_ROWS ? 3 : 2) + (gated && !fused_act ? 1 : 0);
     }
     return ok();
 }

@@ -80,6 +80,8 @@ struct Params {
     int no_units; // 1: h comes from the tensor-core shrink kernel (no shrink work units)
     int max_tiles; // token tiles the routing kernel may list (0: the workspace bound)
     int ystore_ok; // 1: maps.y is encoded (y 16-byte aligned, y_stride a multiple of 8)
+    const void *pool;  // the route's pool (A of slot s at pool + s * slot_bytes when packed there)
+    size_t slot_bytes;
     int gated, I;  // 1: W is the fused [gate I | up I] (N = 2I) read as tiles of 64 gate + 64 up rows,
                    // and y receives act = silu(g) * u, [rows][I] (one K part, TMA stores only)
     const uint16_t *W[MAX_E];
@@ -174,7 +176,10 @@ cudaError_t launch_prep(const Params &p, cudaStream_t st);
 cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st);
 cudaError_t launch_simt(const Params &p, int num_sms, cudaStream_t st);
 // Tensor-core shrink (lora_shrink_tc.cu); xmap: x with 64 x 128 boxes.
-cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, int num_sms, cudaStream_t st);
+// amap: the pool's A rows in boxes of round16(R) rows x 64 k (one copy per
+// slot and K chunk), or nullptr (every A row by cp.async through a_table).
+cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, const CUtensorMap *amap, int num_sms,
+                             cudaStream_t st);
 // Rows from which a projection call computes h with the tensor-core shrink
 // kernel (one CTA per 128 rows: enough tiles to spread over the SMs).
 constexpr int TC_SHRINK_MIN_ROWS = 2048;

@@ -7,7 +7,9 @@
 // Rs = max_rank rounded up to 16 columns each, up to 256 columns per group:
 //   D[t, i*Rs + r] = sum_k x[t, k] A_{slot_i}[r, k]
 // so a tile whose rows share one adapter (a prefill sequence) costs one
-// 128 x Rs x K product. x tiles arrive by TMA; the A rows are copied with
+// 128 x Rs x K product. x tiles arrive by TMA, and so do the A rows when
+// every slot of a group lies in the route's pool (one box of Rs rows per slot
+// and K chunk, pad rows zero by the pack); otherwise they are copied with
 // cp.async through the slot pointer table (a_table), into the same 128-byte
 // swizzled K-major layout. The epilogue keeps, for row t, the Rs columns of
 // its own slot and writes them to h[t][0..R) in fp32 -- with K unsplit, so h
@@ -21,6 +23,8 @@
 // programmatic dependent launch: it lets the projection kernel start at once,
 // and before it exits it waits for the routing kernel, so a kernel that waits
 // for this one also sees the routing results.
+#include <cstring>
+
 #include "lora_internal.cuh"
 #include "ptx.cuh"
 #include "vec.cuh"
@@ -63,7 +67,8 @@ __device__ __forceinline__ void stc_abort(const Params &p, StcShared *sh)
 __device__ __forceinline__ bool stc_aborted(StcShared *sh) { return *(volatile int *)&sh->abort_flag != 0; }
 
 __global__ void __launch_bounds__(STC_THREADS, 1)
-    shrink_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ Params p, int Rs)
+    shrink_tc_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap amap,
+                     const __grid_constant__ Params p, int Rs, int a_map)
 {
     extern __shared__ uint8_t stc_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(stc_raw) + 1023) & ~uintptr_t(1023));
@@ -83,6 +88,8 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
         sh->abort_flag = 0;
         fence_barrier_init();
         prefetch_tmap(&xmap);
+        if (a_map)
+            prefetch_tmap(&amap);
     }
     if (warp == 1)
         tmem_alloc(&sh->tmem_base, STC_MAX_N);
@@ -153,6 +160,13 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
         for (int grp = 0; grp < ngroups; ++grp, ++groups_done) {
             const int gs = min(G, nslots - grp * G);
             const int N = gs * Rs;
+            // A rows by TMA when every slot of the group lies in the pool
+            bool a_tma = a_map != 0;
+            for (int i = 0; i < gs && a_tma; ++i) {
+                const int li = grp * G + i;
+                a_tma = reinterpret_cast<const uint8_t *>(sh->slot_a[li]) ==
+                        static_cast<const uint8_t *>(p.pool) + (size_t)sh->slot_list[li] * p.slot_bytes;
+            }
             if (warp == 0) {
                 if (lane == 0) { // x copies
                     for (int kc = 0; kc < kchunks; ++kc, ++gx) {
@@ -161,8 +175,20 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
                             stc_abort(p, sh);
                             break;
                         }
-                        mbar_arrive_expect_tx(sh->full + st, STC_X_BYTES);
-                        tma_load_2d(smem + (size_t)st * STC_STAGE_BYTES, &xmap, kc * 64, r0, sh->full + st);
+                        uint8_t *xs = smem + (size_t)st * STC_STAGE_BYTES;
+                        if (a_tma) {
+                            // x and every slot's Rs A rows of the chunk on one arrival, and
+                            // the loaders' arrivals given at once (they copy nothing)
+                            mbar_arrive_expect_tx(sh->full + st, STC_X_BYTES + (uint32_t)N * 128u);
+                            tma_load_2d(xs, &xmap, kc * 64, r0, sh->full + st);
+                            for (int i = 0; i < gs; ++i)
+                                tma_load_3d(xs + STC_X_BYTES + (size_t)i * Rs * 128, &amap, kc * 64, 0,
+                                            sh->slot_list[grp * G + i], sh->full + st);
+                            mbar_arrive_count(sh->full + st, STC_LOADERS);
+                        } else {
+                            mbar_arrive_expect_tx(sh->full + st, STC_X_BYTES);
+                            tma_load_2d(xs, &xmap, kc * 64, r0, sh->full + st);
+                        }
                     }
                 }
             } else if (warp == 1) {
@@ -201,7 +227,8 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
                 const int et = tid - 64;
                 constexpr int LAG = STC_STAGES - 1;
                 const int ga0 = ga;
-                int kc = 0;
+                int kc = a_tma ? kchunks : 0; // by TMA: nothing to copy here
+                ga += kc;
                 for (; kc < kchunks; ++kc, ++ga) {
                     const int st = ga % STC_STAGES;
                     if (stc_aborted(sh) || !mbar_wait(sh->empty + st, ((uint32_t)(ga / STC_STAGES) & 1u) ^ 1u)) {
@@ -228,8 +255,9 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
                 // the last (up to LAG) stages issued
                 cp_async_wait_all();
                 fence_proxy_async_smem();
-                for (int q = max(0, kc - LAG); q < kc; ++q)
-                    mbar_arrive(sh->full + (ga0 + q) % STC_STAGES);
+                if (!a_tma)
+                    for (int q = max(0, kc - LAG); q < kc; ++q)
+                        mbar_arrive(sh->full + (ga0 + q) % STC_STAGES);
                 // epilogue: row t keeps the columns of its own slot
                 const bool got = mbar_wait(&sh->acc_full, (uint32_t)groups_done & 1u);
                 tc_fence_after();
@@ -290,7 +318,8 @@ __global__ void __launch_bounds__(STC_THREADS, 1)
     grid_dependency_wait();
 }
 
-cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, int num_sms, cudaStream_t st)
+cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, const CUtensorMap *amap, int num_sms,
+                             cudaStream_t st)
 {
     static std::atomic<uint64_t> raised{0};
     cudaError_t ea = raise_smem_limit(raised, shrink_tc_kernel, (int)STC_SMEM);
@@ -311,7 +340,11 @@ cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, int num_s
     cfg.stream = st;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, shrink_tc_kernel, xmap, p, Rs);
+    CUtensorMap am;
+    memset(&am, 0, sizeof am);
+    if (amap != nullptr)
+        am = *amap;
+    return cudaLaunchKernelEx(&cfg, shrink_tc_kernel, xmap, am, p, Rs, amap != nullptr ? 1 : 0);
 }
 
 } // namespace rd

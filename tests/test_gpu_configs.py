@@ -78,6 +78,39 @@ def test_qkv_no_delta_rows_are_base_bytes(qkv, path):
     assert np.array_equal(y[none], base[none])
 
 
+@pytest.mark.parametrize("path", PATHS)
+def test_gated_q_fused_equals_split_and_matches_oracle(path):
+    """A gated query projection, output [q | gate] twice the query width,
+    one A per adapter and B rows split q / gate (spark_model lora_delta.rs,
+    the attention weight holder's gated q width): the fused call matches the
+    oracle on every row and its bytes equal the two split calls'."""
+    wl = workloads.make("gated_q")
+    run = ProjRun(wl)
+    fused = run.apply(path=path)
+    assert run.last_status == 0
+    assert_all_rows(fused, oracle.workload_proj(wl), "gated q [q | gate]")
+    parts, runs, row0 = [], [], 0
+    for n in wl.splits:
+        sub = workloads.ProjWorkload(
+            f"gq{row0}", wl.seed, wl.M, wl.K, n, wl.max_loras, wl.max_rank,
+            np.ascontiguousarray(wl.W[row0:row0 + n]), wl.x, wl.seq_slot,
+            [workloads.Adapter(a.A, np.ascontiguousarray(a.B[row0:row0 + n]), a.rank, a.alpha,
+                               a.use_rslora, a.adapter_scale) for a in wl.adapters])
+        sr = ProjRun(sub)
+        parts.append(sr.apply(path=path))
+        runs.append(sr)
+        row0 += n
+    # bytes agree when the fused and the split calls take the same kernel
+    plans = {rd.lora_proj_plan(wl.M, r.route.rt, path=path)["path"] for r in [run] + runs}
+    if path == rd.LORA_PATH_AUTO:
+        assert plans == {rd.LORA_PLAN_TC}
+    if len(plans) == 1:
+        assert np.array_equal(fused, np.concatenate(parts, axis=1))
+    else:  # the one-launch path: 8192 outputs need more CTAs than SMs, 4096 fit
+        assert plans == {rd.LORA_PLAN_TC, rd.LORA_PLAN_ONE_LAUNCH}, plans
+        assert_all_rows(np.concatenate(parts, axis=1), oracle.workload_proj(wl), "gated q split calls")
+
+
 def test_one_launch_path_with_the_default_workspace_is_the_tensor_core_path(qkv):
     """LORA_PATH_TC_ONE given only the default path's workspace runs the
     tensor-core path instead: the same bytes as LORA_PATH_TC."""

@@ -267,6 +267,25 @@ def qkv(seed: int = 2, M: int = 256) -> ProjWorkload:
                              "alpha=32 adapter_scale~U{0,0.5,1} Zipf(1.1) 5% rows -1")
 
 
+def gated_q(seed: int = 6, M: int = 64) -> ProjWorkload:
+    """Gated attention query: one fused base [q 4096 | gate 4096][4096] whose
+    output is twice the query width (q rows, then the gate rows), 16 adapters
+    of rank 16 with one A each and B over all 8192 rows. Draw order: W, x,
+    per adapter (A, B), Zipf slots, the 10% no-adapter rows.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    K, N, L, R = 4096, 8192, 16, 16
+    W = _normal_bf16(rng, (N, K), 1.0 / K)
+    x = _normal_bf16(rng, (M, K), 1.0)
+    ads = [_adapter(rng, K, N, 16, 1.0 / 64, 0.02, alpha=32.0) for _ in range(L)]
+    seq_slot = zipf_slots(rng, M, L, 1.1)
+    seq_slot = _mark_no_adapter(rng, seq_slot, 0.10)
+    return ProjWorkload("gated_q", seed, M, K, N, L, R, W, x, seq_slot, ads,
+                        splits=[4096, 4096],
+                        note="W~N(0,1/4096) x~N(0,1) r=16 A~U(+-1/64) B~N(0,0.02) alpha=32 "
+                             "Zipf(1.1) 10% rows -1; output [q | gate]")
+
+
 def prefill(seed: int = 3, seq_len: int = 1024, n_seq: int = 8) -> ProjWorkload:
     """Gate/up base [14336][4096], 8 contiguous sequences of 1024 rows.
 
@@ -465,6 +484,7 @@ CONFIGS = {
     "tiny": tiny,
     "decode": decode,
     "qkv": qkv,
+    "gated_q": gated_q,
     "prefill": prefill,
     "moe": moe,
 }

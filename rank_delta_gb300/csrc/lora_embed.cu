@@ -851,16 +851,20 @@ cudaError_t launch_embed(const EmbedParams &p, int num_sms, cudaStream_t st)
     const long long chunks = p.M / CH + (p.M < nb ? p.M : nb);
     const long long items = chunks * p.nft;
     const int grid = (int)(items < num_sms ? (items > 0 ? items : 1) : num_sms);
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
+    // CTAs wait on counters other CTAs write: cooperative, so the whole grid
+    // is resident at once or the launch fails
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(EMB_THREADS);
     cfg.dynamicSmemBytes = c.smem_bytes;
     cfg.stream = st;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, embed_kernel, p, c);
 }
 

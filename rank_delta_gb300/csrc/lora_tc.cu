@@ -50,8 +50,10 @@
 //                an [m, n_out] scratch).
 // The shrink is handed over inside the launch: a unit bumps its bucket's
 // counter after writing h; the epilogue waits (bounded) for the counters of
-// the slots it stages. The grid never exceeds the SM count (one CTA per SM),
-// so every unit and every K part runs while others wait.
+// the slots it stages. The grid never exceeds the SM count (one CTA per SM)
+// and launches with such waits are cooperative, so every unit and every K
+// part runs while others wait (a grid that cannot be resident at once fails
+// to launch).
 //
 // The kernel starts before the routing/prep kernel has finished (programmatic
 // dependent launch); only the roles that read its results wait for it.
@@ -1360,23 +1362,32 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
         return ea;
     if (c.smem_bytes > SMEM_LIMIT)
         return cudaErrorInvalidConfiguration;
-    // One CTA per SM at most, so every CTA is resident (the in-launch waits
-    // rely on it); never more CTAs than work items.
+    // One CTA per SM at most (the in-launch waits need every CTA resident; the
+    // cooperative launch below makes sure they are); never more CTAs than work
+    // items.
     int grid = num_sms;
     if (c.static_tiles >= 0 && c.static_tiles * c.csplit < grid)
         grid = c.static_tiles * c.csplit;
     grid = grid / c.csplit * c.csplit;
 
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
+    // Where CTAs wait on counters other CTAs write (split-K parts, in-launch
+    // shrink units) the launch is cooperative, so the whole grid is resident
+    // at once or the launch fails -- never a wait on a CTA that has not
+    // started. Launches without such waits (one K part, h from the shrink
+    // kernel) stay plain, so they start beside the kernel before them.
+    const bool waits = c.csplit > 1 || !p.no_units;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = waits ? 1 : 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(TC_THREADS);
     cfg.dynamicSmemBytes = c.smem_bytes;
     cfg.stream = st;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, tc_kernel, maps, p, c);
 }
 

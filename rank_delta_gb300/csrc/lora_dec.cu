@@ -1627,6 +1627,12 @@ void dec_test_hook(uint64_t wait_ns, int extra_arrivals)
     g_test_extra.store(extra_arrivals);
 }
 
+void test_hook_get(uint64_t &wait_ns, int &extra)
+{
+    wait_ns = g_test_wait_ns.load();
+    extra = wait_ns ? g_test_extra.load() : 0;
+}
+
 // Plan and launch; returns cudaErrorNotSupported when the shape does not fit
 // this kernel (the caller then takes the general tensor-core path).
 cudaError_t launch_dec(const DecLaunch &d, int num_sms, cudaStream_t st)

@@ -306,6 +306,9 @@ int dec_plan_info(int M, int K, int N, int L, int R, int gated, int I, int num_s
 int dec_flag_count(int M, int K, int N, int gated);
 // cudaErrorNotSupported: the shape or the device does not take this kernel.
 cudaError_t launch_dec(const DecLaunch &d, int num_sms, cudaStream_t st);
+// The test hook's setting (lora_test_wait_hook): a wait limit in ns (0 = the
+// normal one) and arrivals that never come added to the waits it covers.
+void test_hook_get(uint64_t &wait_ns, int &extra);
 // 1 when the tensor-core kernel can take this gated call (W the fused
 // [gate | up], act written from its drain): see launch_tc.
 bool tc_gated_ok(const Params &p);

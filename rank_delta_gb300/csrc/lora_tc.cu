@@ -94,6 +94,8 @@ struct TcCfg {
     int borrow;       // 1: no room for D' beside two accumulators; D' borrows the other one
     int local_route;  // 1: one token tile holds every row; each CTA sorts them itself for the shrink
     int ystore;       // y boxes staged in the XH buffers: 0 = per-thread stores, else 1 or 2 buffers
+    uint64_t wait_ns; // limit of the split-K wait (the test hook shortens it)
+    int extra_parts;  // test hook: parts the split-K wait also waits for, that never come
     uint32_t x_chunk, stage_bytes;
     uint32_t xb_off, xh_off, aux_off, meta_off, red_off, umeta_off, bar_off, smem_bytes;
     uint32_t tmem_cols;
@@ -354,7 +356,7 @@ __device__ __forceinline__ void issue_mma(const Params &p, const TcCfg &c, Bars 
     }
 }
 
-__device__ __forceinline__ bool wait_count(const int32_t *cnt, int target)
+__device__ __forceinline__ bool wait_count(const int32_t *cnt, int target, uint64_t wait_ns)
 {
     if (ld_acquire_gpu(cnt) >= target)
         return true;
@@ -362,7 +364,7 @@ __device__ __forceinline__ bool wait_count(const int32_t *cnt, int target)
     for (;;) {
         if (ld_acquire_gpu(cnt) >= target)
             return true;
-        if (globaltimer_ns() - t0 > WAIT_NS)
+        if (globaltimer_ns() - t0 > wait_ns)
             return false;
     }
 }
@@ -1067,7 +1069,7 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
         }
         if (C > 1) {
             // every part of the tile written: sum this part's share of the columns
-            if (et == 0 && !wait_count(p.ws.tile_cnt + tile, C))
+            if (et == 0 && !wait_count(p.ws.tile_cnt + tile, C + c.extra_parts, c.wait_ns))
                 flag_abort(p, bars);
             named_bar_sync(1, EPI_THREADS);
             if (aborted(bars))
@@ -1355,7 +1357,10 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
                       cudaStream_t st)
 {
     const bool dyn = p.expert_offsets != nullptr;
-    const TcCfg c = make_cfg(p, plan, dyn);
+    TcCfg c = make_cfg(p, plan, dyn);
+    uint64_t tw = 0;
+    test_hook_get(tw, c.extra_parts);
+    c.wait_ns = tw ? tw : WAIT_NS;
     static std::atomic<uint64_t> raised{0};
     cudaError_t ea = raise_smem_limit(raised, tc_kernel, (int)SMEM_LIMIT);
     if (ea != cudaSuccess)

@@ -47,3 +47,24 @@ def test_exchange_wait_runs_out_then_the_next_call_is_correct(name):
     y2 = run.apply(path=one)
     assert run.last_status == 0, f"{name}: the next call reports {run.last_status:#x}"
     assert_close(y2, oracle.workload_proj(run.wl), f"{name} after a timed-out call")
+
+
+def test_split_k_wait_runs_out_then_the_next_call_is_correct():
+    """The tensor-core path's split-K sum waits (bounded) for every K part of
+    its tile; with the hook the wait also counts a part that never comes, so
+    it runs out: the call returns with LORA_FLAG_WAIT_TIMEOUT, and the next
+    normal call on the same workspace is correct and clean."""
+    run = ProjRun(workloads.make("decode"))  # 64 rows: four K parts per tile
+    tc = rd.LORA_PATH_TC
+    run.apply(path=tc)
+    assert run.last_status == 0
+    rd.lora_test_wait_hook(200_000, 1)
+    try:
+        run.apply(path=tc)
+        flags = run.last_status
+    finally:
+        rd.lora_test_wait_hook(0, 0)
+    assert flags & rd.LORA_FLAG_WAIT_TIMEOUT, f"status {flags:#x}"
+    y = run.apply(path=tc)
+    assert run.last_status == 0, f"the next call reports {run.last_status:#x}"
+    assert_close(y, oracle.workload_proj(run.wl), "decode after a timed-out split-K wait")

@@ -7,7 +7,7 @@
 //
 // Work: items = (token tile, 128-feature tile, K part), spread over a grid
 // that never exceeds the SMs (every CTA resident); several token tiles are
-// walked in groups of 8 per feature tile so a wave shares W tiles in L2.
+// walked in groups of 16 per feature tile so a wave shares W tiles in L2.
 // With csplit K parts, each part writes its fp32 partial tile to the
 // workspace (coalesced, L2-resident) and bumps the tile's counter; once all
 // parts are in, each part's CTA sums a contiguous share of the columns in
@@ -79,7 +79,7 @@ constexpr int MAX_STAGES = 8;
 constexpr uint32_t W_CHUNK_BYTES = TC_BM * 64 * 2;
 constexpr uint32_t XB_BLOCK = TC_BM * 128; // 64 k of 128 B rows, 128 rows
 constexpr int LR_MAX_L = 64;               // slots a launch may have for local routing
-constexpr int TC_TGROUP = 8;               // token tiles per group of the grouped tile order
+constexpr int TC_TGROUP = 16;              // token tiles per group of the grouped tile order
 
 struct TcCfg {
     int tn, kc, stages, csplit;

@@ -788,9 +788,10 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
         }
         // y by TMA stores where its layout allows (16-byte aligned rows);
         // otherwise the epilogue stores y element by element
-        if (p.gated) // act [rows][I], boxes of 64 act features x 64 rows
-            p.ystore_ok = make_map_plain(&maps.y, p.y, (uint64_t)p.I, (uint64_t)p.rows, (uint64_t)p.y_stride, 64,
-                                         (uint32_t)YSTORE_ROWS)
+        if (p.gated) // act [rows][I], boxes of 64 act features x 64 rows (the one-part drain)
+            p.ystore_ok = (aligned16(p.y) && p.y_stride % 8 == 0 &&
+                           make_map_plain(&maps.y, p.y, (uint64_t)p.I, (uint64_t)p.rows, (uint64_t)p.y_stride, 64,
+                                          (uint32_t)YSTORE_ROWS))
                               ? 1
                               : 0;
         else
@@ -799,7 +800,8 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
                                           128, (uint32_t)YSTORE_ROWS))
                               ? 1
                               : 0;
-        if (p.gated && !p.ystore_ok)
+        // with one K part the gated drain writes act only through these boxes
+        if (p.gated && !p.ystore_ok && plan.csplit == 1)
             return fail(LORA_ERR_CUDA, "%s: encoding the act tensor map failed", who);
         e = launch_tc(p, maps, plan, di.num_sms, st);
     }
@@ -1089,9 +1091,9 @@ lora_status lora_gate_up_apply_ex(const void *x, int64_t x_stride, const void *W
         if (taken || s != LORA_OK)
             return s;
     }
-    // several token tiles (one K part): the tensor-core kernel reads W as 64
-    // gate + 64 up rows per tile and writes act from its drain
-    if (path != LORA_PATH_SIMT && M > DEC_MAX_ROWS && aligned16(act) && act_stride % 8 == 0) {
+    // the tensor-core kernel reads W as 64 gate + 64 up rows per tile and
+    // writes act from its drain (one K part) or from its split-K sum
+    if (path != LORA_PATH_SIMT && !(path == LORA_PATH_AUTO && M <= SIMT_MAX_ROWS)) {
         Params q;
         memset(&q, 0, sizeof q);
         q.rows = M;
@@ -1103,6 +1105,7 @@ lora_status lora_gate_up_apply_ex(const void *x, int64_t x_stride, const void *W
         q.L = rt->max_loras;
         q.R = rt->max_rank;
         q.tn = tc_token_tile(M);
+        q.ystore_ok = aligned16(act) && act_stride % 8 == 0 ? 1 : 0;
         if (tc_gated_ok(q))
             return proj_apply(x, x_stride, W, M, K, 2 * I, seq_slot, rt, act, act_stride, ws, proj_ws,
                               LORA_PATH_TC, stream, I);
@@ -1411,9 +1414,10 @@ lora_status lora_proj_plan(int M, const lora_route *rt, int gated, int path, lor
         info->kernels = gated ? 4 : 3;
         return ok();
     }
-    // the gated call of several token tiles writes act from the tensor-core drain
+    // the gated call writes act from the tensor-core drain or split-K sum
+    // (act rows taken as 16-byte aligned)
     bool fused_act = false;
-    if (gated && M > DEC_MAX_ROWS) {
+    if (gated) {
         Params q;
         memset(&q, 0, sizeof q);
         q.rows = M;
@@ -1425,6 +1429,7 @@ lora_status lora_proj_plan(int M, const lora_route *rt, int gated, int path, lor
         q.L = rt->max_loras;
         q.R = rt->max_rank;
         q.tn = tc_token_tile(M);
+        q.ystore_ok = 1;
         fused_act = tc_gated_ok(q);
     }
     uint32_t smem = 0;

@@ -975,7 +975,7 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
             for (int j = 0; j < 16; ++j)
                 v[j] = (on16 >> j) & 1u ? __uint_as_float(rb[j]) + __uint_as_float(rdl[j])
                                         : __uint_as_float(rb[j]);
-            if (p.gated) {
+            if (p.gated && C == 1) {
                 // act = silu(g) * u of the bf16-rounded halves, rounded once: each
                 // thread's 16 values (gate or up of one feature) go through shared
                 // memory [16 rows][128] to the thread forming them; thread et then
@@ -1077,6 +1077,41 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
             const float *parts = p.ws.part + (size_t)tile * C * c.tn * EPI_THREADS;
             const size_t pstride = (size_t)c.tn * EPI_THREADS;
             const int cb = part * ti.cnt / C, ce = (part + 1) * ti.cnt / C;
+            if (p.gated) {
+                // act of 4 consecutive features (fq) x every 8th column of the
+                // share: gate rows 4 fq.. and up rows 64 + 4 fq.. of the tile,
+                // each summed in part order and rounded to bf16, then silu(g) * u
+                // rounded once
+                const int fq = et & 15, cg8 = et >> 4;
+                const int fa = (ti.n0 >> 1) + 4 * fq;
+                for (int cc = cb + cg8; cc < ce; cc += 8) {
+                    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q < C) {
+                            const float *pc = parts + q * pstride + (size_t)cc * EPI_THREADS;
+                            const float4 gq = __ldcg(reinterpret_cast<const float4 *>(pc) + fq);
+                            const float4 uq = __ldcg(reinterpret_cast<const float4 *>(pc + 64) + fq);
+                            if (q == 0) {
+                                g = gq;
+                                u = uq;
+                            } else {
+                                g.x += gq.x; g.y += gq.y; g.z += gq.z; g.w += gq.w;
+                                u.x += uq.x; u.y += uq.y; u.z += uq.z; u.w += uq.w;
+                            }
+                        }
+                    const float gv[4] = {g.x, g.y, g.z, g.w}, uv[4] = {u.x, u.y, u.z, u.w};
+                    uint16_t *ar = p.y + (int64_t)(ti.r0 + cc) * p.y_stride;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float gb = bf_lo(f32_to_bf16_bits(gv[i])), ub = bf_lo(f32_to_bf16_bits(uv[i]));
+                        if (fa + i < p.I)
+                            ar[fa + i] = f32_to_bf16_bits(gb / (1.0f + expf(-gb)) * ub);
+                    }
+                }
+                named_bar_sync(1, EPI_THREADS); // per-item state is rewritten by the next item
+                continue;
+            }
             // thread = 4 consecutive features (quad) x every 4th column of the
             // share: 16-byte loads, each warp reading whole 512-byte column rows
             const int quad = et & 31, cg = et >> 5;
@@ -1337,19 +1372,23 @@ TcPlan plan_tc(const Params &p, bool dyn)
     return plan;
 }
 
-// The gated view (act written from the drain) needs one K part, 64-wide K
-// chunks and the TMA-store drain: the plan of these rows must give them.
+// The gated view needs 64-wide K chunks and, with one K part, the TMA-store
+// drain (p.ystore_ok: act 16-byte aligned rows): the plan of these rows must
+// give them. With several K parts the split-K sum forms act.
 bool tc_gated_ok(const Params &p)
 {
     if (p.expert_offsets != nullptr || p.K % 64 != 0 || p.I % 64 != 0 || p.N != 2 * p.I)
         return false;
-    Params q = p;
-    q.ystore_ok = 1;
+    const Params &q = p;
     const TcPlan plan = plan_tc(q, false);
     const TcCfg c = make_cfg(q, plan, false);
     const uint32_t xh_bytes = (uint32_t)c.hl * (uint32_t)c.xblk * (uint32_t)c.tn * 128u;
     // act boxes [64 rows][64] bf16, then the [16][128] bf16 exchange rows
-    return plan.use3d && c.csplit == 1 && c.ystore > 0 && c.smem_bytes <= SMEM_LIMIT &&
+    // one K part: the drain writes act through TMA boxes; several: the split-K
+    // sum forms it
+    if (c.csplit > 1)
+        return plan.use3d && c.smem_bytes <= SMEM_LIMIT;
+    return plan.use3d && c.ystore > 0 && c.smem_bytes <= SMEM_LIMIT &&
            xh_bytes >= (uint32_t)c.ystore * YSTORE_ROWS * 64u * 2u + 16u * EPI_THREADS * 2u;
 }
 

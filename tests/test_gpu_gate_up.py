@@ -111,6 +111,23 @@ def test_gate_up_decode_shapes_and_no_delta_rows(path):
     assert np.array_equal(act[rows], base[rows])
 
 
+def test_gate_up_decode_shapes_strided_act_from_the_split_k_sum():
+    """64 rows on K 4096: four K parts whose sum forms act, written into rows
+    of a wider act buffer; the columns past I keep their sentinel."""
+    wl = workloads.make("decode")
+    run = GateUpRun(wl)
+    st = run.I + 24
+    wide = torch.full((wl.M, st), SENTINEL, dtype=torch.int16, device="cuda")
+    rd.lora_gate_up_apply(run.x, run.x.stride(0), run.W, wl.M, wl.K, run.I, run.slots, run.route.rt, wide, st,
+                          run.ws, run.ws.numel())
+    torch.cuda.synchronize()
+    assert rd.lora_status_get(run.ws) == 0
+    bits = wide.cpu().numpy().view(np.uint16)
+    assert (bits[:, run.I:] == np.uint16(SENTINEL & 0xFFFF)).all()
+    assert_close_act(bits[:, :run.I], oracle.proj(wl.x, wl.W, wl.seq_slot, wl.adapters), run.I,
+                     "gate_up decode, act stride I + 24")
+
+
 def test_gate_up_prefill_shapes_every_token_tile():
     """act from the tensor-core drain (W read as 64 gate + 64 up rows per
     tile): one row of every 256-row token tile at a different offset in each,

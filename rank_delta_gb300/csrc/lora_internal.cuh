@@ -188,6 +188,7 @@ constexpr int TC_SHRINK_MIN_ROWS = 2048;
 // is used, and the expand's staging buffers.
 struct TcPlan {
     int tn, kc, stages, csplit, use3d;
+    int pair; // 1: two adjacent feature tiles per x box (per-expert tiles)
     int xblk; // 64-wide k blocks of one tensor-core expand round
     int hl;   // planes of the staged s * h: 1 (bf16) or 2 (bf16 hi + lo)
 };

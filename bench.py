@@ -267,7 +267,7 @@ class ClockSampler:
 # while these are unchanged)
 KERNEL_SOURCES = {
     "dec_kernel": ["lora_dec.cu", "ptx.cuh", "vec.cuh", "lora_internal.cuh"],
-    "tc_kernel": ["lora_tc.cu", "shrink.cuh", "ptx.cuh", "vec.cuh", "lora_internal.cuh"],
+    "tc_kernel": ["lora_tc.cu", "shrink.cuh", "shrink_tc.cuh", "ptx.cuh", "vec.cuh", "lora_internal.cuh"],
     "simt_kernel": ["lora_simt.cu", "shrink.cuh", "vec.cuh", "lora_internal.cuh"],
     "embed_kernel": ["lora_embed.cu", "ptx.cuh", "lora_internal.cuh"],
 }
@@ -455,29 +455,29 @@ def job_rate(rows: int, steps: int, world: int, elapsed_ms: float) -> float:
     return rows * steps * world / (elapsed_ms / 1e3)
 
 
-# kernels one call launches: up to 256 rows, one kernel (routing, shrink,
-# base, expand-fold and the split-K sum); beyond, the routing sort, then one
-# fused tensor-core launch, with a tensor-core shrink launch between the two
-# from 2048 projection rows; the CUDA-core path (<= 16 rows) runs the sort, a
-# shrink launch and the GEMV; the embedding gather runs the sort and one launch
+# kernels one call launches: the one-launch kernel (opt-in path) one; the
+# tensor-core path the routing sort, then one fused launch (shrink tiles or
+# units, base, expand-fold, split-K sum); the CUDA-core path (<= 16 rows) the
+# sort, a shrink launch and the GEMV; the embedding gather the sort and one
+# launch. Projection and gated calls ask the library's plan (lora_proj_plan),
+# which also says whether a gated call needs the separate activation kernel.
 LAUNCHES_DEC, LAUNCHES_TC, LAUNCHES_SIMT, LAUNCHES_EMBED = 1, 2, 3, 2
-TC_SHRINK_MIN_ROWS = 2048
 DEC_MAX_ROWS = 256
 
 
-def launches_per_call(config, rows, kernel):
+def launches_per_call(config, rows, kernel, rd=None, rt=None):
     if kernel == "embed_kernel":
         return LAUNCHES_EMBED
     if config == "moe_gather":  # expert sort + row copy, the grouped fold, the combine
         return LAUNCHES_TC + 2
     if kernel == "dec_kernel":
         return LAUNCHES_DEC
-    if config in GATE_UP: # the projection, then the activation kernel
+    if rd is not None and rt is not None and config not in ("moe",):
+        return rd.lora_proj_plan(rows, rt, config in GATE_UP, PROJ_PATH[0])["kernels"]
+    if config in GATE_UP: # the projection, then (at most) the activation kernel
         return launches_per_call(GATE_UP[config], rows, kernel) + 1
     if kernel == "simt_kernel":
         return LAUNCHES_SIMT
-    if config != "moe" and rows >= TC_SHRINK_MIN_ROWS:
-        return LAUNCHES_TC + 1
     return LAUNCHES_TC
 
 
@@ -769,7 +769,8 @@ def measure(b, want_cpu=True):
                           delta_share=1.0 - base["median_us"] / full["median_us"]),
         "roofline": b.roofline(med),
         "e2e": b.e2e(args.steps),
-        "gpu_launches_per_call": launches_per_call(config, b.rows, kernel_of(config, b.rows)),
+        "gpu_launches_per_call": launches_per_call(config, b.rows, kernel_of(config, b.rows), b.rd,
+                                                   getattr(getattr(b.sets[0], "route", None), "rt", None)),
         "status_flags": b.rd.lora_status_get(b.sets[0].ws),
         "config": config_dict(config, b.rows, world, b.small),
     }

@@ -91,7 +91,8 @@ enum {
     LORA_PATH_AUTO = 0, /* by row count: CUDA-core GEMV for few rows, tensor cores otherwise */
     LORA_PATH_SIMT = 1, /* CUDA-core GEMV path (any row count; slow for many rows) */
     LORA_PATH_TC = 2,   /* tcgen05 tensor-core path: a routing kernel, then the projection kernel
-                           (from 2048 rows a tensor-core shrink kernel before it) */
+                           (which also runs the shrink: CUDA-core units below 2048 rows,
+                           tensor-core tiles of 128 rows from 2048) */
     LORA_PATH_TC_ONE = 3 /* batches of up to 256 rows in one launch: routing, shrink, base, expand
                             and the split-K sum in a single kernel (other shapes, or a device that
                             cannot hold its grid, take LORA_PATH_TC). Measured slower than

@@ -15,9 +15,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "librank_delta.so")
-SOURCES = ["lora_api.cu", "lora_prep.cu", "lora_simt.cu", "lora_tc.cu", "lora_shrink_tc.cu", "lora_embed.cu", "lora_act.cu", "lora_gather.cu",
+SOURCES = ["lora_api.cu", "lora_prep.cu", "lora_simt.cu", "lora_tc.cu", "lora_embed.cu", "lora_act.cu", "lora_gather.cu",
            "lora_static_ws.cu", "lora_dec.cu"]
-HEADERS = ["lora_internal.cuh", "ptx.cuh", "shrink.cuh", "vec.cuh"]
+HEADERS = ["lora_internal.cuh", "ptx.cuh", "shrink.cuh", "shrink_tc.cuh", "vec.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

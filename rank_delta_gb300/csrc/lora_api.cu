@@ -698,6 +698,7 @@ lora_status carve_ws(void *ws, size_t ws_bytes, int rows, int nb, int R, int kp,
     out.tiles = reinterpret_cast<int32_t *>(b + l.tiles);
     out.part = reinterpret_cast<float *>(b + l.part);
     out.tile_cnt = reinterpret_cast<int32_t *>(b + l.tile_cnt);
+    out.stile = reinterpret_cast<int32_t *>(b + l.stile);
     return LORA_OK;
 }
 
@@ -760,20 +761,19 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
                           (uint32_t)plan.tn);
         if (!ok)
             return fail(LORA_ERR_CUDA, "%s: encoding the x tensor map failed", who);
-        if (!moe && p.rows >= TC_SHRINK_MIN_ROWS) {
-            // h from the tensor-core shrink kernel: whole K, one part, no work units
-            CUtensorMap xm;
-            if (!make_map(&xm, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64, 128))
+        if (p.stc_tiles > 0) {
+            // h from the launch's own tensor-core shrink tiles: whole K, one
+            // part, no work units; x in 128-row boxes
+            if (!make_map(&maps.sx, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64, 128))
                 return fail(LORA_ERR_CUDA, "%s: encoding the x tensor map of the shrink failed", who);
             // the pool's A rows by TMA (one box of R rows per slot and chunk) when
-            // R is a multiple of 16 (the kernel's rows per slot)
-            CUtensorMap am;
-            const bool a_ok = p.pool != nullptr && p.R % 16 == 0 && p.R <= 256 &&
-                              make_map_pool_rows(&am, p.pool, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.L,
-                                                 (uint64_t)p.slot_bytes, (uint32_t)p.R);
-            e = launch_shrink_tc(p, xm, a_ok ? &am : nullptr, di.num_sms, st);
-            if (e != cudaSuccess)
-                return cuda_fail(e, who);
+            // R is a multiple of 16 (the shrink's rows per slot)
+            p.stc_rs = (p.R + 15) & ~15;
+            p.stc_amap = (p.pool != nullptr && p.R % 16 == 0 && p.R <= 256 &&
+                          make_map_pool_rows(&maps.sa, p.pool, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.L,
+                                             (uint64_t)p.slot_bytes, (uint32_t)p.R))
+                             ? 1
+                             : 0;
         }
         for (int q = 0; q < p.E; ++q) {
             if (p.gated)
@@ -954,8 +954,9 @@ lora_status proj_apply(const void *x, int64_t x_stride, const void *W, int M, in
         path = LORA_PATH_TC;
     }
     if (path == LORA_PATH_TC && M >= TC_SHRINK_MIN_ROWS) {
-        p.kp = 1; // the tensor-core shrink writes h over the whole K
+        p.kp = 1; // the tensor-core shrink tiles write h over the whole K
         p.no_units = 1;
+        p.stc_tiles = (M + 127) / 128;
     }
     return run(p, path, reinterpret_cast<cudaStream_t>(stream), who);
 }
@@ -1444,7 +1445,7 @@ lora_status lora_proj_plan(int M, const lora_route *rt, int gated, int path, lor
         info->kernels = 1;
     } else {
         info->path = LORA_PLAN_TC;
-        info->kernels = (M >= TC_SHRINK_MIN_ROWS ? 3 : 2) + (gated && !fused_act ? 1 : 0);
+        info->kernels = 2 + (gated && !fused_act ? 1 : 0);
     }
     return ok();
 }

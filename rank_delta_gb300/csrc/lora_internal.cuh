@@ -56,10 +56,11 @@ struct Ws {
     int32_t *unit_off;  // [nb + 1] first shrink unit of each bucket
     int32_t *done;      // [nb] finished shrink units per bucket
     float *h;           // [kp][rows][R] partial A_s x_i of every adapted row (fp32)
-    uint16_t *hs;       // [rows][R] bf16 of (s * comp[r]) * h, written by the tensor-core shrink
+    uint16_t *hs;       // [rows][R] bf16 of (s * comp[r]) * h, written by the tensor-core shrink tiles
     int32_t *tiles;     // [1 + 3*max_tiles]: count, then (expert, first row, rows) per token tile
     float *part;        // [tiles][csplit][tn][128] split-K partial tiles (fp32)
     int32_t *tile_cnt;  // [tiles] split-K parts written so far (zeroed by prep)
+    int32_t *stile;     // [ceil(rows / 128)] shrink tiles of the projection launch published (zeroed by prep)
 };
 
 // Everything a launch needs except tensor maps.
@@ -77,20 +78,23 @@ struct Params {
     int tn;   // token tile of the tensor-core path (rows per tile)
     int kp;   // K parts of a shrink unit (h is summed over them)
     int ncnt; // split-K tile counters the prep kernel clears
-    int no_units; // 1: h comes from the tensor-core shrink kernel (no shrink work units)
+    int no_units; // 1: h comes from the tensor-core shrink tiles (no shrink work units)
     int max_tiles; // token tiles the routing kernel may list (0: the workspace bound)
     int ystore_ok; // 1: maps.y is encoded (y 16-byte aligned, y_stride a multiple of 8)
     const void *pool;  // the route's pool (A of slot s at pool + s * slot_bytes when packed there)
     size_t slot_bytes;
     int gated, I;  // 1: W is the fused [gate I | up I] (N = 2I) read as tiles of 64 gate + 64 up rows,
                    // and y receives act = silu(g) * u, [rows][I] (one K part, TMA stores only)
+    int stc_tiles; // shrink tiles (128 rows) the projection launch runs itself (no_units), else 0
+    int stc_rs;    // their max rank rounded up to 16
+    int stc_amap;  // 1: maps.sa covers the route's pool (A rows by TMA)
     const uint16_t *W[MAX_E];
     Tables tab[MAX_E];
     Ws ws;
 };
 
 struct WsLayout {
-    size_t status, perm, seg_off, unit_off, done, h, hs, tiles, part, tile_cnt, total;
+    size_t status, perm, seg_off, unit_off, done, h, hs, tiles, part, tile_cnt, stile, total;
 };
 
 // Status words at the start of a workspace: [0] LORA_FLAG_* bits, [1] the
@@ -137,6 +141,7 @@ inline WsLayout ws_layout(int rows, int nb, int R, int kp, size_t part_elems = 0
     l.tiles = o;    o = align256(o + sizeof(int32_t) * (1 + 3 * (size_t)max_token_tiles(rows, nb)));
     l.part = o;     o = align256(o + sizeof(float) * part_elems);
     l.tile_cnt = o; o = align256(o + sizeof(int32_t) * (size_t)ncnt);
+    l.stile = o;    o = align256(o + sizeof(int32_t) * (size_t)((rows + 127) / 128));
     l.total = o;
     return l;
 }
@@ -145,7 +150,9 @@ inline WsLayout ws_layout(int rows, int nb, int R, int kp, size_t part_elems = 0
 struct TmapSet {
     CUtensorMap x;
     CUtensorMap w[MAX_E];
-    CUtensorMap y; // boxes of 128 features x YSTORE_ROWS rows of y, no swizzle (when ystore_ok)
+    CUtensorMap y;  // boxes of 128 features x YSTORE_ROWS rows of y, no swizzle (when ystore_ok)
+    CUtensorMap sx; // the shrink tiles' x: boxes of 64 x 128 rows (when stc_tiles > 0)
+    CUtensorMap sa; // the pool's A rows: boxes of 64 x Rs rows x one slot (when stc_amap)
 };
 // Rows of one TMA store of the tensor-core epilogue.
 constexpr int YSTORE_ROWS = 64;
@@ -175,13 +182,9 @@ inline cudaError_t raise_smem_limit(std::atomic<uint64_t> &done, F *fn, int byte
 cudaError_t launch_prep(const Params &p, cudaStream_t st);
 cudaError_t launch_shrink(const Params &p, int num_sms, cudaStream_t st);
 cudaError_t launch_simt(const Params &p, int num_sms, cudaStream_t st);
-// Tensor-core shrink (lora_shrink_tc.cu); xmap: x with 64 x 128 boxes.
-// amap: the pool's A rows in boxes of round16(R) rows x 64 k (one copy per
-// slot and K chunk), or nullptr (every A row by cp.async through a_table).
-cudaError_t launch_shrink_tc(const Params &p, const CUtensorMap &xmap, const CUtensorMap *amap, int num_sms,
-                             cudaStream_t st);
-// Rows from which a projection call computes h with the tensor-core shrink
-// kernel (one CTA per 128 rows: enough tiles to spread over the SMs).
+// Rows from which a projection call computes h with tensor-core shrink tiles
+// of 128 rows inside the projection launch (enough tiles to spread over the
+// SMs; below, CUDA-core shrink units).
 constexpr int TC_SHRINK_MIN_ROWS = 2048;
 // Shape of one tensor-core launch: token tile, 64-wide K chunks per pipeline
 // stage, stages, K parts, whether the 3D tensor-map view (K a multiple of 64)

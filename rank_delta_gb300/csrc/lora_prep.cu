@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1) prep_kernel(Params p)
         brank[b] = rk;
         p.ws.done[b] = 0;
     }
+    for (int q = tid; q < p.stc_tiles; q += PREP_THREADS)
+        p.ws.stile[q] = 0;
     for (int q = tid; q < p.ncnt; q += PREP_THREADS)
         p.ws.tile_cnt[q] = 0;
     __syncthreads();

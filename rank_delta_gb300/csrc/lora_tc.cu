@@ -50,23 +50,29 @@
 //                an [m, n_out] scratch).
 // The shrink is handed over inside the launch: a unit bumps its bucket's
 // counter after writing h; the epilogue waits (bounded) for the counters of
-// the slots it stages. The grid never exceeds the SM count (one CTA per SM)
-// and launches with such waits are cooperative, so every unit and every K
-// part runs while others wait (a grid that cannot be resident at once fails
-// to launch).
+// the slots it stages. From 2048 rows the shrink runs on the tensor cores in
+// tiles of 128 rows (shrink_tc.cuh), as the first work of the CTAs that have
+// one item fewer; a tile bumps its own counter once h and s * h are written,
+// and the epilogue waits for the tiles of its rows. The grid never exceeds
+// the SM count (one CTA per SM) and launches with such waits are
+// cooperative, so every unit, tile and K part runs while others wait (a grid
+// that cannot be resident at once fails to launch).
 //
 // The kernel starts before the routing/prep kernel has finished (programmatic
 // dependent launch); only the roles that read its results wait for it.
 //
 // MoE (spark_model `lora_delta.rs`, `LoraKernels`: the down_proj fold keyed on
 // expert_offsets): token tiles come from the prep kernel's per-expert list and
-// W from that expert's tensor map.
+// W from that expert's tensor map; tiles of at least 128 rows run as pairs of
+// adjacent feature tiles (two W boxes per x box, one K loop into both
+// accumulators).
 //
 // Every wait is bounded; on a timeout the CTA records LORA_FLAG_WAIT_TIMEOUT,
 // stops issuing work, lets its own copies land, frees TMEM and exits.
 #include "lora_internal.cuh"
 #include "ptx.cuh"
 #include "shrink.cuh"
+#include "shrink_tc.cuh"
 #include "vec.cuh"
 
 namespace rd {
@@ -101,6 +107,7 @@ struct TcCfg {
                       //    both W boxes and one x box per stage, one K loop into both accumulators
     uint32_t xb_off, xh_off, aux_off, meta_off, red_off, umeta_off, bar_off, smem_bytes;
     uint32_t tmem_cols;
+    int stc_stages;   // pipeline stages of the launch's shrink tiles (below bar_off), 0: none
 };
 
 // Per-item state of the epilogue warps (shared memory at aux_off) and the
@@ -603,7 +610,7 @@ __device__ __forceinline__ void stage_h(const Params &p, const TcCfg &c, const E
         // ranks r (multiples of 8, r < rank) of this slot that fall in the pass
         const int rlo = max(0, r0k - ko), rhi = min(rk, r0k + kt - ko);
         if (c.hl == 1 && p.no_units) {
-            // the tensor-core shrink wrote this operand already rounded to
+            // the tensor-core shrink tiles wrote this operand already rounded to
             // bf16 (ws.hs, zero past the rank): copy it in 16-byte chunks
             const uint16_t *hsrow = p.ws.hs + (size_t)(ti.r0 + j) * p.R;
             for (int r = rlo + 8 * sub; r < rhi; r += 8 * tpc) {
@@ -1003,6 +1010,11 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
                     if (!wait_bucket(p, b, unit_off))
                         flag_abort(p, bars);
                 }
+                // or the launch's shrink tiles of these rows
+                if (p.stc_tiles > 0)
+                    for (int t = ti.r0 / STC_M + et; t <= (ti.r0 + ti.cnt - 1) / STC_M; t += EPI_THREADS)
+                        if (!stc_wait_tile(p, t))
+                            flag_abort(p, bars);
                 named_bar_sync(1, EPI_THREADS);
                 if (aborted(bars)) {
                     cp_async_wait_all();
@@ -1311,6 +1323,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
+    // the shrink tiles of this CTA (batches from 2048 rows), before its items:
+    // they publish h for the epilogues of every CTA
+    const StcArgs sa{p.stc_tiles, p.stc_rs, p.stc_amap, c.stc_stages};
+    const bool stc_wrote = p.stc_tiles > 0 && stc_phase(maps.sx, maps.sa, p, sa, smem, tmem);
+
     if (warp == 0) {
         if (lane == 0)
             produce(maps, p, c, bars, smem);
@@ -1320,6 +1337,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     } else if (warp < 4) {
         if (c.local_route)
             shrink_warps(p, c, smem);
+        else if (stc_wrote && warp == 2 && lane == 0)
+            stc_publish(p, sa);
     } else {
         epilogue(maps, p, c, bars, smem, tmem);
         tc_fence_before();
@@ -1385,6 +1404,16 @@ static TcCfg make_cfg(const Params &p, const TcPlan &plan, bool dyn)
     c.bar_off = align_up(o, 16);
     c.smem_bytes = 1024u + c.bar_off + (uint32_t)sizeof(Bars);
     c.tmem_cols = c.borrow ? 512u : pow2_at_least(3u * (uint32_t)c.tn);
+    // the launch's shrink tiles: stages below this kernel's barriers, 256 TMEM columns
+    c.stc_stages = 0;
+    if (p.stc_tiles > 0) {
+        int s = STC_MAX_STAGES;
+        while (s > 2 && stc_smem_bytes(s) > c.bar_off)
+            --s;
+        c.stc_stages = s;
+        if (c.tmem_cols < (uint32_t)STC_MAX_N)
+            c.tmem_cols = STC_MAX_N;
+    }
     // region 1: XB blocks then XH blocks (hl planes) carved from the stages
     c.xblk_b = (int)min(8u, (uint32_t)c.stages * c.stage_bytes / (XB_BLOCK + (uint32_t)c.hl * (uint32_t)c.tn * 128u));
     const int tt = (p.rows + c.tn - 1) / c.tn;
@@ -1527,7 +1556,7 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
     cudaError_t ea = raise_smem_limit(raised, tc_kernel, (int)SMEM_LIMIT);
     if (ea != cudaSuccess)
         return ea;
-    if (c.smem_bytes > SMEM_LIMIT)
+    if (c.smem_bytes > SMEM_LIMIT || (p.stc_tiles > 0 && stc_smem_bytes(c.stc_stages) > c.bar_off))
         return cudaErrorInvalidConfiguration;
     // One CTA per SM at most (the in-launch waits need every CTA resident; the
     // cooperative launch below makes sure they are); never more CTAs than work
@@ -1542,7 +1571,7 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
     // at once or the launch fails -- never a wait on a CTA that has not
     // started. Launches without such waits (one K part, h from the shrink
     // kernel) stay plain, so they start beside the kernel before them.
-    const bool waits = c.csplit > 1 || !p.no_units;
+    const bool waits = c.csplit > 1 || !p.no_units || p.stc_tiles > 0;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;

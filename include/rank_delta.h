@@ -563,8 +563,9 @@ lora_status lora_proj_plan(int M, const lora_route *rt, int gated, int path, lor
  * wait runs out: the call then returns with LORA_FLAG_WAIT_TIMEOUT in its
  * status word and y holding the base product without the delta. The same
  * setting covers the tensor-core kernel's split-K wait (LORA_PATH_TC with K
- * parts): every tile's wait for its parts runs out, the call returns with
- * LORA_FLAG_WAIT_TIMEOUT and y is not written. Nothing faults or hangs.
+ * parts) and, from 2048 rows, its wait for the launch's shrink tiles: those
+ * waits run out, the call returns with LORA_FLAG_WAIT_TIMEOUT and y is not
+ * (fully) written. Nothing faults or hangs.
  * wait_ns = 0 restores normal operation. Process-wide; for tests only.
  */
 void lora_test_wait_hook(uint64_t wait_ns, int extra_flags);

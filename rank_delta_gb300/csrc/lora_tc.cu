@@ -100,8 +100,8 @@ struct TcCfg {
     int borrow;       // 1: no room for D' beside two accumulators; D' borrows the other one
     int local_route;  // 1: one token tile holds every row; each CTA sorts them itself for the shrink
     int ystore;       // y boxes staged in the XH buffers: 0 = per-thread stores, else 1 or 2 buffers
-    uint64_t wait_ns; // limit of the split-K wait (the test hook shortens it)
-    int extra_parts;  // test hook: parts the split-K wait also waits for, that never come
+    uint64_t wait_ns; // limit of the split-K and shrink-tile waits (the test hook shortens it)
+    int extra_parts;  // test hook: parts (or tile publications) those waits also wait for, that never come
     uint32_t x_chunk, stage_bytes;
     int pair;         // 1: a CTA takes items in pairs (adjacent feature tiles of one token tile),
                       //    both W boxes and one x box per stage, one K loop into both accumulators
@@ -1013,7 +1013,7 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
                 // or the launch's shrink tiles of these rows
                 if (p.stc_tiles > 0)
                     for (int t = ti.r0 / STC_M + et; t <= (ti.r0 + ti.cnt - 1) / STC_M; t += EPI_THREADS)
-                        if (!stc_wait_tile(p, t))
+                        if (!stc_wait_tile(p, t, 1 + c.extra_parts, c.wait_ns))
                             flag_abort(p, bars);
                 named_bar_sync(1, EPI_THREADS);
                 if (aborted(bars)) {

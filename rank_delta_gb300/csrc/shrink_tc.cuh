@@ -358,17 +358,18 @@ __device__ __forceinline__ void stc_publish(const Params &p, const StcArgs &a)
         atomicAdd(p.ws.stile + tile, 1);
 }
 
-// Wait until shrink tile t has been published; false after ~1 s.
-__device__ __forceinline__ bool stc_wait_tile(const Params &p, int t)
+// Wait until shrink tile t has been published (its counter reaches target,
+// 1 but under the test hook); false after wait_ns.
+__device__ __forceinline__ bool stc_wait_tile(const Params &p, int t, int target, uint64_t wait_ns)
 {
     const int32_t *cnt = p.ws.stile + t;
-    if (ld_acquire_gpu(cnt) >= 1)
+    if (ld_acquire_gpu(cnt) >= target)
         return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (ld_acquire_gpu(cnt) >= 1)
+        if (ld_acquire_gpu(cnt) >= target)
             return true;
-        if (globaltimer_ns() - t0 > WAIT_NS)
+        if (globaltimer_ns() - t0 > wait_ns)
             return false;
     }
 }

@@ -68,3 +68,27 @@ def test_split_k_wait_runs_out_then_the_next_call_is_correct():
     y = run.apply(path=tc)
     assert run.last_status == 0, f"the next call reports {run.last_status:#x}"
     assert_close(y, oracle.workload_proj(run.wl), "decode after a timed-out split-K wait")
+
+
+def test_shrink_tile_wait_runs_out_then_the_next_call_is_correct():
+    """From 2048 rows the projection launch computes h in tensor-core shrink
+    tiles of 128 rows and the epilogue waits (bounded) for the tiles of its
+    rows before staging s * h; with the hook that wait also counts a
+    publication that never comes, so it runs out: the call returns with
+    LORA_FLAG_WAIT_TIMEOUT, and the next normal call on the same workspace is
+    correct and clean."""
+    wl = workloads.random_small(seed=2150, M=2100, K=200, N=136, L=5, R=24)
+    run = ProjRun(wl)
+    tc = rd.LORA_PATH_TC
+    run.apply(path=tc)
+    assert run.last_status == 0
+    rd.lora_test_wait_hook(200_000, 1)
+    try:
+        run.apply(path=tc)
+        flags = run.last_status
+    finally:
+        rd.lora_test_wait_hook(0, 0)
+    assert flags & rd.LORA_FLAG_WAIT_TIMEOUT, f"status {flags:#x}"
+    y = run.apply(path=tc)
+    assert run.last_status == 0, f"the next call reports {run.last_status:#x}"
+    assert_close(y, oracle.workload_proj(wl), "2100 rows after a timed-out shrink-tile wait")

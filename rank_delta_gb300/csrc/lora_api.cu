@@ -752,6 +752,8 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
         const TcPlan plan = plan_tc(p, moe);
         TmapSet maps;
         memset(&maps, 0, sizeof maps);
+        StcMaps sm;
+        memset(&sm, 0, sizeof sm);
         bool ok;
         if (plan.use3d)
             ok = make_map_3d(&maps.x, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride,
@@ -764,13 +766,13 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
         if (p.stc_tiles > 0) {
             // h from the launch's own tensor-core shrink tiles: whole K, one
             // part, no work units; x in 128-row boxes
-            if (!make_map(&maps.sx, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64, 128))
+            if (!make_map(&sm.sx, p.x, (uint64_t)p.K, (uint64_t)p.rows, (uint64_t)p.x_stride, 64, 128))
                 return fail(LORA_ERR_CUDA, "%s: encoding the x tensor map of the shrink failed", who);
             // the pool's A rows by TMA (one box of R rows per slot and chunk) when
             // R is a multiple of 16 (the shrink's rows per slot)
             p.stc_rs = (p.R + 15) & ~15;
             p.stc_amap = (p.pool != nullptr && p.R % 16 == 0 && p.R <= 256 &&
-                          make_map_pool_rows(&maps.sa, p.pool, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.L,
+                          make_map_pool_rows(&sm.sa, p.pool, (uint64_t)p.K, (uint64_t)p.R, (uint64_t)p.L,
                                              (uint64_t)p.slot_bytes, (uint32_t)p.R))
                              ? 1
                              : 0;
@@ -803,7 +805,7 @@ lora_status run(Params &p, int path, cudaStream_t st, const char *who)
         // with one K part the gated drain writes act only through these boxes
         if (p.gated && !p.ystore_ok && plan.csplit == 1)
             return fail(LORA_ERR_CUDA, "%s: encoding the act tensor map failed", who);
-        e = launch_tc(p, maps, plan, di.num_sms, st);
+        e = launch_tc(p, maps, sm, plan, di.num_sms, st);
     }
     if (e != cudaSuccess)
         return cuda_fail(e, who);

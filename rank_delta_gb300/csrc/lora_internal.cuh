@@ -85,12 +85,12 @@ struct Params {
     size_t slot_bytes;
     int gated, I;  // 1: W is the fused [gate I | up I] (N = 2I) read as tiles of 64 gate + 64 up rows,
                    // and y receives act = silu(g) * u, [rows][I] (one K part, TMA stores only)
-    int stc_tiles; // shrink tiles (128 rows) the projection launch runs itself (no_units), else 0
-    int stc_rs;    // their max rank rounded up to 16
-    int stc_amap;  // 1: maps.sa covers the route's pool (A rows by TMA)
     const uint16_t *W[MAX_E];
     Tables tab[MAX_E];
     Ws ws;
+    int stc_tiles; // shrink tiles (128 rows) the projection launch runs itself (no_units), else 0
+    int stc_rs;    // their max rank rounded up to 16
+    int stc_amap;  // 1: the shrink's A map covers the route's pool (A rows by TMA)
 };
 
 struct WsLayout {
@@ -151,7 +151,12 @@ struct TmapSet {
     CUtensorMap x;
     CUtensorMap w[MAX_E];
     CUtensorMap y;  // boxes of 128 features x YSTORE_ROWS rows of y, no swizzle (when ystore_ok)
-    CUtensorMap sx; // the shrink tiles' x: boxes of 64 x 128 rows (when stc_tiles > 0)
+};
+
+// Tensor maps of the shrink tiles of a launch (stc_tiles > 0), passed only to
+// the kernel instantiation that runs them.
+struct StcMaps {
+    CUtensorMap sx; // x: boxes of 64 x 128 rows
     CUtensorMap sa; // the pool's A rows: boxes of 64 x Rs rows x one slot (when stc_amap)
 };
 // Rows of one TMA store of the tensor-core epilogue.
@@ -196,7 +201,7 @@ struct TcPlan {
     int hl;   // planes of the staged s * h: 1 (bf16) or 2 (bf16 hi + lo)
 };
 TcPlan plan_tc(const Params &p, bool per_expert_tiles);
-cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, int num_sms,
+cudaError_t launch_tc(const Params &p, const TmapSet &maps, const StcMaps &sm, const TcPlan &plan, int num_sms,
                       cudaStream_t st);
 cudaError_t launch_table_set(const lora_route &rt, int slot, const void *a, const void *b,
                              int rank, float factor, float scale, cudaStream_t st);

@@ -718,6 +718,7 @@ __device__ __forceinline__ void shrink_warps(const Params &p, const TcCfg &c, ui
 // them); then drain the accumulator (adding D' to those columns only), and
 // with csplit > 1 write the partial tile and, once every part is in, sum this
 // part's share of the columns in part order.
+template <bool kStc>
 __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, const TcCfg &c, Bars *bars,
                                          uint8_t *smem, uint32_t tmem)
 {
@@ -1011,7 +1012,7 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
                         flag_abort(p, bars);
                 }
                 // or the launch's shrink tiles of these rows
-                if (p.stc_tiles > 0)
+                if (kStc && p.stc_tiles > 0)
                     for (int t = ti.r0 / STC_M + et; t <= (ti.r0 + ti.cnt - 1) / STC_M; t += EPI_THREADS)
                         if (!stc_wait_tile(p, t, 1 + c.extra_parts, c.wait_ns))
                             flag_abort(p, bars);
@@ -1266,9 +1267,21 @@ __device__ __forceinline__ void epilogue(const TmapSet &maps, const Params &p, c
         bulk_wait_all(); // the y stores have landed
 }
 
+// The shrink tiles' maps as a kernel argument: present only in the
+// instantiation that runs them.
+template <bool kStc> struct StcMapsArg {
+    StcMaps m;
+};
+template <> struct StcMapsArg<false> {
+    int none;
+};
+
+// kStc: the launch runs shrink tiles (a separate instantiation, so the
+// launches without them keep the smaller code and arguments of the other).
+template <bool kStc>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     tc_kernel(const __grid_constant__ TmapSet maps, const __grid_constant__ Params p,
-              const __grid_constant__ TcCfg c)
+              const __grid_constant__ TcCfg c, const __grid_constant__ StcMapsArg<kStc> sm)
 {
     extern __shared__ uint8_t tc_smem_raw[];
     uint8_t *smem = align1024(tc_smem_raw);
@@ -1326,7 +1339,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // the shrink tiles of this CTA (batches from 2048 rows), before its items:
     // they publish h for the epilogues of every CTA
     const StcArgs sa{p.stc_tiles, p.stc_rs, p.stc_amap, c.stc_stages};
-    const bool stc_wrote = p.stc_tiles > 0 && stc_phase(maps.sx, maps.sa, p, sa, smem, tmem);
+    bool stc_wrote = false;
+    if constexpr (kStc)
+        stc_wrote = p.stc_tiles > 0 && stc_phase(sm.m.sx, sm.m.sa, p, sa, smem, tmem);
 
     if (warp == 0) {
         if (lane == 0)
@@ -1340,7 +1355,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         else if (stc_wrote && warp == 2 && lane == 0)
             stc_publish(p, sa);
     } else {
-        epilogue(maps, p, c, bars, smem, tmem);
+        epilogue<kStc>(maps, p, c, bars, smem, tmem);
         tc_fence_before();
         mbar_arrive(&bars->epi_done);
     }
@@ -1544,7 +1559,7 @@ bool tc_gated_ok(const Params &p)
            xh_bytes >= (uint32_t)c.ystore * YSTORE_ROWS * 64u * 2u + 16u * EPI_THREADS * 2u;
 }
 
-cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, int num_sms,
+cudaError_t launch_tc(const Params &p, const TmapSet &maps, const StcMaps &stc_maps, const TcPlan &plan, int num_sms,
                       cudaStream_t st)
 {
     const bool dyn = p.expert_offsets != nullptr;
@@ -1552,11 +1567,13 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
     uint64_t tw = 0;
     test_hook_get(tw, c.extra_parts);
     c.wait_ns = tw ? tw : WAIT_NS;
-    static std::atomic<uint64_t> raised{0};
-    cudaError_t ea = raise_smem_limit(raised, tc_kernel, (int)SMEM_LIMIT);
+    static std::atomic<uint64_t> raised{0}, raised_stc{0};
+    const bool stc = p.stc_tiles > 0;
+    cudaError_t ea = stc ? raise_smem_limit(raised_stc, tc_kernel<true>, (int)SMEM_LIMIT)
+                         : raise_smem_limit(raised, tc_kernel<false>, (int)SMEM_LIMIT);
     if (ea != cudaSuccess)
         return ea;
-    if (c.smem_bytes > SMEM_LIMIT || (p.stc_tiles > 0 && stc_smem_bytes(c.stc_stages) > c.bar_off))
+    if (c.smem_bytes > SMEM_LIMIT || (stc && stc_smem_bytes(c.stc_stages) > c.bar_off))
         return cudaErrorInvalidConfiguration;
     // One CTA per SM at most (the in-launch waits need every CTA resident; the
     // cooperative launch below makes sure they are); never more CTAs than work
@@ -1584,7 +1601,12 @@ cudaError_t launch_tc(const Params &p, const TmapSet &maps, const TcPlan &plan, 
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, tc_kernel, maps, p, c);
+    if (stc) {
+        StcMapsArg<true> a;
+        a.m = stc_maps;
+        return cudaLaunchKernelEx(&cfg, tc_kernel<true>, maps, p, c, a);
+    }
+    return cudaLaunchKernelEx(&cfg, tc_kernel<false>, maps, p, c, StcMapsArg<false>{0});
 }
 
 } // namespace rd

@@ -182,7 +182,8 @@ def test_alpha_zero_and_rslora_scales_on_gpu():
 @pytest.mark.parametrize("M,K,N,L,R", [(2100, 200, 136, 5, 24), (2048, 320, 128, 40, 16),
                                        (4096, 128, 64, 3, 64)])
 def test_large_batch_tensor_core_shrink(M, K, N, L, R):
-    """From 2048 rows h comes from the tensor-core shrink kernel: ragged row
+    """From 2048 rows h comes from the tensor-core shrink tiles inside the
+    projection launch: ragged row
     tiles, K not a multiple of 64, a pool rank that is not a multiple of 16,
     and tiles holding more slots than one UMMA group (16 slots of rank 16)."""
     wl = workloads.random_small(seed=M + K + L, M=M, K=K, N=N, L=L, R=R)

@@ -134,7 +134,8 @@ def test_stack_with_every_scale_zero_is_an_empty_slot(stack64):
 
 
 def test_stack_large_batch_tensor_core_shrink():
-    """From 2048 rows h comes from the tensor-core shrink kernel."""
+    """From 2048 rows h comes from the tensor-core shrink tiles inside the
+    projection launch."""
     wl = workloads.stacked(seed=8, M=2048, K=512, N=384, L=6, R=64)
     run = StackRun(wl)
     y = run.apply()

@@ -201,6 +201,25 @@ def test_small_moe_matches_oracle_everywhere():
     assert_close(y, oracle.workload_moe(wl), "small moe")
 
 
+@pytest.mark.parametrize("n_adapters,rank", [(4, 16), (8, 32)])
+def test_paired_moe_tiles_match_oracle_everywhere(n_adapters, rank):
+    """Per-expert tiles of 128 rows or more run as feature-tile pairs (two W
+    boxes per x box, one K loop into both accumulators). With 64 feature
+    tiles most CTAs take two pairs, and the second waits for both
+    accumulators of the first; with 8 adapters of rank 32 a tile's expand
+    takes several rounds, so the pair's second tile stages its own s * h
+    instead of reusing the first one's."""
+    wl = workloads.synth.moe(seed=20 + rank, tokens=512, E=8, top_k=2, K=1024, N=8192,
+                             n_adapters=n_adapters, rank=rank)
+    run = MoeRun(wl)
+    y = run.apply()
+    assert run.last_status == 0
+    assert_close(y, oracle.workload_moe(wl), f"paired moe, {n_adapters} adapters of rank {rank}")
+    base = run.apply(slots=torch.full_like(run.slots, -1))
+    none = wl.seq_slot < 0
+    assert np.array_equal(y[none], base[none])
+
+
 def test_moe_bad_offsets_are_flagged():
     wl = workloads.synth.moe(seed=10, tokens=32, E=3, top_k=2, K=64, N=64, n_adapters=2, rank=8)
     run = MoeRun(wl)

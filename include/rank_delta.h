@@ -366,8 +366,13 @@ lora_status lora_proj_apply_static_ws(const void *x, int64_t x_stride, const voi
  *          workspace followed by its [M][2I] bf16 output
  * The projection is lora_proj_apply (every row rule and the status word
  * included: lora_status_get(ws) reads it); the halves are rounded to bf16,
- * then silu(g) * u is formed in fp32 and rounded once to bf16. Errors: those
- * of lora_proj_apply, a route whose n_out is not 2I, act_stride < I.
+ * then silu(g) * u is formed in fp32 and rounded once to bf16. On the
+ * tensor-core path, with K and I multiples of 64 and act rows 16-byte
+ * aligned, act is formed inside the projection launch -- in its drain
+ * (batches of several token tiles) or its split-K sum (decode sizes) -- and
+ * the [M][2I] output is not written; other shapes run the projection, then
+ * a separate activation pass. Errors: those of lora_proj_apply, a route
+ * whose n_out is not 2I, act_stride < I.
  */
 size_t lora_gate_up_workspace_bytes(int M, const lora_route *rt);
 /* The workspace of lora_gate_up_apply_ex on `path` (the projection's part
@@ -381,7 +386,9 @@ lora_status lora_gate_up_apply(const void *x, int64_t x_stride, const void *W, i
  * LORA_PATH_TC_ONE takes batches of 17..256 rows with K and I multiples of
  * 64 through the one-launch kernel, whose split-K sum writes act directly
  * (silu(g) * u of the bf16-rounded halves, rounded once: the same rule);
- * every other case runs the projection on that path, then the act pass. */
+ * LORA_PATH_TC (and AUTO beyond 16 rows) forms act inside the projection
+ * launch where lora_gate_up_apply says; every other case runs the projection
+ * on that path, then the act pass. */
 lora_status lora_gate_up_apply_ex(const void *x, int64_t x_stride, const void *W, int M, int K,
                                   int I, const int32_t *seq_slot, const lora_route *rt, void *act,
                                   int64_t act_stride, void *ws, size_t ws_bytes, int path,
@@ -530,7 +537,8 @@ lora_status lora_status_get(const void *ws, uint32_t *flags, lora_stream_t strea
  * device (lora_proj_plan; the pages have no counterpart: a diagnostic). */
 enum {
     LORA_PLAN_SIMT = 1,        /* <= 16 rows: CUDA-core GEMV (routing, shrink, GEMV launches) */
-    LORA_PLAN_TC = 2,          /* routing launch, then tensor-core launches */
+    LORA_PLAN_TC = 2,          /* routing launch, then one tensor-core launch (and the act pass
+                                  of gated shapes that cannot form act in it) */
     LORA_PLAN_ONE_LAUNCH = 3   /* <= 256 rows: everything in one clustered tensor-core launch */
 };
 typedef struct lora_plan_info {
